@@ -1,0 +1,204 @@
+"""Python wrapper of the C oracle (``oracle/moe_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: the plain fp64 CPU definition of the MoE FFN layer
+forward that the CUDA library is checked against.  Only the test suite, the
+smoke check and the benchmark's CPU-baseline leg use it; the product path never
+imports it.  It shares no code with the CUDA library.
+
+Inputs are torch CPU tensors (bf16 / fp32 / int32) or numpy arrays; outputs are
+numpy arrays.  The shared library is compiled on first use (``build()``).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Dict, Optional, Sequence, Tuple
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_LIB = os.path.join(_HERE, "libmoe_oracle.so")
+_lib = None
+
+GATE_TOPK_SOFTMAX = 0
+GATE_SOFTMAX_TOPK = 1
+GATE_SOFTMAX_TOPK_RENORM = 2
+GATE_SIGMOID_BIAS_RENORM = 3
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/libmoe_oracle.so`` (gcc, OpenMP).
+
+    ``-ffp-contract=off`` keeps every multiply and add separately rounded, so
+    the oracle gives the same bits on x86-64 and aarch64."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fopenmp", "-fPIC",
+                               "-shared", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P, I64, I32, D = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
+        lib.oracle_router_logits.argtypes = [P, P, I64, I64, I64, P, I32]
+        lib.oracle_router_logits.restype = None
+        lib.oracle_topk_gating.argtypes = [P, P, I64, I64, I64, I32, P, P, P]
+        lib.oracle_topk_gating.restype = I32
+        lib.oracle_dispatch.argtypes = [P, I64, I64, I64, P, P, P, P]
+        lib.oracle_dispatch.restype = I32
+        lib.oracle_imbalance.argtypes = [P, I64, I64, P, P]
+        lib.oracle_imbalance.restype = None
+        lib.oracle_expert_ffn.argtypes = [P, P, P, I64, I64, P]
+        lib.oracle_expert_ffn.restype = None
+        lib.oracle_layer_tokens.argtypes = [P, I64, I64, I64, P, P, P, P, P, P, P, I64, P, I32]
+        lib.oracle_layer_tokens.restype = None
+        lib.oracle_max_threads.argtypes = []
+        lib.oracle_max_threads.restype = I32
+        _lib = lib
+    return _lib
+
+
+def _u16(t) -> np.ndarray:
+    """bf16 torch tensor (or uint16/int16 numpy array) -> contiguous uint16 array."""
+    if isinstance(t, torch.Tensor):
+        assert t.dtype == torch.bfloat16, t.dtype
+        return np.ascontiguousarray(t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+    a = np.asarray(t)
+    assert a.dtype in (np.uint16, np.int16)
+    return np.ascontiguousarray(a.view(np.uint16))
+
+
+def _np(t, dtype) -> np.ndarray:
+    if isinstance(t, torch.Tensor):
+        t = t.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(t, dtype=dtype))
+
+
+def _p(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def router_logits(x, w_router, nthreads: int = 0) -> np.ndarray:
+    """float32 logits s[T,E] (exact double dot product rounded once)."""
+    xa = _u16(x)
+    wr = _np(w_router, np.float32)
+    T, H = xa.shape
+    E = wr.shape[0]
+    assert wr.shape[1] == H
+    s = np.empty((T, E), dtype=np.float32)
+    _load().oracle_router_logits(_p(xa), _p(wr), T, H, E, _p(s), nthreads or max_threads())
+    return s
+
+
+def topk_gating(s, k: int, mode: int, sel_bias=None) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """(ids[T,k] int32, w[T,k] float64, gap[T] float64) from float32 logits."""
+    sa = _np(s, np.float32)
+    T, E = sa.shape
+    b = None if sel_bias is None else _np(sel_bias, np.float32)
+    ids = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float64)
+    gap = np.empty((T,), dtype=np.float64)
+    rc = _load().oracle_topk_gating(_p(sa), None if b is None else _p(b), T, E, k, mode,
+                                     _p(ids), _p(w), _p(gap))
+    if rc != 0:
+        raise ValueError("oracle_topk_gating: bad arguments")
+    return ids, w, gap
+
+
+def dispatch(ids, E: int):
+    """(counts[E], offsets[E+1], perm_src[T*k], inv_pos[T*k]) int32."""
+    ia = _np(ids, np.int32)
+    T, k = ia.shape if ia.ndim == 2 else (ia.shape[0], 1)
+    counts = np.empty((E,), dtype=np.int32)
+    offsets = np.empty((E + 1,), dtype=np.int32)
+    perm_src = np.empty((T * k,), dtype=np.int32)
+    inv_pos = np.empty((T * k,), dtype=np.int32)
+    rc = _load().oracle_dispatch(_p(ia), T, k, E, _p(counts), _p(offsets), _p(perm_src), _p(inv_pos))
+    if rc != 0:
+        raise ValueError("oracle_dispatch: expert id out of range")
+    return counts, offsets, perm_src, inv_pos
+
+
+def imbalance(counts, n_assign: int) -> Tuple[int, int]:
+    """Imbalance ratio max_e n_e / (N_a/E) as an exact fraction (num, den)."""
+    c = _np(counts, np.int32)
+    num = ctypes.c_int64()
+    den = ctypes.c_int64()
+    _load().oracle_imbalance(_p(c), c.shape[0], n_assign, ctypes.byref(num), ctypes.byref(den))
+    return int(num.value), int(den.value)
+
+
+def expert_ffn(x_row, w13_e, w2_e) -> np.ndarray:
+    xa, g, d = _u16(x_row), _u16(w13_e), _u16(w2_e)
+    H = xa.shape[-1]
+    I = g.shape[0] // 2
+    out = np.empty((H,), dtype=np.float64)
+    _load().oracle_expert_ffn(_p(xa), _p(g), _p(d), H, I, _p(out))
+    return out
+
+
+def layer_tokens(x, ids, w, w13, w2, tokens: Sequence[int], w13_shared=None, w2_shared=None,
+                 nthreads: int = 0) -> np.ndarray:
+    """y[n,H] (float64) for token indices ``tokens``.
+
+    ``w13``/``w2`` are [E,2I,H]/[E,H,I] bf16 tensors or dicts {expert: block}
+    holding at least the experts the listed tokens select."""
+    xa = _u16(x)
+    T, H = xa.shape
+    ia = _np(ids, np.int32)
+    wa = _np(w, np.float64)
+    k = ia.shape[1]
+    toks = np.ascontiguousarray(np.asarray(tokens, dtype=np.int64))
+    need = sorted({int(e) for e in ia[toks].reshape(-1)}) if len(toks) else []
+    if isinstance(w13, dict):
+        E = max(max(w13.keys()) + 1, int(ia.max()) + 1)
+        blocks13 = {e: _u16(w13[e]) for e in need}
+        blocks2 = {e: _u16(w2[e]) for e in need}
+    else:
+        E = w13.shape[0]
+        blocks13 = {e: _u16(w13[e]) for e in need}
+        blocks2 = {e: _u16(w2[e]) for e in need}
+    some = next(iter(blocks13.values())) if blocks13 else None
+    I = (some.shape[0] // 2) if some is not None else (_u16(w13_shared).shape[0] // 2)
+    p13 = (ctypes.c_void_p * E)()
+    p2 = (ctypes.c_void_p * E)()
+    for e in need:
+        p13[e] = _p(blocks13[e])
+        p2[e] = _p(blocks2[e])
+    s13 = None if w13_shared is None else _u16(w13_shared)
+    s2 = None if w2_shared is None else _u16(w2_shared)
+    y = np.empty((len(toks), H), dtype=np.float64)
+    _load().oracle_layer_tokens(_p(xa), H, I, k, _p(ia), _p(wa), p13, p2,
+                                None if s13 is None else _p(s13), None if s2 is None else _p(s2),
+                                _p(toks), len(toks), _p(y), nthreads or max_threads())
+    return y
+
+
+def route(inputs, nthreads: int = 0) -> Dict[str, np.ndarray]:
+    """Router + gating of a ``synth.LayerInputs`` batch: logits, ids, w, gap."""
+    s = router_logits(inputs.x, inputs.w_router, nthreads)
+    ids, w, gap = topk_gating(s, inputs.cfg.k, inputs.cfg.gating, inputs.sel_bias)
+    return {"logits": s, "ids": ids, "w": w, "gap": gap}
+
+
+def layer(inputs, tokens: Optional[Sequence[int]] = None, nthreads: int = 0):
+    """Full layer forward of a ``synth.LayerInputs`` batch (optionally only some
+    tokens' outputs).  Returns (y[n,H] float64, routing dict)."""
+    r = route(inputs, nthreads)
+    if tokens is None:
+        tokens = range(inputs.T)
+    y = layer_tokens(inputs.x, r["ids"], r["w"], inputs.w13, inputs.w2, list(tokens),
+                     inputs.w13_shared, inputs.w2_shared, nthreads)
+    return y, r
