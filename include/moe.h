@@ -1,0 +1,258 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) forward pass of one Mixture-of-Experts
+ * FFN layer: router, top-k gating, count / prefix-sum / permute dispatch,
+ * grouped SwiGLU expert GEMMs over ragged per-expert row counts, and the
+ * inverse permutation with the gate-weighted sum.
+ *
+ *   y = sum_{i in top-k(r(x))} g_i(x) * FFN_i(x)
+ *       (Moebius reading notes, "MoE（混合专家）架构回顾", eq. (1))
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers are DEVICE pointers (memory of the current CUDA device) unless a
+ *   comment says otherwise.  The caller owns every buffer; the library never
+ *   allocates, frees, synchronises or copies to the host inside a compute
+ *   call.  All compute calls are asynchronous on `stream`.
+ * - Tensors are dense and row-major; `bf16` is IEEE bfloat16 stored as
+ *   uint16_t.  Every device pointer must be 16-byte aligned.
+ * - Shapes: T tokens, H hidden size, E routed experts, k experts per token,
+ *   I expert intermediate size.  Limits: 1 <= T <= 2^20, 1 <= k <= min(E, 32),
+ *   1 <= E <= 512, T*k <= 2^24, 64 <= H <= 16384 and H % 64 == 0,
+ *   64 <= I <= 32768 and I % 64 == 0.
+ * - Errors: arguments are validated on the host before anything is launched;
+ *   a bad argument returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED_SHAPE /
+ *   MOE_ERR_WORKSPACE_TOO_SMALL and launches nothing.  A failed launch returns
+ *   MOE_ERR_CUDA.  Conditions only the device can see (an expert id out of
+ *   range, a pipeline wait that ran out of time) are latched in a status word
+ *   at the start of the workspace and read with moe_get_device_status(); the
+ *   kernels never trap.
+ * - Workspace: one caller-allocated device buffer of moe_workspace_size(desc)
+ *   bytes (256-byte aligned) serves every call made with that descriptor;
+ *   initialise its status word once with moe_workspace_init().  Calls that
+ *   share a workspace must be ordered on one stream.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *moe_stream_t; /* identical to cudaStream_t */
+typedef struct CUevent_st *moe_event_t;   /* identical to cudaEvent_t  */
+
+typedef int32_t moe_status_t;
+enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,         /* NULL / misaligned pointer, bad enum        */
+  MOE_ERR_UNSUPPORTED_SHAPE = -2,   /* a size outside the limits above            */
+  MOE_ERR_WORKSPACE_TOO_SMALL = -3, /* ws_bytes < moe_workspace_size(desc)        */
+  MOE_ERR_CUDA = -4,                /* a CUDA runtime / launch error              */
+  MOE_ERR_DEVICE_CHECK = -5,        /* device saw invalid metadata (expert id)    */
+  MOE_ERR_TIMEOUT = -6,             /* a bounded device pipeline wait ran out     */
+  MOE_ERR_UNSUPPORTED_DEVICE = -7   /* current device is not compute capability 10.3 */
+};
+
+/*
+ * Gating variants (CS349D lecture 8 notes, section 1.2 "MoE 层的结构"):
+ *  TOPK_SOFTMAX          keep the k largest logits, softmax over them; the k
+ *                        weights sum to 1 (Shazeer, Mixtral).
+ *  SOFTMAX_TOPK          softmax over all E logits, keep the k largest
+ *                        probabilities without renormalising; sum < 1
+ *                        (DeepSeek-V2).
+ *  SOFTMAX_TOPK_RENORM   as SOFTMAX_TOPK, divided by the sum of the kept k
+ *                        (Qwen3 layers); equal to TOPK_SOFTMAX in exact
+ *                        arithmetic, since softmax keeps the order.
+ *  SIGMOID_BIAS_RENORM   affinity a = sigmoid(s); select the k largest of
+ *                        a + b with a per-expert bias b that only changes the
+ *                        selection; weight a_i / sum of selected a
+ *                        (DeepSeek-V3).
+ * Selection is decided on float32 keys; equal keys go to the lower expert
+ * index; slot j of a token is its j-th best expert.
+ */
+enum {
+  MOE_GATE_TOPK_SOFTMAX = 0,
+  MOE_GATE_SOFTMAX_TOPK = 1,
+  MOE_GATE_SOFTMAX_TOPK_RENORM = 2,
+  MOE_GATE_SIGMOID_BIAS_RENORM = 3
+};
+
+/* Layer shape.  has_shared_expert adds one expert every token passes through
+ * with weight 1 (CS349D lecture 8 notes, section 1.2, "专家的粒度": 256 routed
+ * experts plus 1 shared expert). */
+typedef struct {
+  int32_t T, H, E, k, I;
+  int32_t gating;            /* MOE_GATE_* */
+  int32_t has_shared_expert; /* 0 or 1 */
+} moe_layer_desc_t;
+
+/* Layer weights (device, read-only, owned by the caller).
+ *  w_router   [E,H] fp32, router s = W_r x ("MoE推理优化全景指南",
+ *             "从 Dense FFN 到专家集合").
+ *  sel_bias   [E] fp32 selection-only bias; required for
+ *             SIGMOID_BIAS_RENORM, ignored (may be NULL) otherwise.
+ *  w13        [E,2I,H] bf16: rows [0,I) gate projection, rows [I,2I) up
+ *             projection of each expert's SwiGLU MLP (Moebius reading notes,
+ *             eq. (2); Moebius paper, "Weights Resharding").
+ *  w2         [E,H,I] bf16 down projection.
+ *  w13_shared [2I,H] bf16 and w2_shared [H,I] bf16: the shared expert;
+ *             required iff has_shared_expert. */
+typedef struct {
+  const float *w_router;
+  const float *sel_bias;
+  const void *w13;
+  const void *w2;
+  const void *w13_shared;
+  const void *w2_shared;
+} moe_layer_weights_t;
+
+/* Byte offsets (from the workspace base) of the buffers moe_layer_forward
+ * leaves in the workspace, for inspection after the stream has synchronised.
+ * R = T*k + (has_shared_expert ? T : 0) permuted rows. */
+typedef struct {
+  size_t status;       /* int32 status word                             */
+  size_t logits;       /* [T,E] fp32 router logits                       */
+  size_t topk_ids;     /* [T,k] int32                                    */
+  size_t topk_w;       /* [T,k] fp32 gate weights                        */
+  size_t gap;          /* [T] fp32 top-k boundary gap                     */
+  size_t counts;       /* [E] int32                                      */
+  size_t offsets;      /* [E+1] int32                                    */
+  size_t perm_src;     /* [T*k] int32                                    */
+  size_t inv_pos;      /* [T*k] int32                                    */
+  size_t w_perm;       /* [T*k] fp32 gate weight in permuted order        */
+  size_t x_perm;       /* [R,H] bf16 tokens grouped by expert             */
+  size_t h;            /* [R,I] bf16 SiLU(gate)*up                        */
+  size_t out_perm;     /* [R,H] bf16 gate-weighted expert outputs         */
+  size_t total;        /* == moe_workspace_size(desc)                     */
+} moe_workspace_layout_t;
+
+/* Number of events moe_layer_forward records when given an event array:
+ * before routing, after routing, after dispatch, after the gather, after the
+ * gate/up GEMM, after the down GEMM, after the combine. */
+#define MOE_STAGE_EVENTS 7
+
+/* ----------------------------------------------------------------- host -- */
+
+/* Workspace bytes every call below needs for this descriptor (worst case over
+ * all routings).  Host only; 0 if the descriptor is invalid. */
+size_t moe_workspace_size(const moe_layer_desc_t *d);
+
+/* Fill *out with the workspace layout of this descriptor.  Host only. */
+moe_status_t moe_workspace_layout(const moe_layer_desc_t *d, moe_workspace_layout_t *out);
+
+/* Clear the workspace's status word (async on stream).  Call once after
+ * allocating a workspace. */
+moe_status_t moe_workspace_init(void *workspace, size_t ws_bytes, moe_stream_t stream);
+
+/* Synchronise `stream`, read the status word, optionally clear it.  Returns
+ * MOE_OK, MOE_ERR_DEVICE_CHECK or MOE_ERR_TIMEOUT (device conditions latched
+ * since the last clear) or MOE_ERR_CUDA.  *raw (may be NULL) receives the
+ * status bits. */
+moe_status_t moe_get_device_status(void *workspace, size_t ws_bytes, moe_stream_t stream,
+                                   int32_t clear, int32_t *raw);
+
+/* Static text for a status code. */
+const char *moe_status_string(moe_status_t s);
+
+/* ------------------------------------------------------------ compute -- */
+
+/*
+ * moe_route -- router and top-k gating.
+ * Router s = W_r x ("MoE推理优化全景指南", section "从 Dense FFN 到专家集合");
+ * top-k and gate weights per the variant d->gating (CS349D lecture 8 notes,
+ * section 1.2).
+ *   x            [T,H] bf16 hidden states
+ *   w_router     [E,H] fp32;  sel_bias [E] fp32 (SIGMOID_BIAS_RENORM only)
+ *   logits       [T,E] fp32 out: router logits, fp32 FMA accumulation
+ *   topk_ids     [T,k] int32 out, topk_w [T,k] fp32 out (slot order: best first)
+ *   boundary_gap [T] fp32 out or NULL: selection key of the k-th best expert
+ *                minus that of the (k+1)-th (0 when k == E); gaps below 1e-5
+ *                mark near-ties whose selection rounding can decide.
+ * Uses the workspace's router scratch.
+ */
+moe_status_t moe_route(const moe_layer_desc_t *d, const void *x, const float *w_router,
+                       const float *sel_bias, float *logits, int32_t *topk_ids, float *topk_w,
+                       float *boundary_gap, void *workspace, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_build_dispatch -- count / prefix sum / permute by expert
+ * ("MoE推理优化全景指南", section "Dispatch 并不是一次普通 all-to-all":
+ * histogram, each expert's offset from the prefix sum, tokens permuted into
+ * contiguous per-expert segments).
+ *   topk_ids  [T,k] int32 in; assignment a = t*k + j
+ *   topk_w    [T,k] fp32 in or NULL
+ *   counts    [E] int32 out: assignments per expert
+ *   offsets   [E+1] int32 out: offsets[e] = sum of counts[<e], offsets[E] = T*k
+ *   perm_src  [T*k] int32 out: position p -> assignment a; expert e owns
+ *             positions [offsets[e], offsets[e+1]) in ascending token order
+ *   inv_pos   [T*k] int32 out: assignment a -> position p (inverse of perm_src)
+ *   w_perm    [T*k] fp32 out or NULL: topk_w in permuted order (needs topk_w)
+ * Bit-exact and deterministic (no atomics decide positions).  An id outside
+ * [0,E) latches MOE_ERR_DEVICE_CHECK in the status word; its assignment is
+ * dropped from the layout, and the outputs are then not meaningful.
+ */
+moe_status_t moe_build_dispatch(const moe_layer_desc_t *d, const int32_t *topk_ids,
+                                const float *topk_w, int32_t *counts, int32_t *offsets,
+                                int32_t *perm_src, int32_t *inv_pos, float *w_perm,
+                                void *workspace, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_grouped_swiglu_ffn -- the experts' SwiGLU FFNs as grouped GEMMs over the
+ * ragged per-expert row counts ("MoE推理优化全景指南", section
+ * "Expert GEMM 为什么经常不够大": one scheduled GEMM over [m_i, hidden] @ W_i
+ * for all experts; expert shapes from Moebius reading notes eq. (2)).
+ *   h_p      = SiLU(W_gate,e x_t) * (W_up,e x_t)      (gate/up GEMM + epilogue)
+ *   out_p    = w_perm[p] * (W_down,e h_p)              (down GEMM + epilogue)
+ * for every position p of expert e's segment, x_t the token at p.
+ *   x            [T,H] bf16
+ *   perm_src     [T*k] int32, offsets [E+1] int32 (from moe_build_dispatch)
+ *   w_perm       [T*k] fp32 or NULL (NULL: unweighted outputs)
+ *   w13, w2      routed expert weights; w13_shared / w2_shared required iff
+ *                d->has_shared_expert (run as one more segment of all T tokens
+ *                with weight 1, stored in rows [T*k, T*k+T) of out_perm)
+ *   out_perm     [R,H] bf16 out, R = T*k + (shared ? T : 0)
+ * Uses the workspace for x_perm, h and the tile plan.  Experts with no rows
+ * read no weights.
+ */
+moe_status_t moe_grouped_swiglu_ffn(const moe_layer_desc_t *d, const void *x,
+                                    const int32_t *perm_src, const int32_t *offsets,
+                                    const float *w_perm, const void *w13, const void *w2,
+                                    const void *w13_shared, const void *w2_shared,
+                                    void *out_perm, void *workspace, size_t ws_bytes,
+                                    moe_stream_t stream);
+
+/*
+ * moe_combine -- inverse permutation and gate-weighted sum
+ * ("MoE推理优化全景指南", section "一个 token 为什么要跨 GPU", last step
+ * "inverse permutation + weighted sum", and section "Dispatch 并不是一次普通
+ * all-to-all": restore the original token order and apply the routing weights).
+ *   y[t,:] = sum_j wt(t,j) * out_perm[inv_pos[t*k+j],:]  (+ out_perm[T*k+t,:]
+ *            when d->has_shared_expert)
+ *   wt(t,j) = topk_w[t*k+j], or 1 when topk_w is NULL (weights already applied
+ *            by moe_grouped_swiglu_ffn)
+ *   y        [T,H] bf16 out; sums in fp32 in slot order.
+ */
+moe_status_t moe_combine(const moe_layer_desc_t *d, const void *out_perm, const int32_t *inv_pos,
+                         const float *topk_w, void *y, moe_stream_t stream);
+
+/*
+ * moe_layer_forward -- the whole layer (Moebius reading notes eq. (1)): route,
+ * dispatch, grouped SwiGLU FFN with the gate weights applied in the down-GEMM
+ * epilogue, combine.  One stream, no host synchronisation; intermediates stay
+ * in the workspace (moe_workspace_layout).
+ *   x [T,H] bf16 in, y [T,H] bf16 out.
+ *   stage_events: NULL, or MOE_STAGE_EVENTS cudaEvent_t handles recorded on
+ *   `stream` at the stage boundaries (for per-stage timing).
+ */
+moe_status_t moe_layer_forward(const moe_layer_desc_t *d, const moe_layer_weights_t *w,
+                               const void *x, void *y, void *workspace, size_t ws_bytes,
+                               moe_stream_t stream, moe_event_t const *stage_events);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

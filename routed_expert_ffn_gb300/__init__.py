@@ -1,0 +1,232 @@
+"""Python binding of the sm_103a MoE FFN layer library (``libmoe_gb300.so``).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels.  Functions carry the C ABI's names (``include/moe.h``) and take torch
+CUDA tensors (or raw device pointers as ints); streams default to torch's
+current stream.  There is no CPU fallback: if the library is missing, every
+call raises ``LibraryNotBuilt``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional, Sequence
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = -1
+MOE_ERR_UNSUPPORTED_SHAPE = -2
+MOE_ERR_WORKSPACE_TOO_SMALL = -3
+MOE_ERR_CUDA = -4
+MOE_ERR_DEVICE_CHECK = -5
+MOE_ERR_TIMEOUT = -6
+MOE_ERR_UNSUPPORTED_DEVICE = -7
+
+MOE_GATE_TOPK_SOFTMAX = 0
+MOE_GATE_SOFTMAX_TOPK = 1
+MOE_GATE_SOFTMAX_TOPK_RENORM = 2
+MOE_GATE_SIGMOID_BIAS_RENORM = 3
+
+MOE_STAGE_EVENTS = 7
+STAGE_NAMES = ("route", "dispatch", "gather", "gateup", "down", "combine")
+
+
+class LibraryNotBuilt(ImportError):
+    pass
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {status} ({moe_status_string(status)})")
+
+
+class LayerDesc(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("k", ctypes.c_int32), ("I", ctypes.c_int32), ("gating", ctypes.c_int32),
+                ("has_shared_expert", ctypes.c_int32)]
+
+
+class LayerWeights(ctypes.Structure):
+    _fields_ = [("w_router", ctypes.c_void_p), ("sel_bias", ctypes.c_void_p),
+                ("w13", ctypes.c_void_p), ("w2", ctypes.c_void_p),
+                ("w13_shared", ctypes.c_void_p), ("w2_shared", ctypes.c_void_p)]
+
+
+_LAYOUT_FIELDS = ("status", "logits", "topk_ids", "topk_w", "gap", "counts", "offsets",
+                  "perm_src", "inv_pos", "w_perm", "x_perm", "h", "out_perm", "total")
+
+
+class WorkspaceLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in _LAYOUT_FIELDS]
+
+
+_lib = None
+
+
+def library() -> ctypes.CDLL:
+    """The loaded CUDA library (raises LibraryNotBuilt if it is missing)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise LibraryNotBuilt(f"{LIB_PATH} is missing: build it with "
+                              "`python -m routed_expert_ffn_gb300.build` (there is no CPU fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, S, I32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32
+    D = ctypes.POINTER(LayerDesc)
+    sig = {
+        "moe_workspace_size": ([D], S),
+        "moe_workspace_layout": ([D, ctypes.POINTER(WorkspaceLayout)], I32),
+        "moe_workspace_init": ([P, S, P], I32),
+        "moe_get_device_status": ([P, S, P, I32, ctypes.POINTER(I32)], I32),
+        "moe_status_string": ([I32], ctypes.c_char_p),
+        "moe_route": ([D, P, P, P, P, P, P, P, P, S, P], I32),
+        "moe_build_dispatch": ([D, P, P, P, P, P, P, P, P, S, P], I32),
+        "moe_grouped_swiglu_ffn": ([D, P, P, P, P, P, P, P, P, P, P, S, P], I32),
+        "moe_combine": ([D, P, P, P, P, P], I32),
+        "moe_layer_forward": ([D, ctypes.POINTER(LayerWeights), P, P, P, S, P, P], I32),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    _lib = lib
+    return lib
+
+
+# ---------------------------------------------------------------- helpers --
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, st: int):
+    if st != MOE_OK:
+        raise MoeError(fn, st)
+
+
+def desc(T: int, H: int, E: int, k: int, I: int, gating: int, shared: bool = False) -> LayerDesc:
+    return LayerDesc(T, H, E, k, I, gating, 1 if shared else 0)
+
+
+# ---------------------------------------------------------------- host API --
+
+def moe_status_string(status: int) -> str:
+    return library().moe_status_string(status).decode()
+
+
+def moe_workspace_size(d: LayerDesc) -> int:
+    return int(library().moe_workspace_size(ctypes.byref(d)))
+
+
+def moe_workspace_layout(d: LayerDesc) -> Dict[str, int]:
+    out = WorkspaceLayout()
+    _check("moe_workspace_layout", library().moe_workspace_layout(ctypes.byref(d), ctypes.byref(out)))
+    return {n: int(getattr(out, n)) for n in _LAYOUT_FIELDS}
+
+
+def alloc_workspace(d: LayerDesc, device="cuda"):
+    """A zero-initialised workspace tensor (uint8) of moe_workspace_size(d) bytes."""
+    import torch
+    n = moe_workspace_size(d)
+    if n == 0:
+        raise MoeError("moe_workspace_size", MOE_ERR_UNSUPPORTED_SHAPE)
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    moe_workspace_init(ws)
+    return ws
+
+
+def moe_workspace_init(ws, stream=None):
+    _check("moe_workspace_init", library().moe_workspace_init(_ptr(ws), _nbytes(ws), _stream(stream)))
+
+
+def moe_get_device_status(ws, clear: bool = True, stream=None):
+    """(status, raw bits) of the workspace's device status word (synchronises)."""
+    raw = ctypes.c_int32(0)
+    st = library().moe_get_device_status(_ptr(ws), _nbytes(ws), _stream(stream), 1 if clear else 0,
+                                         ctypes.byref(raw))
+    return int(st), int(raw.value)
+
+
+# ------------------------------------------------------------- compute API --
+
+def moe_route(d: LayerDesc, x, w_router, sel_bias, logits, topk_ids, topk_w, boundary_gap, ws,
+              stream=None):
+    _check("moe_route", library().moe_route(
+        ctypes.byref(d), _ptr(x), _ptr(w_router), _ptr(sel_bias), _ptr(logits), _ptr(topk_ids),
+        _ptr(topk_w), _ptr(boundary_gap), _ptr(ws), _nbytes(ws), _stream(stream)))
+
+
+def moe_build_dispatch(d: LayerDesc, topk_ids, topk_w, counts, offsets, perm_src, inv_pos, w_perm,
+                       ws, stream=None):
+    _check("moe_build_dispatch", library().moe_build_dispatch(
+        ctypes.byref(d), _ptr(topk_ids), _ptr(topk_w), _ptr(counts), _ptr(offsets), _ptr(perm_src),
+        _ptr(inv_pos), _ptr(w_perm), _ptr(ws), _nbytes(ws), _stream(stream)))
+
+
+def moe_grouped_swiglu_ffn(d: LayerDesc, x, perm_src, offsets, w_perm, w13, w2, w13_shared,
+                           w2_shared, out_perm, ws, stream=None):
+    _check("moe_grouped_swiglu_ffn", library().moe_grouped_swiglu_ffn(
+        ctypes.byref(d), _ptr(x), _ptr(perm_src), _ptr(offsets), _ptr(w_perm), _ptr(w13), _ptr(w2),
+        _ptr(w13_shared), _ptr(w2_shared), _ptr(out_perm), _ptr(ws), _nbytes(ws), _stream(stream)))
+
+
+def moe_combine(d: LayerDesc, out_perm, inv_pos, topk_w, y, stream=None):
+    _check("moe_combine", library().moe_combine(
+        ctypes.byref(d), _ptr(out_perm), _ptr(inv_pos), _ptr(topk_w), _ptr(y), _stream(stream)))
+
+
+def layer_weights(w_router, w13, w2, sel_bias=None, w13_shared=None, w2_shared=None) -> LayerWeights:
+    return LayerWeights(_ptr(w_router), _ptr(sel_bias), _ptr(w13), _ptr(w2), _ptr(w13_shared),
+                        _ptr(w2_shared))
+
+
+def moe_layer_forward(d: LayerDesc, w: LayerWeights, x, y, ws, stream=None,
+                      stage_events: Optional[Sequence] = None):
+    """Whole layer forward.  ``stage_events``: None or MOE_STAGE_EVENTS torch.cuda.Event
+    objects (created with enable_timing and already recorded once) or raw handles."""
+    ev = None
+    if stage_events is not None:
+        if len(stage_events) != MOE_STAGE_EVENTS:
+            raise ValueError(f"need {MOE_STAGE_EVENTS} events")
+        ev = (ctypes.c_void_p * MOE_STAGE_EVENTS)(
+            *[e if isinstance(e, int) else e.cuda_event for e in stage_events])
+    _check("moe_layer_forward", library().moe_layer_forward(
+        ctypes.byref(d), ctypes.byref(w), _ptr(x), _ptr(y), _ptr(ws), _nbytes(ws), _stream(stream),
+        ev))
+
+
+def workspace_view(ws, layout: Dict[str, int], name: str, dtype, shape):
+    """A tensor view of one buffer moe_layer_forward leaves in the workspace."""
+    import torch
+    itemsize = torch.empty((), dtype=dtype).element_size()
+    n = 1
+    for s in shape:
+        n *= s
+    off = layout[name]
+    return ws[off:off + n * itemsize].view(dtype).view(*shape)

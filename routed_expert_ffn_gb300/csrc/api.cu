@@ -1,0 +1,333 @@
+// C ABI of the MoE FFN layer forward: argument validation, workspace layout,
+// the stage calls and the fused layer forward.  Declarations and the meaning
+// of every argument are in include/moe.h.
+#include <stdint.h>
+#include <string.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+int num_sms() {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 1;
+  }
+  return cache[dev];
+}
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+Layout make_layout(const moe_layer_desc_t &d) {
+  Layout L;
+  memset(&L, 0, sizeof L);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 1024);
+    return o;
+  };
+  const int64_t Na = (int64_t)d.T * d.k;
+  const int shared = d.has_shared_expert ? 1 : 0;
+  L.rows = Na + (shared ? d.T : 0);
+  L.nseg = d.E + shared;
+  L.route_splits = route_splits(d.T, d.E, d.H);
+  L.nblk = (int)((Na + kDispatchChunk - 1) / kDispatchChunk);
+  L.status = take(256);
+  L.route_part = take((size_t)L.route_splits * d.T * d.E * 4);
+  L.blk_counts = take((size_t)L.nblk * d.E * 4);
+  L.blk_base = take((size_t)L.nblk * d.E * 4);
+  L.plan = take((size_t)plan_ints(L.nseg) * 4);
+  L.logits = take((size_t)d.T * d.E * 4);
+  L.topk_ids = take((size_t)Na * 4);
+  L.topk_w = take((size_t)Na * 4);
+  L.gap = take((size_t)d.T * 4);
+  L.counts = take((size_t)d.E * 4);
+  L.offsets = take((size_t)(d.E + 1) * 4);
+  L.perm_src = take((size_t)Na * 4);
+  L.inv_pos = take((size_t)Na * 4);
+  L.w_perm = take((size_t)Na * 4);
+  L.x_perm = take((size_t)L.rows * d.H * 2);
+  L.h = take((size_t)L.rows * d.I * 2);
+  L.out_perm = take((size_t)L.rows * d.H * 2);
+  L.total = off;
+  return L;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+moe_status_t validate_desc(const moe_layer_desc_t *d) {
+  if (d == nullptr) return MOE_ERR_INVALID_ARG;
+  if (d->gating < MOE_GATE_TOPK_SOFTMAX || d->gating > MOE_GATE_SIGMOID_BIAS_RENORM)
+    return MOE_ERR_INVALID_ARG;
+  if (d->has_shared_expert != 0 && d->has_shared_expert != 1) return MOE_ERR_INVALID_ARG;
+  if (d->T < 1 || d->T > kMaxT) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (d->E < 1 || d->E > kMaxE) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (d->k < 1 || d->k > d->E || d->k > kMaxK) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((int64_t)d->T * d->k > kMaxAssign) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (d->H < 64 || d->H > 16384 || d->H % 64 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (d->I < 64 || d->I > 32768 || d->I % 64 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+bool ok_ptr(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool ok_opt(const void *p) { return p == nullptr || ok_ptr(p); }
+
+moe_status_t check_device() {
+  static int8_t state[64] = {};  // 0 unknown, 1 supported, -1 not
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  if (state[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    state[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  return state[dev] == 1 ? MOE_OK : MOE_ERR_UNSUPPORTED_DEVICE;
+}
+
+// Common prologue of the compute calls: descriptor and workspace (host only;
+// the device check comes after every argument has been validated).
+moe_status_t prologue(const moe_layer_desc_t *d, void *ws, size_t ws_bytes, Layout *L) {
+  moe_status_t st = validate_desc(d);
+  if (st != MOE_OK) return st;
+  if (ws != nullptr) {
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_INVALID_ARG;
+    *L = make_layout(*d);
+    if (ws_bytes < L->total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  }
+  return MOE_OK;
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+template <typename T>
+T *at(void *ws, size_t off) {
+  return reinterpret_cast<T *>(static_cast<uint8_t *>(ws) + off);
+}
+
+const __nv_bfloat16 *bf(const void *p) { return static_cast<const __nv_bfloat16 *>(p); }
+__nv_bfloat16 *bfw(void *p) { return static_cast<__nv_bfloat16 *>(p); }
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_workspace_size(const moe_layer_desc_t *d) {
+  if (validate_desc(d) != MOE_OK) return 0;
+  return make_layout(*d).total;
+}
+
+moe_status_t moe_workspace_layout(const moe_layer_desc_t *d, moe_workspace_layout_t *out) {
+  moe_status_t st = validate_desc(d);
+  if (st != MOE_OK) return st;
+  if (out == nullptr) return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(*d);
+  out->status = L.status;
+  out->logits = L.logits;
+  out->topk_ids = L.topk_ids;
+  out->topk_w = L.topk_w;
+  out->gap = L.gap;
+  out->counts = L.counts;
+  out->offsets = L.offsets;
+  out->perm_src = L.perm_src;
+  out->inv_pos = L.inv_pos;
+  out->w_perm = L.w_perm;
+  out->x_perm = L.x_perm;
+  out->h = L.h;
+  out->out_perm = L.out_perm;
+  out->total = L.total;
+  return MOE_OK;
+}
+
+moe_status_t moe_workspace_init(void *workspace, size_t ws_bytes, moe_stream_t stream) {
+  if (workspace == nullptr || ws_bytes < 256 ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(workspace, 0, 256, (cudaStream_t)stream));
+}
+
+moe_status_t moe_get_device_status(void *workspace, size_t ws_bytes, moe_stream_t stream,
+                                   int32_t clear, int32_t *raw) {
+  if (workspace == nullptr || ws_bytes < 256) return MOE_ERR_INVALID_ARG;
+  uint32_t word = 0;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(&word, workspace, sizeof word, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (clear) {
+    if (cudaMemsetAsync(workspace, 0, sizeof word, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (raw != nullptr) *raw = (int32_t)word;
+  if (word & (kStatusTimeoutGateUp | kStatusTimeoutDown)) return MOE_ERR_TIMEOUT;
+  if (word & (kStatusBadExpertId | kStatusBadOffsets)) return MOE_ERR_DEVICE_CHECK;
+  return MOE_OK;
+}
+
+const char *moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument (NULL or misaligned pointer, bad enum)";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "shape outside the supported limits";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than moe_workspace_size()";
+    case MOE_ERR_CUDA: return "CUDA runtime or launch error";
+    case MOE_ERR_DEVICE_CHECK: return "device check failed (expert id or offsets out of range)";
+    case MOE_ERR_TIMEOUT: return "a bounded device pipeline wait timed out";
+    case MOE_ERR_UNSUPPORTED_DEVICE: return "current device is not compute capability 10.3";
+    default: return "unknown status";
+  }
+}
+
+moe_status_t moe_route(const moe_layer_desc_t *d, const void *x, const float *w_router,
+                       const float *sel_bias, float *logits, int32_t *topk_ids, float *topk_w,
+                       float *boundary_gap, void *workspace, size_t ws_bytes,
+                       moe_stream_t stream) {
+  if (workspace == nullptr) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  moe_status_t st = prologue(d, workspace, ws_bytes, &L);
+  if (st != MOE_OK) return st;
+  if (!ok_ptr(x) || !ok_ptr(w_router) || !ok_ptr(logits) || !ok_ptr(topk_ids) || !ok_ptr(topk_w) ||
+      !ok_opt(boundary_gap))
+    return MOE_ERR_INVALID_ARG;
+  if (d->gating == MOE_GATE_SIGMOID_BIAS_RENORM && !ok_ptr(sel_bias)) return MOE_ERR_INVALID_ARG;
+  if ((st = check_device()) != MOE_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  float *part = at<float>(workspace, L.route_part);
+  cudaError_t e = launch_router_logits(bf(x), w_router, d->T, d->H, d->E, L.route_splits, part, s);
+  if (e == cudaSuccess)
+    e = launch_topk_gating(part, L.route_splits, sel_bias, d->T, d->E, d->k, d->gating, logits,
+                           topk_ids, topk_w, boundary_gap, s);
+  return cuda_status(e);
+}
+
+moe_status_t moe_build_dispatch(const moe_layer_desc_t *d, const int32_t *topk_ids,
+                                const float *topk_w, int32_t *counts, int32_t *offsets,
+                                int32_t *perm_src, int32_t *inv_pos, float *w_perm,
+                                void *workspace, size_t ws_bytes, moe_stream_t stream) {
+  if (workspace == nullptr) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  moe_status_t st = prologue(d, workspace, ws_bytes, &L);
+  if (st != MOE_OK) return st;
+  if (!ok_ptr(topk_ids) || !ok_ptr(counts) || !ok_ptr(offsets) || !ok_ptr(perm_src) ||
+      !ok_ptr(inv_pos) || !ok_opt(topk_w) || !ok_opt(w_perm))
+    return MOE_ERR_INVALID_ARG;
+  if (w_perm != nullptr && topk_w == nullptr) return MOE_ERR_INVALID_ARG;
+  if ((st = check_device()) != MOE_OK) return st;
+  cudaError_t e = launch_dispatch(topk_ids, topk_w, d->T, d->k, d->E,
+                                  at<int32_t>(workspace, L.blk_counts),
+                                  at<int32_t>(workspace, L.blk_base), counts, offsets, perm_src,
+                                  inv_pos, w_perm, at<uint32_t>(workspace, L.status),
+                                  (cudaStream_t)stream);
+  return cuda_status(e);
+}
+
+moe_status_t moe_grouped_swiglu_ffn(const moe_layer_desc_t *d, const void *x,
+                                    const int32_t *perm_src, const int32_t *offsets,
+                                    const float *w_perm, const void *w13, const void *w2,
+                                    const void *w13_shared, const void *w2_shared,
+                                    void *out_perm, void *workspace, size_t ws_bytes,
+                                    moe_stream_t stream) {
+  if (workspace == nullptr) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  moe_status_t st = prologue(d, workspace, ws_bytes, &L);
+  if (st != MOE_OK) return st;
+  if (!ok_ptr(x) || !ok_ptr(perm_src) || !ok_ptr(offsets) || !ok_opt(w_perm) || !ok_ptr(w13) ||
+      !ok_ptr(w2) || !ok_ptr(out_perm))
+    return MOE_ERR_INVALID_ARG;
+  if (d->has_shared_expert && (!ok_ptr(w13_shared) || !ok_ptr(w2_shared)))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = check_device()) != MOE_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t *status = at<uint32_t>(workspace, L.status);
+  int32_t *plan = at<int32_t>(workspace, L.plan);
+  __nv_bfloat16 *x_perm = at<__nv_bfloat16>(workspace, L.x_perm);
+  __nv_bfloat16 *h = at<__nv_bfloat16>(workspace, L.h);
+  cudaError_t e = launch_gather_plan(bf(x), perm_src, offsets, d->T, d->k, d->E, d->H, d->I,
+                                     d->has_shared_expert, x_perm, plan, status, s);
+  if (e == cudaSuccess) e = launch_expert_gateup(*d, w13, w13_shared, x_perm, plan, h, status, s);
+  if (e == cudaSuccess)
+    e = launch_expert_down(*d, w2, w2_shared, h, plan, w_perm, bfw(out_perm), status, s);
+  return cuda_status(e);
+}
+
+moe_status_t moe_combine(const moe_layer_desc_t *d, const void *out_perm, const int32_t *inv_pos,
+                         const float *topk_w, void *y, moe_stream_t stream) {
+  Layout L;
+  moe_status_t st = prologue(d, nullptr, 0, &L);
+  if (st != MOE_OK) return st;
+  if (!ok_ptr(out_perm) || !ok_ptr(inv_pos) || !ok_opt(topk_w) || !ok_ptr(y))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = check_device()) != MOE_OK) return st;
+  return cuda_status(launch_combine(bf(out_perm), inv_pos, topk_w, d->T, d->k, d->H,
+                                    d->has_shared_expert, bfw(y), (cudaStream_t)stream));
+}
+
+moe_status_t moe_layer_forward(const moe_layer_desc_t *d, const moe_layer_weights_t *w,
+                               const void *x, void *y, void *workspace, size_t ws_bytes,
+                               moe_stream_t stream, moe_event_t const *stage_events) {
+  if (workspace == nullptr || w == nullptr) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  moe_status_t st = prologue(d, workspace, ws_bytes, &L);
+  if (st != MOE_OK) return st;
+  if (!ok_ptr(x) || !ok_ptr(y) || !ok_ptr(w->w_router) || !ok_ptr(w->w13) || !ok_ptr(w->w2))
+    return MOE_ERR_INVALID_ARG;
+  if (d->gating == MOE_GATE_SIGMOID_BIAS_RENORM && !ok_ptr(w->sel_bias)) return MOE_ERR_INVALID_ARG;
+  if (d->has_shared_expert && (!ok_ptr(w->w13_shared) || !ok_ptr(w->w2_shared)))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = check_device()) != MOE_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  auto mark = [&](int i) -> cudaError_t {
+    return stage_events ? cudaEventRecord((cudaEvent_t)stage_events[i], s) : cudaSuccess;
+  };
+  uint32_t *status = at<uint32_t>(workspace, L.status);
+  float *logits = at<float>(workspace, L.logits);
+  int32_t *ids = at<int32_t>(workspace, L.topk_ids);
+  float *tw = at<float>(workspace, L.topk_w);
+  int32_t *offsets = at<int32_t>(workspace, L.offsets);
+  int32_t *perm_src = at<int32_t>(workspace, L.perm_src);
+  int32_t *inv_pos = at<int32_t>(workspace, L.inv_pos);
+  float *w_perm = at<float>(workspace, L.w_perm);
+  int32_t *plan = at<int32_t>(workspace, L.plan);
+  __nv_bfloat16 *x_perm = at<__nv_bfloat16>(workspace, L.x_perm);
+  __nv_bfloat16 *h = at<__nv_bfloat16>(workspace, L.h);
+  __nv_bfloat16 *out_perm = at<__nv_bfloat16>(workspace, L.out_perm);
+  float *part = at<float>(workspace, L.route_part);
+
+  cudaError_t e = mark(0);
+  if (e == cudaSuccess)
+    e = launch_router_logits(bf(x), w->w_router, d->T, d->H, d->E, L.route_splits, part, s);
+  if (e == cudaSuccess)
+    e = launch_topk_gating(part, L.route_splits, w->sel_bias, d->T, d->E, d->k, d->gating, logits,
+                           ids, tw, at<float>(workspace, L.gap), s);
+  if (e == cudaSuccess) e = mark(1);
+  if (e == cudaSuccess)
+    e = launch_dispatch(ids, tw, d->T, d->k, d->E, at<int32_t>(workspace, L.blk_counts),
+                        at<int32_t>(workspace, L.blk_base), at<int32_t>(workspace, L.counts),
+                        offsets, perm_src, inv_pos, w_perm, status, s);
+  if (e == cudaSuccess) e = mark(2);
+  if (e == cudaSuccess)
+    e = launch_gather_plan(bf(x), perm_src, offsets, d->T, d->k, d->E, d->H, d->I,
+                           d->has_shared_expert, x_perm, plan, status, s);
+  if (e == cudaSuccess) e = mark(3);
+  if (e == cudaSuccess) e = launch_expert_gateup(*d, w->w13, w->w13_shared, x_perm, plan, h, status, s);
+  if (e == cudaSuccess) e = mark(4);
+  if (e == cudaSuccess)
+    e = launch_expert_down(*d, w->w2, w->w2_shared, h, plan, w_perm, out_perm, status, s);
+  if (e == cudaSuccess) e = mark(5);
+  if (e == cudaSuccess)
+    e = launch_combine(out_perm, inv_pos, nullptr, d->T, d->k, d->H, d->has_shared_expert, bfw(y), s);
+  if (e == cudaSuccess) e = mark(6);
+  return cuda_status(e);
+}
+
+}  // extern "C"

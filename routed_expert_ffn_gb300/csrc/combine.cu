@@ -1,0 +1,63 @@
+// Inverse permutation and gate-weighted sum ("MoE推理优化全景指南", section
+// "一个 token 为什么要跨 GPU", last step of the data path, and section
+// "Dispatch 并不是一次普通 all-to-all": restore the original token order and
+// apply the routing weights):
+//
+//   y[t,:] = sum_j wt(t,j) * out_perm[inv_pos[t*k+j],:]  (+ out_perm[T*k+t,:])
+//
+// One thread per 16-byte vector of a token row; the k expert rows of a token
+// are gathered with 16-byte loads and summed in fp32 in slot order.
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+
+__global__ void __launch_bounds__(256)
+    combine_kernel(const __nv_bfloat16 *__restrict__ out_perm, const int32_t *__restrict__ inv_pos,
+                   const float *__restrict__ topk_w, int T, int k, int H, int shared,
+                   __nv_bfloat16 *__restrict__ y) {
+  const int t = blockIdx.x;
+  const int v = blockIdx.y * blockDim.x + threadIdx.x;
+  const int nv = H / 8;
+  if (v >= nv) return;
+  const int64_t Na = (int64_t)T * k;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  auto add_row = [&](int64_t row, float wt) {
+    const uint4 raw = reinterpret_cast<const uint4 *>(out_perm + row * H)[v];
+    const __nv_bfloat162 *p = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(p[i]);
+      acc[2 * i] = fmaf(wt, f.x, acc[2 * i]);
+      acc[2 * i + 1] = fmaf(wt, f.y, acc[2 * i + 1]);
+    }
+  };
+  for (int j = 0; j < k; ++j) {
+    const int64_t a = (int64_t)t * k + j;
+    const int32_t p = inv_pos[a];
+    if (p < 0 || p >= Na) continue;
+    add_row(p, topk_w != nullptr ? topk_w[a] : 1.0f);
+  }
+  if (shared) add_row(Na + t, 1.0f);
+  uint4 o;
+  __nv_bfloat162 *q = reinterpret_cast<__nv_bfloat162 *>(&o);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) q[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+  reinterpret_cast<uint4 *>(y + (int64_t)t * H)[v] = o;
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const __nv_bfloat16 *out_perm, const int32_t *inv_pos,
+                           const float *topk_w, int T, int k, int H, int shared, __nv_bfloat16 *y,
+                           cudaStream_t s) {
+  const int nv = H / 8;
+  dim3 grid(T, (nv + 255) / 256);
+  combine_kernel<<<grid, 256, 0, s>>>(out_perm, inv_pos, topk_w, T, k, H, shared, y);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,241 @@
+// Count / prefix sum / permute dispatch ("MoE推理优化全景指南", section
+// "Dispatch 并不是一次普通 all-to-all"), and the gather of the permuted token
+// rows plus the tile plan the grouped GEMMs read.
+//
+// The flat assignment list a = t*k + j is cut into blocks of kDispatchChunk:
+//   1. hist:    per-block expert histogram in shared memory (atomics only
+//               count; they never decide a position);
+//   2. scan:    one CTA sums the block histograms per expert, scans them into
+//               the expert offsets and gives every (block, expert) its base;
+//   3. scatter: each block re-reads its assignments in order and ranks them
+//               stably: __match_any_sync groups equal experts inside a warp,
+//               per-warp counts in shared memory order the warps, and a
+//               running per-expert base orders the block's sub-chunks.
+// The result is bit-exact: expert e owns positions [offsets[e], offsets[e+1])
+// in ascending assignment (hence token) order.
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kWarps = kDispatchThreads / 32;
+
+__global__ void __launch_bounds__(kDispatchThreads)
+    dispatch_hist_kernel(const int32_t *__restrict__ ids, int64_t Na, int E,
+                         int32_t *__restrict__ blk_counts, uint32_t *__restrict__ status) {
+  __shared__ int cnt[kMaxE];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  const int64_t beg = (int64_t)blockIdx.x * kDispatchChunk;
+  const int64_t end = min(Na, beg + kDispatchChunk);
+  bool bad = false;
+  for (int64_t a = beg + threadIdx.x; a < end; a += blockDim.x) {
+    const int e = ids[a];
+    if (e >= 0 && e < E)
+      atomicAdd(&cnt[e], 1);
+    else
+      bad = true;
+  }
+  if (bad) atomicOr(status, kStatusBadExpertId);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) blk_counts[(size_t)blockIdx.x * E + e] = cnt[e];
+}
+
+// Exclusive scan of one value per thread over a block of up to 1024 threads.
+__device__ int block_exclusive_scan(int v, int *warp_tot, int *total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) warp_tot[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int t = (lane < nw) ? warp_tot[lane] : 0;
+    int ti = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, ti, o);
+      if (lane >= o) ti += u;
+    }
+    if (lane < nw) warp_tot[lane] = ti - t;  // exclusive prefix of warp totals
+    if (lane == nw - 1) *total = ti;
+  }
+  __syncthreads();
+  const int r = warp_tot[w] + incl - v;
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kMaxE)
+    dispatch_scan_kernel(const int32_t *__restrict__ blk_counts, int nblk, int E,
+                         int32_t *__restrict__ blk_base, int32_t *__restrict__ counts,
+                         int32_t *__restrict__ offsets) {
+  __shared__ int warp_tot[32];
+  __shared__ int total;
+  const int e = threadIdx.x;
+  int tot = 0;
+  if (e < E)
+    for (int b = 0; b < nblk; ++b) tot += blk_counts[(size_t)b * E + e];
+  const int excl = block_exclusive_scan(tot, warp_tot, &total);
+  if (e < E) {
+    counts[e] = tot;
+    offsets[e] = excl;
+    int run = excl;
+    for (int b = 0; b < nblk; ++b) {
+      blk_base[(size_t)b * E + e] = run;
+      run += blk_counts[(size_t)b * E + e];
+    }
+  }
+  if (e == 0) offsets[E] = total;
+}
+
+__global__ void __launch_bounds__(kDispatchThreads)
+    dispatch_scatter_kernel(const int32_t *__restrict__ ids, const float *__restrict__ topk_w,
+                            int64_t Na, int E, const int32_t *__restrict__ blk_base,
+                            int32_t *__restrict__ perm_src, int32_t *__restrict__ inv_pos,
+                            float *__restrict__ w_perm) {
+  __shared__ int base[kMaxE];
+  __shared__ int wcnt[kWarps][kMaxE];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) base[e] = blk_base[(size_t)blockIdx.x * E + e];
+  const int64_t beg = (int64_t)blockIdx.x * kDispatchChunk;
+  const int64_t end = min(Na, beg + kDispatchChunk);
+  for (int64_t sub = beg; sub < end; sub += kDispatchThreads) {
+    for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) wcnt[i / E][i % E] = 0;
+    __syncthreads();
+    const int64_t a = sub + threadIdx.x;
+    int e = (a < end) ? ids[a] : -1;
+    if (e < 0 || e >= E) e = -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    const uint32_t below = peers & lanemask_lt();
+    const int rank = __popc(below);
+    const bool leader = (below == 0);
+    if (e >= 0 && leader) wcnt[w][e] = __popc(peers);
+    __syncthreads();
+    if (e >= 0) {
+      int before = 0;
+      for (int ww = 0; ww < w; ++ww) before += wcnt[ww][e];
+      const int pos = base[e] + before + rank;
+      perm_src[pos] = (int32_t)a;
+      inv_pos[a] = pos;
+      if (w_perm != nullptr) w_perm[pos] = topk_w[a];
+    }
+    __syncthreads();
+    if (e >= 0 && leader) atomicAdd(&base[e], __popc(peers));
+    __syncthreads();
+  }
+  (void)lane;
+}
+
+// Rows [0, Na): x_perm[p] = x[perm_src[p] / k]; rows [Na, Na+T) (shared
+// expert): x_perm[Na+t] = x[t].  One warp per row, 16-byte vectors.  The last
+// block instead writes the tile plan of the grouped GEMMs.
+__global__ void __launch_bounds__(256)
+    gather_plan_kernel(const __nv_bfloat16 *__restrict__ x, const int32_t *__restrict__ perm_src,
+                       const int32_t *__restrict__ offsets, int T, int k, int E, int H, int I,
+                       int shared, __nv_bfloat16 *__restrict__ x_perm, int32_t *__restrict__ plan,
+                       uint32_t *__restrict__ status) {
+  const int64_t Na = (int64_t)T * k;
+  const int64_t R = Na + (shared ? T : 0);
+  if (blockIdx.x == gridDim.x - 1) {
+    // ---- tile plan ----
+    __shared__ int warp_tot[32];
+    __shared__ int tot_gu, tot_dn, bad;
+    const int nseg = E + (shared ? 1 : 0);
+    const int nj_gu = (I + kBM - 1) / kBM, nj_dn = (H + kBM - 1) / kBM;
+    if (threadIdx.x == 0) bad = 0;
+    __syncthreads();
+    // validate the offsets (caller-provided in the standalone call)
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+      if (offsets[e] < 0 || offsets[e + 1] < offsets[e] || offsets[e + 1] > Na) bad = 1;
+    if (threadIdx.x == 0 && offsets[0] != 0) bad = 1;
+    __syncthreads();
+    if (threadIdx.x == 0 && bad) atomicOr(status, kStatusBadOffsets);
+    int32_t *seg_row = plan, *pref_gu = plan + nseg + 1, *pref_dn = plan + 2 * (nseg + 1);
+    // each thread owns up to 3 consecutive segments (nseg <= 513 < 3*256)
+    constexpr int kPer = 3;
+    const int s0 = threadIdx.x * kPer;
+    int gu[kPer], dn[kPer], sum_gu = 0, sum_dn = 0;
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int s = s0 + q;
+      int m = 0;
+      if (!bad && s < nseg) m = (s < E) ? offsets[s + 1] - offsets[s] : T;
+      const int chunks = (m + kBN - 1) / kBN;
+      gu[q] = chunks * nj_gu;
+      dn[q] = chunks * nj_dn;
+      sum_gu += gu[q];
+      sum_dn += dn[q];
+      if (s < nseg) seg_row[s] = bad ? 0 : ((s < E) ? offsets[s] : (int)Na);
+    }
+    int run_gu = block_exclusive_scan(sum_gu, warp_tot, &tot_gu);
+    int run_dn = block_exclusive_scan(sum_dn, warp_tot, &tot_dn);
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int s = s0 + q;
+      if (s < nseg) {
+        pref_gu[s] = run_gu;
+        pref_dn[s] = run_dn;
+      }
+      run_gu += gu[q];
+      run_dn += dn[q];
+    }
+    if (threadIdx.x == 0) {
+      seg_row[nseg] = bad ? 0 : (int)R;
+      pref_gu[nseg] = tot_gu;
+      pref_dn[nseg] = tot_dn;
+    }
+    return;
+  }
+  // ---- gather ----
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= R) return;
+  int64_t src = -1;
+  if (row < Na) {
+    const int32_t a = perm_src[row];
+    if (a >= 0 && a < Na) src = a / k;
+  } else {
+    src = row - Na;
+  }
+  uint4 *dst = reinterpret_cast<uint4 *>(x_perm + row * H);
+  const int nv = H / 8;
+  if (src < 0) {
+    for (int v = lane; v < nv; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
+    return;
+  }
+  const uint4 *s = reinterpret_cast<const uint4 *>(x + src * H);
+  for (int v = lane; v < nv; v += 32) dst[v] = s[v];
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const int32_t *ids, const float *topk_w, int T, int k, int E,
+                            int32_t *blk_counts, int32_t *blk_base, int32_t *counts,
+                            int32_t *offsets, int32_t *perm_src, int32_t *inv_pos, float *w_perm,
+                            uint32_t *status, cudaStream_t s) {
+  const int64_t Na = (int64_t)T * k;
+  const int nblk = (int)((Na + kDispatchChunk - 1) / kDispatchChunk);
+  dispatch_hist_kernel<<<nblk, kDispatchThreads, 0, s>>>(ids, Na, E, blk_counts, status);
+  dispatch_scan_kernel<<<1, kMaxE, 0, s>>>(blk_counts, nblk, E, blk_base, counts, offsets);
+  dispatch_scatter_kernel<<<nblk, kDispatchThreads, 0, s>>>(ids, topk_w, Na, E, blk_base, perm_src,
+                                                            inv_pos, w_perm);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_plan(const __nv_bfloat16 *x, const int32_t *perm_src,
+                               const int32_t *offsets, int T, int k, int E, int H, int I,
+                               int shared, __nv_bfloat16 *x_perm, int32_t *plan, uint32_t *status,
+                               cudaStream_t s) {
+  const int64_t R = (int64_t)T * k + (shared ? T : 0);
+  const int blocks = (int)((R + 7) / 8) + 1;
+  gather_plan_kernel<<<blocks, 256, 0, s>>>(x, perm_src, offsets, T, k, E, H, I, shared, x_perm,
+                                            plan, status);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,280 @@
+// Internal declarations of the sm_103a MoE FFN library: workspace layout,
+// launch helpers and the inline-PTX wrappers (mbarrier, TMA, tcgen05) the
+// kernels are written with.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// ------------------------------------------------------------ constants --
+
+constexpr int kMaxE = 512;          // routed experts
+constexpr int kMaxK = 32;           // experts per token
+constexpr int kMaxT = 1 << 20;
+constexpr int64_t kMaxAssign = 1 << 24;
+
+// Router logits tile (SIMT fp32): 64 tokens x 64 experts, K chunk 32.
+constexpr int kRouteTT = 64;
+constexpr int kRouteTE = 64;
+constexpr int kRouteBK = 32;
+constexpr int kRouteMaxSplits = 16;
+
+// Dispatch: assignments per block.
+constexpr int kDispatchThreads = 256;
+constexpr int kDispatchChunk = 4096;
+
+// Expert GEMMs (tcgen05): weight rows per tile, K per pipeline stage, token
+// rows per tile.
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kBN = 128;
+
+// Status word bits (latched with atomicOr).
+constexpr uint32_t kStatusBadExpertId = 1u << 0;
+constexpr uint32_t kStatusTimeoutGateUp = 1u << 1;
+constexpr uint32_t kStatusTimeoutDown = 1u << 2;
+constexpr uint32_t kStatusBadOffsets = 1u << 3;
+
+// A bounded pipeline wait gives up after this long (the longest legitimate
+// wait is one tile's mainloop, well under a millisecond).
+constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;
+
+// ---------------------------------------------------------- workspace --
+
+struct Layout {
+  size_t status, route_part, blk_counts, blk_base, plan, x_perm, h, out_perm;
+  size_t logits, topk_ids, topk_w, gap, counts, offsets, perm_src, inv_pos, w_perm;
+  size_t total;
+  int route_splits;
+  int nblk;      // dispatch blocks
+  int nseg;      // E (+1 with the shared expert)
+  int64_t rows;  // R = T*k (+T)
+};
+
+// Host: workspace layout of a (validated) descriptor.
+Layout make_layout(const moe_layer_desc_t &d);
+int route_splits(int T, int E, int H);
+
+// Tile plan layout inside the plan buffer (int32):
+//   [0, nseg]                 segment row offsets (nseg+1)
+//   [nseg+1, 2nseg+1]         gate/up tile prefix (nseg+1)
+//   [2nseg+2, 3nseg+2]        down tile prefix (nseg+1)
+inline int plan_ints(int nseg) { return 3 * (nseg + 1); }
+
+// ------------------------------------------------------------- launches --
+// Each returns cudaSuccess or the launch error.
+cudaError_t launch_router_logits(const __nv_bfloat16 *x, const float *w_router, int T, int H, int E,
+                                 int splits, float *partial, cudaStream_t s);
+cudaError_t launch_topk_gating(const float *partial, int splits, const float *sel_bias, int T,
+                               int E, int k, int gating, float *logits, int32_t *ids, float *w,
+                               float *gap, cudaStream_t s);
+cudaError_t launch_dispatch(const int32_t *ids, const float *topk_w, int T, int k, int E,
+                            int32_t *blk_counts, int32_t *blk_base, int32_t *counts,
+                            int32_t *offsets, int32_t *perm_src, int32_t *inv_pos, float *w_perm,
+                            uint32_t *status, cudaStream_t s);
+cudaError_t launch_gather_plan(const __nv_bfloat16 *x, const int32_t *perm_src,
+                               const int32_t *offsets, int T, int k, int E, int H, int I,
+                               int shared, __nv_bfloat16 *x_perm, int32_t *plan, uint32_t *status,
+                               cudaStream_t s);
+cudaError_t launch_expert_gateup(const moe_layer_desc_t &d, const void *w13, const void *w13_shared,
+                                 const __nv_bfloat16 *x_perm, const int32_t *plan,
+                                 __nv_bfloat16 *h, uint32_t *status, cudaStream_t s);
+cudaError_t launch_expert_down(const moe_layer_desc_t &d, const void *w2, const void *w2_shared,
+                               const __nv_bfloat16 *h, const int32_t *plan, const float *w_perm,
+                               __nv_bfloat16 *out_perm, uint32_t *status, cudaStream_t s);
+cudaError_t launch_combine(const __nv_bfloat16 *out_perm, const int32_t *inv_pos,
+                           const float *topk_w, int T, int k, int H, int shared, __nv_bfloat16 *y,
+                           cudaStream_t s);
+
+int num_sms();  // of the current device (cached)
+
+// ----------------------------------------------------- device helpers --
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// --- mbarrier ---
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for phase `parity` of `bar`.  Gives up (returns false) when the
+// CTA's abort flag is raised or after kWaitLimitNs; on its own timeout it
+// raises the abort flag and latches `code` in the global status word.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          uint32_t *status, uint32_t code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0; it < (1u << 30); ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 63u) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+    }
+  }
+  *abort_flag = 1;
+  atomicOr(status, code);
+  return false;
+}
+
+// Short bounded wait used only while draining after an abort.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity) {
+  uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0; it < (1u << 26); ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 63u && globaltimer_ns() - t0 > kWaitLimitNs / 10) return false;
+  }
+  return false;
+}
+
+// --- TMA (tensor tiles, global -> shared, completion on an mbarrier) ---
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *m, uint64_t *bar, int c0,
+                                            int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(m), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *m, uint64_t *bar, int c0,
+                                            int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(m), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *m, uint64_t *bar, int c0,
+                                            int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(m), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
+// --- tcgen05: tensor memory, MMA, loads ---
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulator, one CTA.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 op this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit columns; thread i gets lane (base + i).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32"
+      " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile written by TMA
+// with 128-byte swizzling: rows of 64 bf16 (128 B), 8-row core groups 1024 B
+// apart.  Fields: start address >> 4 (bits 0-13), leading byte offset >> 4
+// (bits 16-29, unused for this layout), stride byte offset >> 4 (bits
+// 32-45), descriptor version 1 (bits 46-47), swizzle mode 2 = 128 B (bits
+// 61-63).
+__device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), A and
+// B bf16 (bits 7-9 = 1, bits 10-12 = 1), both K-major (bits 15, 16 = 0),
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+}  // namespace moe

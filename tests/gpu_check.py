@@ -1,0 +1,149 @@
+"""Helpers of the GPU parity tests: run the CUDA path through the C ABI and
+compare it with the CPU oracle on the same seeded inputs."""
+
+from __future__ import annotations
+
+import math
+from typing import Dict, Optional, Sequence
+
+import numpy as np
+import torch
+
+import oracle
+import routed_expert_ffn_gb300 as moe
+import synth
+
+# Tolerances (stated with the layer configurations): routing metadata is
+# bit-exact except at near-ties (top-k boundary gap below 1e-5); layer outputs
+# reach relative L2 <= 1e-2 and per-element |err| <= 3e-2 * rms(y).
+NEAR_TIE = 1e-5
+REL_L2 = 1e-2
+ELEM = 3e-2
+GATE_ATOL = 1e-5
+
+
+def rel_l2(a: np.ndarray, b: np.ndarray) -> float:
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+def assert_output_close(got: np.ndarray, ref: np.ndarray, what: str = "y"):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    rms = math.sqrt(float(np.mean(ref ** 2)))
+    r = rel_l2(got, ref)
+    m = float(np.max(np.abs(got - ref))) if got.size else 0.0
+    assert r <= REL_L2, f"{what}: relative L2 {r:.3e} > {REL_L2}"
+    assert m <= ELEM * rms, f"{what}: max |err| {m:.3e} > {ELEM} * rms {rms:.3e}"
+    return r, m / max(rms, 1e-300)
+
+
+def bf16_np(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def selection_keys(s: np.ndarray, gating: int, bias: Optional[np.ndarray]) -> np.ndarray:
+    """float32 selection keys per the gating variant (for validity checks)."""
+    if gating == synth.GATE_SIGMOID_BIAS_RENORM:
+        a = (1.0 / (1.0 + np.exp(-s.astype(np.float64)))).astype(np.float32)
+        return (a + bias.astype(np.float32)).astype(np.float32)
+    return s.astype(np.float32)
+
+
+def check_routing(gpu_ids: np.ndarray, gpu_w: np.ndarray, ref: Dict[str, np.ndarray], gating: int,
+                  bias) -> Dict[str, int]:
+    """Bit-exact ids (and weights within GATE_ATOL) on every token whose oracle
+    boundary gap is >= NEAR_TIE; on near-tie tokens the GPU selection must be a
+    valid top-k of the oracle's keys within NEAR_TIE."""
+    k = gpu_ids.shape[1]
+    gap = ref["gap"]
+    clear = ~(gap < NEAR_TIE)          # NaN gap (k == E) counts as clear
+    assert np.array_equal(gpu_ids[clear], ref["ids"][clear]), "expert ids differ off near-ties"
+    assert np.max(np.abs(gpu_w[clear] - ref["w"][clear]), initial=0.0) <= GATE_ATOL
+    ties = np.where(~clear)[0]
+    flips = 0
+    if len(ties):
+        keys = selection_keys(ref["logits"], gating, None if bias is None else np.asarray(bias))
+        for t in ties:
+            kth = np.sort(keys[t])[::-1][k - 1]
+            sel = set(gpu_ids[t].tolist())
+            assert len(sel) == k
+            for e in range(keys.shape[1]):
+                if e in sel:
+                    assert keys[t, e] >= kth - NEAR_TIE
+                else:
+                    assert keys[t, e] <= kth + NEAR_TIE
+            flips += int(not np.array_equal(gpu_ids[t], ref["ids"][t]))
+    return {"near_ties": int(len(ties)), "flips": flips}
+
+
+class LayerRun:
+    """One moe_layer_forward of a seeded workload on cuda:0."""
+
+    def __init__(self, inputs: synth.LayerInputs):
+        cfg, T = inputs.cfg, inputs.T
+        self.inputs = inputs
+        self.d = moe.desc(T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.gating, cfg.shared)
+        self.ws = moe.alloc_workspace(self.d)
+        self.layout = moe.moe_workspace_layout(self.d)
+        self.w = moe.layer_weights(inputs.w_router, inputs.w13, inputs.w2, inputs.sel_bias,
+                                   inputs.w13_shared, inputs.w2_shared)
+        self.y = torch.empty((T, cfg.H), dtype=torch.bfloat16, device="cuda")
+
+    def forward(self):
+        moe.moe_layer_forward(self.d, self.w, self.inputs.x, self.y, self.ws)
+        torch.cuda.synchronize()
+        st, raw = moe.moe_get_device_status(self.ws)
+        assert st == moe.MOE_OK, (st, raw)
+        return self.y
+
+    def view(self, name, dtype, shape):
+        return moe.workspace_view(self.ws, self.layout, name, dtype, shape)
+
+    def metadata(self):
+        cfg, T = self.inputs.cfg, self.inputs.T
+        Na = T * cfg.k
+        g = lambda n, dt, sh: self.view(n, dt, sh).cpu().numpy()
+        return {
+            "logits": g("logits", torch.float32, (T, cfg.E)),
+            "ids": g("topk_ids", torch.int32, (T, cfg.k)),
+            "w": g("topk_w", torch.float32, (T, cfg.k)),
+            "gap": g("gap", torch.float32, (T,)),
+            "counts": g("counts", torch.int32, (cfg.E,)),
+            "offsets": g("offsets", torch.int32, (cfg.E + 1,)),
+            "perm_src": g("perm_src", torch.int32, (Na,)),
+            "inv_pos": g("inv_pos", torch.int32, (Na,)),
+            "w_perm": g("w_perm", torch.float32, (Na,)),
+        }
+
+
+def host_copy(inputs: synth.LayerInputs, experts: Optional[Sequence[int]] = None):
+    """Host copies of the exact bytes the GPU used: x, router, bias, and the
+    listed experts' weight blocks (all experts when None)."""
+    E = inputs.cfg.E
+    ex = range(E) if experts is None else experts
+    return {
+        "x": inputs.x.cpu(),
+        "w_router": inputs.w_router.cpu(),
+        "sel_bias": None if inputs.sel_bias is None else inputs.sel_bias.cpu(),
+        "w13": {e: inputs.w13[e].cpu() for e in ex},
+        "w2": {e: inputs.w2[e].cpu() for e in ex},
+        "w13_shared": None if inputs.w13_shared is None else inputs.w13_shared.cpu(),
+        "w2_shared": None if inputs.w2_shared is None else inputs.w2_shared.cpu(),
+    }
+
+
+def sample_tokens(T: int, n: int, ids: np.ndarray, counts: np.ndarray, seed: int = 0):
+    """A seeded token sample of size <= n that always includes a token of the
+    hottest and of the coldest touched expert, plus the first and last token."""
+    if T <= n:
+        return list(range(T))
+    rng = np.random.default_rng(seed)
+    pick = set(rng.choice(T, size=n - 4, replace=False).tolist()) | {0, T - 1}
+    touched = np.where(counts > 0)[0]
+    hot = int(touched[np.argmax(counts[touched])])
+    cold = int(touched[np.argmin(counts[touched])])
+    for e in (hot, cold):
+        rows = np.where((ids == e).any(axis=1))[0]
+        pick.add(int(rows[0]))
+    return sorted(pick)
