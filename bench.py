@@ -1,0 +1,425 @@
+"""Benchmark of the MoE FFN layer forward on GB300.
+
+One step = one moe_layer_forward over one batch of synthetic tokens: router,
+top-k gating, dispatch, grouped SwiGLU GEMMs, combine.  Default workload: the
+Qwen3-235B-A22B-shaped layer (H=4096, E=128, top-8, I=1536, softmax-then-top-k
+renormalised, Zipf(1.1) routing skew) at T=1024 tokens per step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--T T]
+    python bench.py --impl reference ...     # the CPU oracle, timed on host cores
+
+Prints one JSON line.  With N > 1 (torchrun) every rank runs an independent
+replica on its own batch (weak scaling); ranks exchange only timings.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s at Qwen3-235B layer shape; % of HBM / bf16-TC roofline"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--config", default="qwen3")
+    p.add_argument("--T", type=int, default=1024)
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--E", type=int, default=0,
+                   help="override the number of experts (reduced cases for profiler captures)")
+    p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-tokens", type=int, default=48)
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            m = json.load(f)
+        return {"hbm_gbs": m["hbm_gbs"], "bf16_tflops": m["bf16_tflops"],
+                "bf16_tflops_sustained": m.get("bf16_tflops_sustained", m["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def layer_config(args):
+    import dataclasses
+
+    import synth
+    cfg = synth.CONFIGS[args.config]
+    if args.E:
+        cfg = dataclasses.replace(cfg, name=f"{cfg.name}_E{args.E}", E=args.E, k=min(cfg.k, args.E))
+    return cfg
+
+
+def workload_config(cfg, T):
+    return {"workload": f"{cfg.name} layer, T={T} tokens/step", "layer": cfg.name,
+            "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I, "T": T,
+            "gating": ["topk_softmax", "softmax_topk", "softmax_topk_renorm",
+                       "sigmoid_bias_renorm"][cfg.gating],
+            "shared_expert": cfg.shared, "routing_skew": str(cfg.skew),
+            "l2": "inputs larger than L2 (the step streams the touched experts' weights, "
+                  f"{cfg.E * 3 * cfg.H * cfg.I * 2 / 1e9:.2f} GB for all experts)"}
+
+
+# ------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) taken while the timed region runs."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.rows = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        inside = [r for t, r in self.rows if t0 <= t <= t1 + 0.15]
+        used = inside if inside else [r for _, r in self.rows]
+        sm = [float(r[1]) for r in used if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in used if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in used for n, v in zip(names, r[5:9]) if v == "Active"})
+        pw = [float(r[3]) for r in used if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "power_w_max": max(pw) if pw else None,
+                "samples": len(inside), "window": "timed region" if inside else "whole run"}
+
+
+# ------------------------------------------------------ roofline model --
+
+def algorithmic(cfg, T, counts):
+    """Algorithmic bytes and flops of one step and of the gate/up GEMM."""
+    touched = int(sum(1 for c in counts if c > 0))
+    H, I, E, k = cfg.H, cfg.I, cfg.E, cfg.k
+    per_expert = 3 * H * I * 2
+    nsh = 1 if cfg.shared else 0
+    layer_bytes = (touched + nsh) * per_expert + E * H * 4 + 2 * T * H * 2
+    layer_flops = 2 * T * k * 3 * H * I + nsh * 2 * T * 3 * H * I + 2 * T * H * E
+    rows = T * k + nsh * T
+    gateup_bytes = (touched + nsh) * 2 * I * H * 2 + rows * H * 2 + rows * I * 2
+    gateup_flops = 2 * rows * 2 * I * H
+    return {"touched": touched, "layer_bytes": layer_bytes, "layer_flops": layer_flops,
+            "gateup_bytes": gateup_bytes, "gateup_flops": gateup_flops}
+
+
+# ------------------------------------------------------------ CPU oracle --
+
+def cpu_oracle_sample(inputs_host, n_tokens, seed=0):
+    """Time the oracle (routing + layer) on a seeded sample of n tokens."""
+    import numpy as np
+
+    import oracle
+    cfg, T = inputs_host.cfg, inputs_host.T
+    rng = np.random.default_rng(seed)
+    toks = sorted(rng.choice(T, size=min(n_tokens, T), replace=False).tolist())
+    x = inputs_host.x[toks].contiguous()
+    threads = oracle.max_threads()
+    t0 = time.perf_counter()
+    s = oracle.router_logits(x, inputs_host.w_router, threads)
+    ids, w, _ = oracle.topk_gating(s, cfg.k, cfg.gating, inputs_host.sel_bias)
+    oracle.layer_tokens(x, ids, w, inputs_host.w13, inputs_host.w2, range(len(toks)),
+                        inputs_host.w13_shared, inputs_host.w2_shared, threads)
+    dt = time.perf_counter() - t0
+    return len(toks), dt, threads
+
+
+def host_inputs(cfg, T, seed, experts_from_gpu=None):
+    """Host copy of a workload; expert blocks are copied lazily from the GPU
+    tensors when given (only the experts the oracle reads are fetched)."""
+    import synth
+
+    class Lazy(dict):
+        def __init__(self, src):
+            super().__init__()
+            self.src = src
+
+        def __missing__(self, e):
+            v = self.src[e].cpu()
+            self[e] = v
+            return v
+
+        def keys(self):
+            return range(self.src.shape[0])
+
+    if experts_from_gpu is not None:
+        g = experts_from_gpu
+        return synth.LayerInputs(cfg, T, seed, g.x.cpu(), g.w_router.cpu(),
+                                 None if g.sel_bias is None else g.sel_bias.cpu(),
+                                 Lazy(g.w13), Lazy(g.w2),
+                                 None if g.w13_shared is None else g.w13_shared.cpu(),
+                                 None if g.w2_shared is None else g.w2_shared.cpu())
+    return synth.make_layer(cfg, T, seed, device="cpu")
+
+
+# ---------------------------------------------------------------- arms --
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def max_over_ranks(value: float, pg):
+    if pg is None:
+        return value
+    import torch
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step is a bounded token sample of
+    the same workload, timed on the host cores."""
+    import synth
+    world, rank, local, pg = dist_setup(args)
+    if rank != 0:
+        return
+    cfg = layer_config(args)
+    T = args.T
+    inp = host_inputs(cfg, T, args.seed)
+    n = min(args.cpu_tokens, T)
+    for _ in range(max(0, min(args.warmup, 1))):
+        cpu_oracle_sample(inp, max(1, n // 8), seed=99)
+    total_tok, total_s, threads = 0, 0.0, 1
+    for step in range(args.steps):
+        k, dt, threads = cpu_oracle_sample(inp, n, seed=step)
+        total_tok += k
+        total_s += dt
+    value = total_tok / total_s
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(cfg, T),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{n} seeded tokens of the T={T} batch per step "
+                                       "(routing + expert FFNs + combine, fp64)"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def run_gpu(args):
+    import torch
+
+    import routed_expert_ffn_gb300 as moe
+    import synth
+    from routed_expert_ffn_gb300 import build as moe_build
+
+    world, rank, local, pg = dist_setup(args)
+    torch.cuda.set_device(local)
+    moe_build.build()
+    cfg = layer_config(args)
+    T = args.T
+    # every rank: the same layer weights, its own batch of tokens
+    inp = synth.make_layer(cfg, T, args.seed, device="cuda")
+    if rank > 0:
+        inp.x = synth.make_tokens(cfg, T, args.seed + 1000 * rank, device="cuda")
+    d = moe.desc(T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.gating, cfg.shared)
+    ws = moe.alloc_workspace(d)
+    lay = moe.moe_workspace_layout(d)
+    wts = moe.layer_weights(inp.w_router, inp.w13, inp.w2, inp.sel_bias, inp.w13_shared,
+                            inp.w2_shared)
+    y = torch.empty((T, cfg.H), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def new_events(n):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in evs:
+            e.record(stream)  # materialise the handles
+        return evs
+
+    # warm-up
+    for _ in range(args.warmup):
+        moe.moe_layer_forward(d, wts, inp.x, y, ws)
+    torch.cuda.synchronize()
+    st, raw = moe.moe_get_device_status(ws)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device status {st} raw={raw:#x}")
+
+    stage_ev = [new_events(moe.MOE_STAGE_EVENTS) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    sampler = ClockSampler(uuid) if rank == 0 else None
+    time.sleep(0.5 if sampler else 0)
+
+    # ---- timed region: K steps ----
+    barrier(pg)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        moe.moe_layer_forward(d, wts, inp.x, y, ws, stage_events=stage_ev[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg)
+    t_wall1 = time.time()
+    ms = start.elapsed_time(end)
+    ms_max = max_over_ranks(ms, pg)
+    st, raw = moe.moe_get_device_status(ws)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device status {st} raw={raw:#x}")
+
+    stage_ms = {n: 0.0 for n in moe.STAGE_NAMES}
+    for ev in stage_ev:
+        for j, n in enumerate(moe.STAGE_NAMES):
+            stage_ms[n] += ev[j].elapsed_time(ev[j + 1])
+    stage_us = {n: 1e3 * v / args.steps for n, v in stage_ms.items()}
+
+    # ---- end to end: pinned host x in, host y out, through the same call ----
+    x_host = inp.x.cpu().pin_memory()
+    y_host = torch.empty((T, cfg.H), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(inp.x)
+    e_steps = max(3, min(args.steps, 50))
+    for _ in range(2):
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.moe_layer_forward(d, wts, x_dev, y, ws)
+        y_host.copy_(y, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(pg)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.moe_layer_forward(d, wts, x_dev, y, ws)
+        y_host.copy_(y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e_ms = max_over_ranks(e0.elapsed_time(e1), pg)
+    if sampler:
+        sampler.stop()
+
+    counts = moe.workspace_view(ws, lay, "counts", torch.int32, (cfg.E,)).cpu().tolist()
+    if rank != 0:
+        return
+    pk = peaks()
+    alg = algorithmic(cfg, T, counts)
+    step_s = ms_max / 1e3 / args.steps
+    value = world * T / step_s
+    gu_s = stage_us["gateup"] / 1e6
+    gu_gbs = alg["gateup_bytes"] / gu_s / 1e9
+    layer_t_hbm = alg["layer_bytes"] / (pk["hbm_gbs"] * 1e9)
+    layer_t_tc = alg["layer_flops"] / (pk["bf16_tflops_sustained"] * 1e12)
+    layer_roof = max(layer_t_hbm, layer_t_tc)
+    num = max(counts) * cfg.E
+    den = T * cfg.k
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        with open(prof) as f:
+            tr = json.load(f).get(f"{cfg.name}_T{T}")
+        if tr and tr.get("kernel_sources_sha") == kernel_sources_sha():
+            traffic = tr["gateup_dram_bytes"]
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded counter-based generator; random-init weights of the layer shape)",
+        "config": workload_config(cfg, T),
+        "roofline": {"bound": "hbm", "kernel": "expert gate/up GEMM + SwiGLU (tcgen05)",
+                     "achieved": gu_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": gu_gbs / pk["hbm_gbs"], "traffic": traffic,
+                     "algorithmic_bytes": alg["gateup_bytes"], "launch_us": stage_us["gateup"],
+                     "peak_source": pk["source"]},
+        "layer_roofline": {"bound": "hbm" if layer_t_hbm >= layer_t_tc else "tensor",
+                           "roof_us": layer_roof * 1e6, "step_us": step_s * 1e6,
+                           "frac": layer_roof / step_s, "bytes": alg["layer_bytes"],
+                           "flops": alg["layer_flops"], "touched_experts": alg["touched"],
+                           "hbm_peak_gbs": pk["hbm_gbs"],
+                           "tc_peak_tflops": pk["bf16_tflops_sustained"]},
+        "stages_us": stage_us,
+        "routing": {"imbalance_ratio": num / den, "touched_experts": alg["touched"]},
+        "e2e": {"value": world * T * e_steps / (e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": T * cfg.H * 2, "d2h_bytes_per_step": T * cfg.H * 2},
+        "gpu_launches": 9 * args.steps,
+        "clocks": sampler.summary(t_wall0, t_wall1) if sampler else None,
+    }
+    if not args.no_cpu_baseline:
+        hin = host_inputs(cfg, T, args.seed, experts_from_gpu=inp)
+        n, dt, threads = cpu_oracle_sample(hin, args.cpu_tokens)
+        line["cpu_baseline"] = {"value": n / dt, "unit": "tokens/s", "cores": threads,
+                                "kind": "oracle",
+                                "sample": f"{n} seeded tokens of the T={T} batch (routing + "
+                                          "expert FFNs + combine, fp64)"}
+    print(json.dumps(line))
+
+
+def kernel_sources_sha():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "routed_expert_ffn_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

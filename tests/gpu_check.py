@@ -38,6 +38,16 @@ def assert_output_close(got: np.ndarray, ref: np.ndarray, what: str = "y"):
     return r, m / max(rms, 1e-300)
 
 
+def assert_rows_close(got: np.ndarray, ref: np.ndarray, what: str = "rows"):
+    """The output criterion applied to each row on its own scale: every row of
+    out_perm is one expert's (gate-weighted) output, an output of its own."""
+    worst = (0.0, 0.0)
+    for i in range(ref.shape[0]):
+        r, m = assert_output_close(got[i], ref[i], f"{what}[{i}]")
+        worst = (max(worst[0], r), max(worst[1], m))
+    return worst
+
+
 def bf16_np(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy().astype(np.float64)
 
