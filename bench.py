@@ -234,7 +234,13 @@ def run_reference(args):
         return
     cfg = layer_config(args)
     T = args.T
-    inp = host_inputs(cfg, T, args.seed)
+    import torch
+    if torch.cuda.is_available():
+        # inputs are generated on the GPU (untimed); the oracle reads host copies
+        gen = synth.make_layer(cfg, T, args.seed, device="cuda")
+        inp = host_inputs(cfg, T, args.seed, experts_from_gpu=gen)
+    else:
+        inp = host_inputs(cfg, T, args.seed)
     n = min(args.cpu_tokens, T)
     for _ in range(max(0, min(args.warmup, 1))):
         cpu_oracle_sample(inp, max(1, n // 8), seed=99)

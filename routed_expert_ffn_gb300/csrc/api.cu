@@ -36,7 +36,8 @@ Layout make_layout(const moe_layer_desc_t &d) {
   L.rows = Na + (shared ? d.T : 0);
   L.nseg = d.E + shared;
   L.route_splits = route_splits(d.T, d.E, d.H);
-  L.nblk = (int)((Na + kDispatchChunk - 1) / kDispatchChunk);
+  const int64_t chunk = dispatch_chunk(Na);
+  L.nblk = (int)((Na + chunk - 1) / chunk);
   L.status = take(256);
   L.route_part = take((size_t)L.route_splits * d.T * d.E * 4);
   L.blk_counts = take((size_t)L.nblk * d.E * 4);
@@ -53,7 +54,7 @@ Layout make_layout(const moe_layer_desc_t &d) {
   L.w_perm = take((size_t)Na * 4);
   L.x_perm = take((size_t)L.rows * d.H * 2);
   L.h = take((size_t)L.rows * d.I * 2);
-  L.out_perm = take((size_t)L.rows * d.H * 2);
+  L.out_perm = take((size_t)L.rows * d.H * 4);
   L.total = off;
   return L;
 }
@@ -256,7 +257,8 @@ moe_status_t moe_grouped_swiglu_ffn(const moe_layer_desc_t *d, const void *x,
                                      d->has_shared_expert, x_perm, plan, status, s);
   if (e == cudaSuccess) e = launch_expert_gateup(*d, w13, w13_shared, x_perm, plan, h, status, s);
   if (e == cudaSuccess)
-    e = launch_expert_down(*d, w2, w2_shared, h, plan, w_perm, bfw(out_perm), status, s);
+    e = launch_expert_down(*d, w2, w2_shared, h, plan, w_perm, static_cast<float *>(out_perm),
+                           status, s);
   return cuda_status(e);
 }
 
@@ -268,7 +270,8 @@ moe_status_t moe_combine(const moe_layer_desc_t *d, const void *out_perm, const 
   if (!ok_ptr(out_perm) || !ok_ptr(inv_pos) || !ok_opt(topk_w) || !ok_ptr(y))
     return MOE_ERR_INVALID_ARG;
   if ((st = check_device()) != MOE_OK) return st;
-  return cuda_status(launch_combine(bf(out_perm), inv_pos, topk_w, d->T, d->k, d->H,
+  return cuda_status(launch_combine(static_cast<const float *>(out_perm), inv_pos, topk_w, d->T,
+                                    d->k, d->H,
                                     d->has_shared_expert, bfw(y), (cudaStream_t)stream));
 }
 
@@ -300,7 +303,7 @@ moe_status_t moe_layer_forward(const moe_layer_desc_t *d, const moe_layer_weight
   int32_t *plan = at<int32_t>(workspace, L.plan);
   __nv_bfloat16 *x_perm = at<__nv_bfloat16>(workspace, L.x_perm);
   __nv_bfloat16 *h = at<__nv_bfloat16>(workspace, L.h);
-  __nv_bfloat16 *out_perm = at<__nv_bfloat16>(workspace, L.out_perm);
+  float *out_perm = at<float>(workspace, L.out_perm);
   float *part = at<float>(workspace, L.route_part);
 
   cudaError_t e = mark(0);

@@ -2,7 +2,7 @@
 // "Dispatch 并不是一次普通 all-to-all"), and the gather of the permuted token
 // rows plus the tile plan the grouped GEMMs read.
 //
-// The flat assignment list a = t*k + j is cut into blocks of kDispatchChunk:
+// The flat assignment list a = t*k + j is cut into per-block chunks:
 //   1. hist:    per-block expert histogram in shared memory (atomics only
 //               count; they never decide a position);
 //   2. scan:    one CTA sums the block histograms per expert, scans them into
@@ -22,13 +22,13 @@ namespace {
 constexpr int kWarps = kDispatchThreads / 32;
 
 __global__ void __launch_bounds__(kDispatchThreads)
-    dispatch_hist_kernel(const int32_t *__restrict__ ids, int64_t Na, int E,
+    dispatch_hist_kernel(const int32_t *__restrict__ ids, int64_t Na, int64_t chunk, int E,
                          int32_t *__restrict__ blk_counts, uint32_t *__restrict__ status) {
   __shared__ int cnt[kMaxE];
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
-  const int64_t beg = (int64_t)blockIdx.x * kDispatchChunk;
-  const int64_t end = min(Na, beg + kDispatchChunk);
+  const int64_t beg = (int64_t)blockIdx.x * chunk;
+  const int64_t end = min(Na, beg + chunk);
   bool bad = false;
   for (int64_t a = beg + threadIdx.x; a < end; a += blockDim.x) {
     const int e = ids[a];
@@ -95,15 +95,16 @@ __global__ void __launch_bounds__(kMaxE)
 
 __global__ void __launch_bounds__(kDispatchThreads)
     dispatch_scatter_kernel(const int32_t *__restrict__ ids, const float *__restrict__ topk_w,
-                            int64_t Na, int E, const int32_t *__restrict__ blk_base,
+                            int64_t Na, int64_t chunk, int E,
+                            const int32_t *__restrict__ blk_base,
                             int32_t *__restrict__ perm_src, int32_t *__restrict__ inv_pos,
                             float *__restrict__ w_perm) {
   __shared__ int base[kMaxE];
   __shared__ int wcnt[kWarps][kMaxE];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   for (int e = threadIdx.x; e < E; e += blockDim.x) base[e] = blk_base[(size_t)blockIdx.x * E + e];
-  const int64_t beg = (int64_t)blockIdx.x * kDispatchChunk;
-  const int64_t end = min(Na, beg + kDispatchChunk);
+  const int64_t beg = (int64_t)blockIdx.x * chunk;
+  const int64_t end = min(Na, beg + chunk);
   for (int64_t sub = beg; sub < end; sub += kDispatchThreads) {
     for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) wcnt[i / E][i % E] = 0;
     __syncthreads();
@@ -219,11 +220,12 @@ cudaError_t launch_dispatch(const int32_t *ids, const float *topk_w, int T, int 
                             int32_t *offsets, int32_t *perm_src, int32_t *inv_pos, float *w_perm,
                             uint32_t *status, cudaStream_t s) {
   const int64_t Na = (int64_t)T * k;
-  const int nblk = (int)((Na + kDispatchChunk - 1) / kDispatchChunk);
-  dispatch_hist_kernel<<<nblk, kDispatchThreads, 0, s>>>(ids, Na, E, blk_counts, status);
+  const int64_t chunk = dispatch_chunk(Na);
+  const int nblk = (int)((Na + chunk - 1) / chunk);
+  dispatch_hist_kernel<<<nblk, kDispatchThreads, 0, s>>>(ids, Na, chunk, E, blk_counts, status);
   dispatch_scan_kernel<<<1, kMaxE, 0, s>>>(blk_counts, nblk, E, blk_base, counts, offsets);
-  dispatch_scatter_kernel<<<nblk, kDispatchThreads, 0, s>>>(ids, topk_w, Na, E, blk_base, perm_src,
-                                                            inv_pos, w_perm);
+  dispatch_scatter_kernel<<<nblk, kDispatchThreads, 0, s>>>(ids, topk_w, Na, chunk, E, blk_base,
+                                                            perm_src, inv_pos, w_perm);
   return cudaGetLastError();
 }
 

@@ -36,7 +36,7 @@
 //               tile overlap the mainloop of the next;
 //   warps 0-3   epilogue: tcgen05.ld of their 32 TMEM lanes (= 32 weight
 //               rows), fused SiLU(gate)*up (gate/up GEMM) or gate weighting
-//               (down GEMM), bf16 stores.
+//               (down GEMM), bf16 (h) or fp32 (out_perm) stores.
 // Every wait is bounded; on expiry the CTA records MOE_ERR_TIMEOUT's status
 // bit, drains its copies and MMAs in flight, frees TMEM and returns.
 #include <stdio.h>
@@ -105,9 +105,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tm_a_sh,  // shared-expert weights (4D)
                        const __grid_constant__ CUtensorMap tm_b,     // activations [R, K] (2D)
                        const int32_t *__restrict__ plan, int nseg, int E, int K, int out_cols,
-                       int64_t Na, const float *__restrict__ w_perm,
-                       __nv_bfloat16 *__restrict__ out, uint32_t *__restrict__ status) {
+                       int64_t Na, const float *__restrict__ w_perm, void *__restrict__ out_,
+                       uint32_t *__restrict__ status) {
   using C = Cfg<kGateUp, BN, STAGES>;
+  // gate/up writes h in bf16 (the next GEMM's operand); down writes fp32
+  // gate-weighted rows, so the combine adds k rows without another rounding
+  __nv_bfloat16 *out_h = static_cast<__nv_bfloat16 *>(out_);
+  float *out_f = static_cast<float *>(out_);
   constexpr uint32_t kCode = kGateUp ? kStatusTimeoutGateUp : kStatusTimeoutDown;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -268,7 +272,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float wt = (w_perm != nullptr && row < Na) ? w_perm[row] : 1.0f;
                 val = __uint_as_float(v0[q]) * wt;
               }
-              out[row * out_cols + col] = __float2bfloat16_rn(val);
+              if (kGateUp)
+                out_h[row * out_cols + col] = __float2bfloat16_rn(val);
+              else
+                out_f[row * out_cols + col] = val;
             }
           }
         }
@@ -337,7 +344,7 @@ bool act_map(CUtensorMap *m, const void *a, int K, int64_t R) {
 template <bool kGateUp, int BN, int STAGES>
 cudaError_t launch_gemm(const moe_layer_desc_t &d, const void *w, const void *w_sh,
                         const __nv_bfloat16 *act, const int32_t *plan, const float *w_perm,
-                        __nv_bfloat16 *out, uint32_t *status, cudaStream_t s) {
+                        void *out, uint32_t *status, cudaStream_t s) {
   using C = Cfg<kGateUp, BN, STAGES>;
   static_assert(BN == kBN, "the tile plan assumes kBN-row token chunks");
   const int shared = d.has_shared_expert ? 1 : 0;
@@ -386,7 +393,7 @@ cudaError_t launch_expert_gateup(const moe_layer_desc_t &d, const void *w13, con
 
 cudaError_t launch_expert_down(const moe_layer_desc_t &d, const void *w2, const void *w2_shared,
                                const __nv_bfloat16 *h, const int32_t *plan, const float *w_perm,
-                               __nv_bfloat16 *out_perm, uint32_t *status, cudaStream_t s) {
+                               float *out_perm, uint32_t *status, cudaStream_t s) {
   return launch_gemm<false, kBN, kStagesDown>(d, w2, w2_shared, h, plan, w_perm, out_perm, status,
                                               s);
 }

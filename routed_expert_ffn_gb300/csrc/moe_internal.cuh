@@ -25,9 +25,16 @@ constexpr int kRouteTE = 64;
 constexpr int kRouteBK = 32;
 constexpr int kRouteMaxSplits = 16;
 
-// Dispatch: assignments per block.
+// Dispatch: threads per block; each block takes a chunk of the assignment
+// list (a multiple of the block size, chosen so there are at most
+// kDispatchMaxBlocks blocks).
 constexpr int kDispatchThreads = 256;
-constexpr int kDispatchChunk = 4096;
+constexpr int kDispatchMaxBlocks = 1024;
+inline int64_t dispatch_chunk(int64_t Na) {
+  int64_t c = (Na + kDispatchMaxBlocks - 1) / kDispatchMaxBlocks;
+  c = (c + kDispatchThreads - 1) / kDispatchThreads * kDispatchThreads;
+  return c < kDispatchThreads ? kDispatchThreads : c;
+}
 
 // Expert GEMMs (tcgen05): weight rows per tile, K per pipeline stage, token
 // rows per tile.
@@ -87,8 +94,8 @@ cudaError_t launch_expert_gateup(const moe_layer_desc_t &d, const void *w13, con
                                  __nv_bfloat16 *h, uint32_t *status, cudaStream_t s);
 cudaError_t launch_expert_down(const moe_layer_desc_t &d, const void *w2, const void *w2_shared,
                                const __nv_bfloat16 *h, const int32_t *plan, const float *w_perm,
-                               __nv_bfloat16 *out_perm, uint32_t *status, cudaStream_t s);
-cudaError_t launch_combine(const __nv_bfloat16 *out_perm, const int32_t *inv_pos,
+                               float *out_perm, uint32_t *status, cudaStream_t s);
+cudaError_t launch_combine(const float *out_perm, const int32_t *inv_pos,
                            const float *topk_w, int T, int k, int H, int shared, __nv_bfloat16 *y,
                            cudaStream_t s);
 
