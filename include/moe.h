@@ -254,6 +254,46 @@ moe_status_t moe_layer_forward(const moe_layer_desc_t *d, const moe_layer_weight
                                const void *x, void *y, void *workspace, size_t ws_bytes,
                                moe_stream_t stream, moe_event_t const *stage_events);
 
+/*
+ * moe_build_dispatch_noalloc -- moe_build_dispatch for callers that cannot
+ * allocate device memory.  The pages have no counterpart: this is an
+ * integration aid, not a step of the method.
+ *
+ * Who needs it: a caller with no way to get a scratch buffer, such as a plugin
+ * inside a host framework that owns the whole device-memory budget and gives
+ * its extensions no allocator, or a latency-critical path that must not call
+ * cudaMalloc because the call can synchronise the device.  Such a caller
+ * cannot provide the workspace moe_build_dispatch needs.
+ *
+ * What it does: the same count / prefix sum / permute with the same results
+ * (bit for bit) as moe_build_dispatch; arguments as there, minus the
+ * workspace.  Its scratch lives in one fixed array of
+ * MOE_NOALLOC_SCRATCH_BYTES in this library's device memory, which every GPU
+ * that loads the library holds until the process exits.  The call allocates
+ * nothing and calls no allocating routine.
+ *   device_status  [1] int32 out or NULL: after the call, the status bits of
+ *                  this dispatch (bit 0 set: an expert id outside [0,E) was
+ *                  seen; its assignment was dropped from the layout).
+ * Limit: with N = T*k assignments, nblk = ceil(N / chunk) blocks where
+ *   chunk = max(256, 256 * ceil(ceil(N / 1024) / 256)), the call needs
+ *   256 + 8 * nblk * E bytes; a larger batch returns MOE_ERR_UNSUPPORTED_SHAPE
+ *   and launches nothing.  (E = 128: every T*k; E = 256: T*k <= 131072;
+ *   E = 512: T*k <= 65536.)
+ * Set-up: the first call on each device looks up the array's device address
+ *   (with that device current); make that first call before any stream
+ *   capture.
+ * Sharing: every call uses the same array and it keeps the last call's
+ *   contents (the call clears what must start at zero).  Calls whose work
+ *   overlaps on the GPU -- e.g. on two streams with no ordering between
+ *   them -- race on the array and give wrong results; order them on one
+ *   stream.
+ */
+#define MOE_NOALLOC_SCRATCH_BYTES ((1u << 20) + 256u) /* 1 MiB of tables + status slot */
+moe_status_t moe_build_dispatch_noalloc(const moe_layer_desc_t *d, const int32_t *topk_ids,
+                                        const float *topk_w, int32_t *counts, int32_t *offsets,
+                                        int32_t *perm_src, int32_t *inv_pos, float *w_perm,
+                                        int32_t *device_status, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -230,3 +230,21 @@ def workspace_view(ws, layout: Dict[str, int], name: str, dtype, shape):
         n *= s
     off = layout[name]
     return ws[off:off + n * itemsize].view(dtype).view(*shape)
+
+
+def moe_build_dispatch_noalloc(d: LayerDesc, topk_ids, topk_w, counts, offsets, perm_src, inv_pos,
+                               w_perm, device_status=None, stream=None):
+    """moe_build_dispatch without a workspace, for callers that cannot allocate
+    device memory: the dispatch scratch lives in a fixed array inside the
+    library (MOE_NOALLOC_SCRATCH_BYTES, held until the process exits).  Calls
+    share that array, so calls that overlap on the GPU race; order them on one
+    stream.  Too large a batch raises MoeError(MOE_ERR_UNSUPPORTED_SHAPE)."""
+    f = library().moe_build_dispatch_noalloc
+    if f.argtypes is None:
+        # pointer-width arguments: without argtypes ctypes would pass ints as C int
+        P = ctypes.c_void_p
+        f.argtypes = [ctypes.POINTER(LayerDesc), P, P, P, P, P, P, P, P, P]
+        f.restype = ctypes.c_int32
+    _check("moe_build_dispatch_noalloc", f(
+        ctypes.byref(d), _ptr(topk_ids), _ptr(topk_w), _ptr(counts), _ptr(offsets), _ptr(perm_src),
+        _ptr(inv_pos), _ptr(w_perm), _ptr(device_status), _stream(stream)))

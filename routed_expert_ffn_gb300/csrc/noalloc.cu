@@ -1,0 +1,109 @@
+// moe_build_dispatch_noalloc: the count / prefix-sum / permute dispatch for
+// callers that cannot allocate device memory.
+//
+// Some callers have no way to obtain a scratch buffer: a plugin running inside
+// a host framework that owns the whole device-memory budget and hands its
+// extensions no allocator, or a latency-critical path that must not call
+// cudaMalloc because the call can synchronise the device.  This entry point
+// needs only its inputs and outputs: the dispatch's scratch (the per-block
+// expert histograms and their prefix bases, plus one status word) lives in a
+// fixed-size array in this library's device memory.
+//
+// The array is shared by every call in the process and keeps the previous
+// call's contents; every scratch entry the dispatch reads is written earlier
+// in the same call, and the status word is cleared at the start of each call.
+// Two calls whose work overlaps on the GPU (for example on two streams with
+// no ordering between them) race on the array.
+#include <mutex>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+// Maximum scratch: one status word (padded to 256 bytes) plus two int32
+// tables of nblk x E entries each.
+constexpr size_t kNoAllocScratchBytes = MOE_NOALLOC_SCRATCH_BYTES;
+
+static __device__ __align__(256) unsigned char g_dispatch_scratch[kNoAllocScratchBytes];
+
+// Device address of g_dispatch_scratch per device.  The array's name in host
+// code is only a host-side stand-in, never a device address; the real address
+// is looked up once per device, with that device current, on the first call.
+void *g_scratch_addr[64] = {};
+std::mutex g_scratch_mutex;
+
+moe_status_t scratch_address(void **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_addr[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess || p == nullptr)
+      return MOE_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" moe_status_t moe_build_dispatch_noalloc(const moe_layer_desc_t *d,
+                                                   const int32_t *topk_ids, const float *topk_w,
+                                                   int32_t *counts, int32_t *offsets,
+                                                   int32_t *perm_src, int32_t *inv_pos,
+                                                   float *w_perm, int32_t *device_status,
+                                                   moe_stream_t stream) {
+  if (d == nullptr) return MOE_ERR_INVALID_ARG;
+  if (d->gating < MOE_GATE_TOPK_SOFTMAX || d->gating > MOE_GATE_SIGMOID_BIAS_RENORM ||
+      (d->has_shared_expert != 0 && d->has_shared_expert != 1))
+    return MOE_ERR_INVALID_ARG;
+  if (d->T < 1 || d->T > kMaxT || d->E < 1 || d->E > kMaxE || d->k < 1 || d->k > d->E ||
+      d->k > kMaxK || (int64_t)d->T * d->k > kMaxAssign || d->H < 64 || d->H > 16384 ||
+      d->H % 64 != 0 || d->I < 64 || d->I > 32768 || d->I % 64 != 0)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  auto aligned = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (topk_ids == nullptr || counts == nullptr || offsets == nullptr || perm_src == nullptr ||
+      inv_pos == nullptr || !aligned(topk_ids) || !aligned(counts) || !aligned(offsets) ||
+      !aligned(perm_src) || !aligned(inv_pos) || !aligned(topk_w) || !aligned(w_perm) ||
+      (device_status != nullptr && (reinterpret_cast<uintptr_t>(device_status) & 3u) != 0))
+    return MOE_ERR_INVALID_ARG;
+  if (w_perm != nullptr && topk_w == nullptr) return MOE_ERR_INVALID_ARG;
+
+  // The scratch this batch needs must fit the fixed array.
+  const int64_t Na = (int64_t)d->T * d->k;
+  const int64_t chunk = dispatch_chunk(Na);
+  const int64_t nblk = (Na + chunk - 1) / chunk;
+  const size_t table = (size_t)nblk * d->E * sizeof(int32_t);
+  if (256 + 2 * table > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED_SHAPE;
+
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (major != 10 || minor != 3) return MOE_ERR_UNSUPPORTED_DEVICE;
+
+  void *base = nullptr;
+  moe_status_t st = scratch_address(&base);
+  if (st != MOE_OK) return st;
+  unsigned char *scratch = static_cast<unsigned char *>(base);
+  uint32_t *status = reinterpret_cast<uint32_t *>(scratch);
+  int32_t *blk_counts = reinterpret_cast<int32_t *>(scratch + 256);
+  int32_t *blk_base = reinterpret_cast<int32_t *>(scratch + 256 + table);
+
+  cudaStream_t s = (cudaStream_t)stream;
+  // Only the status word must start at zero: both tables are fully written
+  // before they are read within this call.
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s);
+  if (e == cudaSuccess)
+    e = launch_dispatch(topk_ids, topk_w, d->T, d->k, d->E, blk_counts, blk_base, counts, offsets,
+                        perm_src, inv_pos, w_perm, status, s);
+  if (e == cudaSuccess && device_status != nullptr)
+    e = cudaMemcpyAsync(device_status, status, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

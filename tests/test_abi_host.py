@@ -122,3 +122,30 @@ def test_status_strings(lib):
         s = moe.moe_status_string(code)
         assert s and s != "unknown status"
     assert moe.moe_status_string(-99) == "unknown status"
+
+
+def test_binding_passes_pointer_width_arguments(lib):
+    # Every entry point must be called with pointer-width argument types: a
+    # function left with ctypes' default (C int) would truncate device pointers
+    # and stream handles.  Calling each Python wrapper with an invalid shape
+    # configures its ctypes signature and returns before any launch.
+    bad = qwen3(k=0)
+    t = FAKE
+    for call in (lambda: moe.moe_build_dispatch_noalloc(bad, t, None, t, t, t, t, None, None, t),):
+        with pytest.raises(moe.MoeError) as ei:
+            call()
+        assert ei.value.status == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    text = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "moe.h")).read(), flags=re.S)
+    for name in declared_functions():
+        params = re.search(name + r"\s*\(([^)]*)\)", text).group(1)
+        params = [q.strip() for q in params.split(",") if q.strip()]
+        f = getattr(lib, name)
+        assert f.argtypes is not None, name
+        assert len(f.argtypes) == len(params), name
+        for decl, a in zip(params, f.argtypes):
+            if "*" in decl or decl.startswith("moe_stream_t"):
+                assert a is ctypes.c_void_p or issubclass(a, ctypes._Pointer), (name, decl)
+            elif decl.startswith("size_t"):
+                assert a is ctypes.c_size_t, (name, decl)
+            else:
+                assert a is ctypes.c_int32, (name, decl)
