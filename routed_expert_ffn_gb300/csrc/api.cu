@@ -40,6 +40,7 @@ Layout make_layout(const moe_layer_desc_t &d) {
   L.nblk = (int)((Na + chunk - 1) / chunk);
   L.status = take(256);
   L.route_part = take((size_t)L.route_splits * d.T * d.E * 4);
+  L.router_w = take((size_t)3 * d.E * d.H * 2);
   L.blk_counts = take((size_t)L.nblk * d.E * 4);
   L.blk_base = take((size_t)L.nblk * d.E * 4);
   L.plan = take((size_t)plan_ints(L.nseg) * 4);
@@ -170,7 +171,8 @@ moe_status_t moe_get_device_status(void *workspace, size_t ws_bytes, moe_stream_
     if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (raw != nullptr) *raw = (int32_t)word;
-  if (word & (kStatusTimeoutGateUp | kStatusTimeoutDown)) return MOE_ERR_TIMEOUT;
+  if (word & (kStatusTimeoutGateUp | kStatusTimeoutDown | kStatusTimeoutRouter))
+    return MOE_ERR_TIMEOUT;
   if (word & (kStatusBadExpertId | kStatusBadOffsets)) return MOE_ERR_DEVICE_CHECK;
   return MOE_OK;
 }
@@ -204,7 +206,9 @@ moe_status_t moe_route(const moe_layer_desc_t *d, const void *x, const float *w_
   if ((st = check_device()) != MOE_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
   float *part = at<float>(workspace, L.route_part);
-  cudaError_t e = launch_router_logits(bf(x), w_router, d->T, d->H, d->E, L.route_splits, part, s);
+  cudaError_t e = launch_router_logits(bf(x), w_router, d->T, d->H, d->E, L.route_splits,
+                                       at<__nv_bfloat16>(workspace, L.router_w), part,
+                                       at<uint32_t>(workspace, L.status), s);
   if (e == cudaSuccess)
     e = launch_topk_gating(part, L.route_splits, sel_bias, d->T, d->E, d->k, d->gating, logits,
                            topk_ids, topk_w, boundary_gap, s);
@@ -308,7 +312,8 @@ moe_status_t moe_layer_forward(const moe_layer_desc_t *d, const moe_layer_weight
 
   cudaError_t e = mark(0);
   if (e == cudaSuccess)
-    e = launch_router_logits(bf(x), w->w_router, d->T, d->H, d->E, L.route_splits, part, s);
+    e = launch_router_logits(bf(x), w->w_router, d->T, d->H, d->E, L.route_splits,
+                             at<__nv_bfloat16>(workspace, L.router_w), part, status, s);
   if (e == cudaSuccess)
     e = launch_topk_gating(part, L.route_splits, w->sel_bias, d->T, d->E, d->k, d->gating, logits,
                            ids, tw, at<float>(workspace, L.gap), s);

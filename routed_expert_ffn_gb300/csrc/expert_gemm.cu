@@ -45,6 +45,42 @@
 
 namespace moe {
 
+// ---------------------------------------------------------- tensor maps --
+
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+}  // namespace
+
+// bf16 tensor map with 128-byte swizzle; dims/strides innermost first,
+// strides in bytes for dims 1..rank-1.
+bool encode_bf16_map(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims,
+              const cuuint64_t *strides, const cuuint32_t *box) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), dims,
+            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+
 namespace {
 
 constexpr int kThreads = 192;
@@ -295,50 +331,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- host --
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
-// bf16 tensor map with 128-byte swizzle; dims/strides innermost first,
-// strides in bytes for dims 1..rank-1.
-bool make_map(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims,
-              const cuuint64_t *strides, const cuuint32_t *box) {
-  EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return false;
-  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), dims,
-            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // Weight map viewed as [E][P][rows][K] (P = 2 halves of W13, or 1 for W2).
 bool weight_map(CUtensorMap *m, const void *w, int K, int rows, int P, int E) {
   const cuuint64_t dims[4] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)P, (cuuint64_t)E};
   const cuuint64_t rs = (cuuint64_t)K * 2;
   const cuuint64_t strides[3] = {rs, rs * rows, rs * rows * P};
   const cuuint32_t box[4] = {(cuuint32_t)kBK, (cuuint32_t)kBM, 1, 1};
-  return make_map(m, w, 4, dims, strides, box);
+  return encode_bf16_map(m, w, 4, dims, strides, box);
 }
 
 bool act_map(CUtensorMap *m, const void *a, int K, int64_t R) {
   const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)R};
   const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
   const cuuint32_t box[2] = {(cuuint32_t)kBK, 16};
-  return make_map(m, a, 2, dims, strides, box);
+  return encode_bf16_map(m, a, 2, dims, strides, box);
 }
 
 template <bool kGateUp, int BN, int STAGES>

@@ -19,10 +19,7 @@ constexpr int kMaxK = 32;           // experts per token
 constexpr int kMaxT = 1 << 20;
 constexpr int64_t kMaxAssign = 1 << 24;
 
-// Router logits tile (SIMT fp32): 64 tokens x 64 experts, K chunk 32.
-constexpr int kRouteTT = 64;
-constexpr int kRouteTE = 64;
-constexpr int kRouteBK = 32;
+// Router: at most this many K splits (summed by the gating kernel).
 constexpr int kRouteMaxSplits = 16;
 
 // Dispatch: threads per block; each block takes a chunk of the assignment
@@ -47,6 +44,7 @@ constexpr uint32_t kStatusBadExpertId = 1u << 0;
 constexpr uint32_t kStatusTimeoutGateUp = 1u << 1;
 constexpr uint32_t kStatusTimeoutDown = 1u << 2;
 constexpr uint32_t kStatusBadOffsets = 1u << 3;
+constexpr uint32_t kStatusTimeoutRouter = 1u << 4;
 
 // A bounded pipeline wait gives up after this long (the longest legitimate
 // wait is one tile's mainloop, well under a millisecond).
@@ -55,7 +53,7 @@ constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;
 // ---------------------------------------------------------- workspace --
 
 struct Layout {
-  size_t status, route_part, blk_counts, blk_base, plan, x_perm, h, out_perm;
+  size_t status, route_part, router_w, blk_counts, blk_base, plan, x_perm, h, out_perm;
   size_t logits, topk_ids, topk_w, gap, counts, offsets, perm_src, inv_pos, w_perm;
   size_t total;
   int route_splits;
@@ -77,7 +75,8 @@ inline int plan_ints(int nseg) { return 3 * (nseg + 1); }
 // ------------------------------------------------------------- launches --
 // Each returns cudaSuccess or the launch error.
 cudaError_t launch_router_logits(const __nv_bfloat16 *x, const float *w_router, int T, int H, int E,
-                                 int splits, float *partial, cudaStream_t s);
+                                 int splits, __nv_bfloat16 *w_split, float *partial,
+                                 uint32_t *status, cudaStream_t s);
 cudaError_t launch_topk_gating(const float *partial, int splits, const float *sel_bias, int T,
                                int E, int k, int gating, float *logits, int32_t *ids, float *w,
                                float *gap, cudaStream_t s);
@@ -100,6 +99,12 @@ cudaError_t launch_combine(const float *out_perm, const int32_t *inv_pos,
                            cudaStream_t s);
 
 int num_sms();  // of the current device (cached)
+
+// bf16 tensor map with 128-byte swizzle; dims/strides innermost first,
+// strides in bytes for dims 1..rank-1.  False if the encoder is unavailable
+// or rejects the arguments.
+bool encode_bf16_map(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims,
+                     const cuuint64_t *strides, const cuuint32_t *box);
 
 // ----------------------------------------------------- device helpers --
 

@@ -62,29 +62,41 @@ def selection_keys(s: np.ndarray, gating: int, bias: Optional[np.ndarray]) -> np
 
 def check_routing(gpu_ids: np.ndarray, gpu_w: np.ndarray, ref: Dict[str, np.ndarray], gating: int,
                   bias) -> Dict[str, int]:
-    """Bit-exact ids (and weights within GATE_ATOL) on every token whose oracle
-    boundary gap is >= NEAR_TIE; on near-tie tokens the GPU selection must be a
-    valid top-k of the oracle's keys within NEAR_TIE."""
-    k = gpu_ids.shape[1]
+    """Routing parity.  Off near-ties (oracle boundary gap >= NEAR_TIE) the
+    selected expert set is bit-exact and each expert's gate weight is within
+    GATE_ATOL.  Slot order is best first: two slots may appear swapped only when
+    their keys differ by less than NEAR_TIE (the order of near-equal keys is not
+    unique).  On near-tie tokens the GPU's set must be a valid top-k of the
+    oracle's keys within NEAR_TIE."""
+    T, k = gpu_ids.shape
     gap = ref["gap"]
+    keys = selection_keys(ref["logits"], gating, None if bias is None else np.asarray(bias))
     clear = ~(gap < NEAR_TIE)          # NaN gap (k == E) counts as clear
-    assert np.array_equal(gpu_ids[clear], ref["ids"][clear]), "expert ids differ off near-ties"
-    assert np.max(np.abs(gpu_w[clear] - ref["w"][clear]), initial=0.0) <= GATE_ATOL
+    g_sorted = np.sort(gpu_ids, axis=1)
+    r_sorted = np.sort(ref["ids"], axis=1)
+    assert np.array_equal(g_sorted[clear], r_sorted[clear]), "selected experts differ off near-ties"
+    # gate weight of each selected expert (matched by expert id)
+    go, ro = np.argsort(gpu_ids, axis=1), np.argsort(ref["ids"], axis=1)
+    gw = np.take_along_axis(gpu_w, go, 1)
+    rw = np.take_along_axis(ref["w"], ro, 1)
+    assert np.max(np.abs(gw[clear] - rw[clear]), initial=0.0) <= GATE_ATOL
+    # slot order: non-increasing oracle keys up to near-equal keys
+    kg = np.take_along_axis(keys, gpu_ids.astype(np.int64), 1).astype(np.float64)
+    assert np.all(np.diff(kg, axis=1) <= NEAR_TIE), "slots not in best-first order"
+    swaps = int(np.sum(clear & ~np.all(gpu_ids == ref["ids"], axis=1)))
     ties = np.where(~clear)[0]
     flips = 0
-    if len(ties):
-        keys = selection_keys(ref["logits"], gating, None if bias is None else np.asarray(bias))
-        for t in ties:
-            kth = np.sort(keys[t])[::-1][k - 1]
-            sel = set(gpu_ids[t].tolist())
-            assert len(sel) == k
-            for e in range(keys.shape[1]):
-                if e in sel:
-                    assert keys[t, e] >= kth - NEAR_TIE
-                else:
-                    assert keys[t, e] <= kth + NEAR_TIE
-            flips += int(not np.array_equal(gpu_ids[t], ref["ids"][t]))
-    return {"near_ties": int(len(ties)), "flips": flips}
+    for t in ties:
+        kth = np.sort(keys[t])[::-1][k - 1]
+        sel = set(gpu_ids[t].tolist())
+        assert len(sel) == k
+        for e in range(keys.shape[1]):
+            if e in sel:
+                assert keys[t, e] >= kth - NEAR_TIE
+            else:
+                assert keys[t, e] <= kth + NEAR_TIE
+        flips += int(set(gpu_ids[t].tolist()) != set(ref["ids"][t].tolist()))
+    return {"near_ties": int(len(ties)), "flips": flips, "order_swaps": swaps}
 
 
 class LayerRun:
