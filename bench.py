@@ -139,7 +139,9 @@ def algorithmic(cfg, T, counts):
     layer_bytes = (touched + nsh) * per_expert + E * H * 4 + 2 * T * H * 2
     layer_flops = 2 * T * k * 3 * H * I + nsh * 2 * T * 3 * H * I + 2 * T * H * E
     rows = T * k + nsh * T
-    gateup_bytes = (touched + nsh) * 2 * I * H * 2 + rows * H * 2 + rows * I * 2
+    # the gate/up kernel reads each token row of x once from HBM (its k-fold
+    # reuse is served by L2) and writes h
+    gateup_bytes = (touched + nsh) * 2 * I * H * 2 + T * H * 2 + rows * I * 2
     gateup_flops = 2 * rows * 2 * I * H
     return {"touched": touched, "layer_bytes": layer_bytes, "layer_flops": layer_flops,
             "gateup_bytes": gateup_bytes, "gateup_flops": gateup_flops}
