@@ -51,7 +51,8 @@ enum {
   MOE_ERR_UNSUPPORTED_SHAPE = -2,   /* a size outside the limits above            */
   MOE_ERR_WORKSPACE_TOO_SMALL = -3, /* ws_bytes < moe_workspace_size(desc)        */
   MOE_ERR_CUDA = -4,                /* a CUDA runtime / launch error              */
-  MOE_ERR_DEVICE_CHECK = -5,        /* device saw invalid metadata (expert id)    */
+  MOE_ERR_DEVICE_CHECK = -5,        /* invalid metadata (expert id, offsets) or an
+                                       expert output beyond fp16 range            */
   MOE_ERR_TIMEOUT = -6,             /* a bounded device pipeline wait ran out     */
   MOE_ERR_UNSUPPORTED_DEVICE = -7   /* current device is not compute capability 10.3 */
 };
@@ -125,7 +126,7 @@ typedef struct {
   size_t w_perm;       /* [T*k] fp32 gate weight in permuted order        */
   size_t x_perm;       /* [R,H] bf16 tokens grouped by expert             */
   size_t h;            /* [R,I] bf16 SiLU(gate)*up                        */
-  size_t out_perm;     /* [R,H] fp32 gate-weighted expert outputs         */
+  size_t out_perm;     /* [R,H] fp16 gate-weighted expert outputs         */
   size_t total;        /* == moe_workspace_size(desc)                     */
 } moe_workspace_layout_t;
 
@@ -213,9 +214,10 @@ moe_status_t moe_build_dispatch(const moe_layer_desc_t *d, const int32_t *topk_i
  *   w13, w2      routed expert weights; w13_shared / w2_shared required iff
  *                d->has_shared_expert (run as one more segment of all T tokens
  *                with weight 1, stored in rows [T*k, T*k+T) of out_perm)
- *   out_perm     [R,H] fp32 out, R = T*k + (shared ? T : 0).  fp32 so that
- *                the combine adds the k rows of a token without rounding each
- *                to bf16 first (h, the down GEMM's operand, is bf16).
+ *   out_perm     [R,H] fp16 out, R = T*k + (shared ? T : 0).  fp16 carries
+ *                11 significant bits -- 8x finer than bf16 -- so the k rows a
+ *                token sums stay accurate; an element beyond +-65504 is
+ *                clamped and latches MOE_ERR_DEVICE_CHECK in the status word.
  * Uses the workspace for x_perm, h and the tile plan.  Experts with no rows
  * read no weights.
  */
@@ -235,7 +237,7 @@ moe_status_t moe_grouped_swiglu_ffn(const moe_layer_desc_t *d, const void *x,
  *            when d->has_shared_expert)
  *   wt(t,j) = topk_w[t*k+j], or 1 when topk_w is NULL (weights already applied
  *            by moe_grouped_swiglu_ffn)
- *   out_perm [R,H] fp32 (as written by moe_grouped_swiglu_ffn)
+ *   out_perm [R,H] fp16 (as written by moe_grouped_swiglu_ffn)
  *   y        [T,H] bf16 out; sums in fp32 in slot order, rounded once.
  */
 moe_status_t moe_combine(const moe_layer_desc_t *d, const void *out_perm, const int32_t *inv_pos,

@@ -38,15 +38,27 @@ def _stale(obj: str, src: str) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False,
+          defines=None, lib_path: str = None) -> str:
+    """Compile the library.  ``defines`` ({name: value}) override the kernels'
+    compile-time tile parameters (MOE_BN_GATEUP, MOE_BN_DOWN, MOE_STAGES_GATEUP,
+    MOE_STAGES_DOWN); such a variant is built in its own directory into
+    ``lib_path``."""
+    build_dir, lib = BUILD, LIB
+    extra = []
+    if defines:
+        tag = "_".join(f"{k}{v}" for k, v in sorted(defines.items()))
+        build_dir = os.path.join(BUILD, tag)
+        lib = lib_path or os.path.join(build_dir, "libmoe_gb300.so")
+        extra = [f"-D{k}={v}" for k, v in sorted(defines.items())]
+    os.makedirs(build_dir, exist_ok=True)
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
-                    "-I", os.path.join(ROOT, "include"), "--expt-relaxed-constexpr"]
+                    "-I", os.path.join(ROOT, "include"), "--expt-relaxed-constexpr"] + extra
     if ptxas_verbose:
         flags += ["-Xptxas", "-v"]
     jobs = []
     for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         if force or ptxas_verbose or _stale(obj, src):
             jobs.append([nvcc(), *flags, "-c", src, "-o", obj])
 
@@ -64,14 +76,14 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
                     failed.append(os.path.basename(cmd[-3]))
     if failed:
         raise RuntimeError(f"nvcc failed for {failed}")
-    objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in sources()]
-    if force or jobs or not os.path.exists(LIB):
-        tmp = LIB + f".tmp{os.getpid()}"
+    objs = [os.path.join(build_dir, os.path.basename(s)[:-3] + ".o") for s in sources()]
+    if force or jobs or not os.path.exists(lib):
+        tmp = lib + f".tmp{os.getpid()}"
         cuda_lib = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "lib64")
         subprocess.check_call([nvcc(), *ARCH, "-shared", "-cudart", "shared", *objs, "-o", tmp,
                                "-Xlinker", f"-rpath,{cuda_lib}"])
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

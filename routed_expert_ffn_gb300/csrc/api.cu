@@ -55,7 +55,7 @@ Layout make_layout(const moe_layer_desc_t &d) {
   L.w_perm = take((size_t)Na * 4);
   L.x_perm = take((size_t)L.rows * d.H * 2);
   L.h = take((size_t)L.rows * d.I * 2);
-  L.out_perm = take((size_t)L.rows * d.H * 4);
+  L.out_perm = take((size_t)L.rows * d.H * 2);
   L.total = off;
   return L;
 }
@@ -173,7 +173,7 @@ moe_status_t moe_get_device_status(void *workspace, size_t ws_bytes, moe_stream_
   if (raw != nullptr) *raw = (int32_t)word;
   if (word & (kStatusTimeoutGateUp | kStatusTimeoutDown | kStatusTimeoutRouter))
     return MOE_ERR_TIMEOUT;
-  if (word & (kStatusBadExpertId | kStatusBadOffsets)) return MOE_ERR_DEVICE_CHECK;
+  if (word & (kStatusBadExpertId | kStatusBadOffsets | kStatusRange)) return MOE_ERR_DEVICE_CHECK;
   return MOE_OK;
 }
 
@@ -184,7 +184,9 @@ const char *moe_status_string(moe_status_t s) {
     case MOE_ERR_UNSUPPORTED_SHAPE: return "shape outside the supported limits";
     case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than moe_workspace_size()";
     case MOE_ERR_CUDA: return "CUDA runtime or launch error";
-    case MOE_ERR_DEVICE_CHECK: return "device check failed (expert id or offsets out of range)";
+    case MOE_ERR_DEVICE_CHECK:
+      return "device check failed (expert id or offsets out of range, or an expert output "
+             "beyond the fp16 range of out_perm)";
     case MOE_ERR_TIMEOUT: return "a bounded device pipeline wait timed out";
     case MOE_ERR_UNSUPPORTED_DEVICE: return "current device is not compute capability 10.3";
     default: return "unknown status";
@@ -261,7 +263,7 @@ moe_status_t moe_grouped_swiglu_ffn(const moe_layer_desc_t *d, const void *x,
                                      d->has_shared_expert, x_perm, plan, status, s);
   if (e == cudaSuccess) e = launch_expert_gateup(*d, w13, w13_shared, x_perm, plan, h, status, s);
   if (e == cudaSuccess)
-    e = launch_expert_down(*d, w2, w2_shared, h, plan, w_perm, static_cast<float *>(out_perm),
+    e = launch_expert_down(*d, w2, w2_shared, h, plan, w_perm, static_cast<__half *>(out_perm),
                            status, s);
   return cuda_status(e);
 }
@@ -274,7 +276,7 @@ moe_status_t moe_combine(const moe_layer_desc_t *d, const void *out_perm, const 
   if (!ok_ptr(out_perm) || !ok_ptr(inv_pos) || !ok_opt(topk_w) || !ok_ptr(y))
     return MOE_ERR_INVALID_ARG;
   if ((st = check_device()) != MOE_OK) return st;
-  return cuda_status(launch_combine(static_cast<const float *>(out_perm), inv_pos, topk_w, d->T,
+  return cuda_status(launch_combine(static_cast<const __half *>(out_perm), inv_pos, topk_w, d->T,
                                     d->k, d->H,
                                     d->has_shared_expert, bfw(y), (cudaStream_t)stream));
 }
@@ -307,7 +309,7 @@ moe_status_t moe_layer_forward(const moe_layer_desc_t *d, const moe_layer_weight
   int32_t *plan = at<int32_t>(workspace, L.plan);
   __nv_bfloat16 *x_perm = at<__nv_bfloat16>(workspace, L.x_perm);
   __nv_bfloat16 *h = at<__nv_bfloat16>(workspace, L.h);
-  float *out_perm = at<float>(workspace, L.out_perm);
+  __half *out_perm = at<__half>(workspace, L.out_perm);
   float *part = at<float>(workspace, L.route_part);
 
   cudaError_t e = mark(0);

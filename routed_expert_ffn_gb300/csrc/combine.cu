@@ -5,7 +5,7 @@
 //
 //   y[t,:] = sum_j wt(t,j) * out_perm[inv_pos[t*k+j],:]  (+ out_perm[T*k+t,:])
 //
-// One thread per 8 columns of a token row; the k fp32 expert rows of a token
+// One thread per 8 columns of a token row; the k fp16 expert rows of a token
 // are gathered with 16-byte loads and summed in fp32 in slot order; y is
 // rounded to bf16 once.
 #include "moe_internal.cuh"
@@ -15,7 +15,7 @@ namespace moe {
 namespace {
 
 __global__ void __launch_bounds__(256)
-    combine_kernel(const float *__restrict__ out_perm, const int32_t *__restrict__ inv_pos,
+    combine_kernel(const __half *__restrict__ out_perm, const int32_t *__restrict__ inv_pos,
                    const float *__restrict__ topk_w, int T, int k, int H, int shared,
                    __nv_bfloat16 *__restrict__ y) {
   const int t = blockIdx.x;
@@ -27,11 +27,14 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
   auto add_row = [&](int64_t row, float wt) {
-    const float4 *src = reinterpret_cast<const float4 *>(out_perm + row * H) + 2 * v;
-    const float4 a = src[0], b = src[1];
-    const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    const uint4 raw = reinterpret_cast<const uint4 *>(out_perm + row * H)[v];
+    const __half2 *p = reinterpret_cast<const __half2 *>(&raw);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = fmaf(wt, f[i], acc[i]);
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __half22float2(p[i]);
+      acc[2 * i] = fmaf(wt, f.x, acc[2 * i]);
+      acc[2 * i + 1] = fmaf(wt, f.y, acc[2 * i + 1]);
+    }
   };
   for (int j = 0; j < k; ++j) {
     const int64_t a = (int64_t)t * k + j;
@@ -49,7 +52,7 @@ __global__ void __launch_bounds__(256)
 
 }  // namespace
 
-cudaError_t launch_combine(const float *out_perm, const int32_t *inv_pos,
+cudaError_t launch_combine(const __half *out_perm, const int32_t *inv_pos,
                            const float *topk_w, int T, int k, int H, int shared, __nv_bfloat16 *y,
                            cudaStream_t s) {
   const int nv = H / 8;

@@ -166,9 +166,8 @@ __global__ void __launch_bounds__(256)
       const int s = s0 + q;
       int m = 0;
       if (!bad && s < nseg) m = (s < E) ? offsets[s + 1] - offsets[s] : T;
-      const int chunks = (m + kBN - 1) / kBN;
-      gu[q] = chunks * nj_gu;
-      dn[q] = chunks * nj_dn;
+      gu[q] = (m + kBNGateUp - 1) / kBNGateUp * nj_gu;
+      dn[q] = (m + kBNDown - 1) / kBNDown * nj_dn;
       sum_gu += gu[q];
       sum_dn += dn[q];
       if (s < nseg) seg_row[s] = bad ? 0 : ((s < E) ? offsets[s] : (int)Na);

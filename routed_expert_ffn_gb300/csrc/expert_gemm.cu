@@ -36,7 +36,7 @@
 //               tile overlap the mainloop of the next;
 //   warps 0-3   epilogue: tcgen05.ld of their 32 TMEM lanes (= 32 weight
 //               rows), fused SiLU(gate)*up (gate/up GEMM) or gate weighting
-//               (down GEMM), bf16 (h) or fp32 (out_perm) stores.
+//               (down GEMM), bf16 (h) or fp16 (out_perm) stores.
 // Every wait is bounded; on expiry the CTA records MOE_ERR_TIMEOUT's status
 // bit, drains its copies and MMAs in flight, frees TMEM and returns.
 #include <stdio.h>
@@ -84,8 +84,8 @@ bool encode_bf16_map(CUtensorMap *m, const void *base, int rank, const cuuint64_
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kStagesGateUp = 4;
-constexpr int kStagesDown = 6;
+constexpr int kStagesGateUp = MOE_STAGES_GATEUP;
+constexpr int kStagesDown = MOE_STAGES_DOWN;
 
 __host__ __device__ constexpr uint32_t tmem_cols_pow2(uint32_t n) {
   return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : n <= 256 ? 256 : 512;
@@ -101,8 +101,10 @@ struct Cfg {
   static constexpr uint32_t ACC_COLS = NA * BN;            // TMEM columns per tile
   static constexpr uint32_t TMEM_COLS = tmem_cols_pow2(2 * ACC_COLS);
   static constexpr uint32_t BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
+  static constexpr uint32_t STAGE_OUT_BYTES = 16 * kBM * 2;  // one 16-token output slice
   static size_t smem_bytes(int nseg) {
-    return 1024 + (size_t)STAGES * STAGE_BYTES + BAR_BYTES + (size_t)2 * (nseg + 1) * 4;
+    return 1024 + (size_t)STAGES * STAGE_BYTES + STAGE_OUT_BYTES + (size_t)BN * 4 + BAR_BYTES +
+           (size_t)2 * (nseg + 1) * 4;
   }
   static_assert(2 * ACC_COLS <= 512, "accumulators exceed TMEM");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "bad token tile");
@@ -111,6 +113,24 @@ struct Cfg {
 struct Tile {
   int seg, j, row0, nrows;
 };
+
+// Named barrier 1 over the 128 epilogue threads (warps 0-3).
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// The same barrier with an AND reduction: every epilogue thread gets the same
+// answer, so all 128 take the same branch before the next epi_sync.
+__device__ __forceinline__ bool epi_all(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred a, b;\n\t"
+      "setp.ne.u32 a, %1, 0;\n\t"
+      "bar.red.and.pred b, 1, 128, a;\n\t"
+      "selp.u32 %0, 1, 0, b;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)p)
+      : "memory");
+  return r != 0;
+}
 
 template <int BN>
 __device__ __forceinline__ Tile decode_tile(int tile, const int32_t *seg_row, const int32_t *pref,
@@ -144,17 +164,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                        int64_t Na, const float *__restrict__ w_perm, void *__restrict__ out_,
                        uint32_t *__restrict__ status) {
   using C = Cfg<kGateUp, BN, STAGES>;
-  // gate/up writes h in bf16 (the next GEMM's operand); down writes fp32
-  // gate-weighted rows, so the combine adds k rows without another rounding
-  __nv_bfloat16 *out_h = static_cast<__nv_bfloat16 *>(out_);
-  float *out_f = static_cast<float *>(out_);
+  // gate/up writes h in bf16 (the next GEMM's operand); down writes the
+  // gate-weighted rows in fp16: 11 significant bits (8x finer than bf16) at
+  // the same bandwidth; magnitudes past the fp16 range are clamped and
+  // latched in the status word.  Both are 2-byte elements.
+  uint16_t *out = static_cast<uint16_t *>(out_);
   constexpr uint32_t kCode = kGateUp ? kStatusTimeoutGateUp : kStatusTimeoutDown;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   uint8_t *sA = smem;                                  // [STAGES][NA][A_BYTES]
   uint8_t *sB = sA + (size_t)STAGES * C::NA * C::A_BYTES;  // [STAGES][B_BYTES]
-  uint64_t *full = reinterpret_cast<uint64_t *>(sB + (size_t)STAGES * C::B_BYTES);
+  uint16_t *sOut = reinterpret_cast<uint16_t *>(sB + (size_t)STAGES * C::B_BYTES);  // [16][kBM]
+  float *sW = reinterpret_cast<float *>(sOut + 16 * kBM);  // [BN] gate weights (down)
+  uint64_t *full = reinterpret_cast<uint64_t *>(sW + BN);
   uint64_t *empty = full + STAGES;
   uint64_t *tfull = empty + STAGES;
   uint64_t *tempty = tfull + 2;
@@ -277,49 +300,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // --------------------------------------------------------- epilogue --
+    // Per 16-token slice: tcgen05.ld of the thread's weight row (16 token
+    // columns), fused SiLU(gate)*up or gate weighting, the slice written
+    // transposed into smem, then stored as token rows with 16-byte vector
+    // stores by all 128 epilogue threads.
+    const int r = warp * 32 + lane;  // TMEM lane = weight row of the tile
     uint32_t tl = 0;
+    bool range_bad = false;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++tl) {
       const Tile t = decode_tile<BN>(tile, seg_row, pref, nseg);
       const uint32_t buf = tl & 1u, use = tl >> 1;
-      // all lanes must agree before the warp-wide tcgen05.ld below
-      if (!__all_sync(0xffffffffu, mbar_wait(&tfull[buf], use & 1u, abort_flag, status, kCode)))
-        break;
+      const bool waited = mbar_wait(&tfull[buf], use & 1u, abort_flag, status, kCode);
+      // one decision for all 128 epilogue threads: they share named barriers
+      if (!epi_all(waited && !*abort_flag)) break;
       tc_fence_after();
-      const int col = t.j * kBM + warp * 32 + lane;  // output column = weight row
+      if (!kGateUp) {
+        for (int n = r; n < BN; n += 128) {
+          const int64_t row = (int64_t)t.row0 + n;
+          sW[n] = (n < t.nrows && w_perm != nullptr && row < Na) ? w_perm[row] : 1.0f;
+        }
+        epi_sync();
+      }
       const uint32_t tb = tmem_base + ((uint32_t)(warp * 32) << 16) + buf * C::ACC_COLS;
       const int N = (t.nrows + 15) & ~15;
+      const int col0 = t.j * kBM;
       for (int n0 = 0; n0 < N; n0 += 16) {
         uint32_t v0[16], v1[16];
         tmem_ld16(tb + n0, v0);
         if (kGateUp) tmem_ld16(tb + BN + n0, v1);
         tmem_ld_wait();
-        if (col < out_cols) {
 #pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            const int n = n0 + q;
-            if (n < t.nrows) {
-              const int64_t row = (int64_t)t.row0 + n;
-              float val;
-              if (kGateUp) {
-                const float g = __uint_as_float(v0[q]);
-                const float u = __uint_as_float(v1[q]);
-                val = g / (1.0f + __expf(-g)) * u;
-              } else {
-                const float wt = (w_perm != nullptr && row < Na) ? w_perm[row] : 1.0f;
-                val = __uint_as_float(v0[q]) * wt;
-              }
-              if (kGateUp)
-                out_h[row * out_cols + col] = __float2bfloat16_rn(val);
-              else
-                out_f[row * out_cols + col] = val;
-            }
+        for (int q = 0; q < 16; ++q) {
+          uint16_t bits;
+          if (kGateUp) {
+            const float g = __uint_as_float(v0[q]);
+            const float u = __uint_as_float(v1[q]);
+            bits = __bfloat16_as_ushort(__float2bfloat16_rn(g / (1.0f + __expf(-g)) * u));
+          } else {
+            const float val = __uint_as_float(v0[q]) * sW[n0 + q];
+            range_bad |= !(fabsf(val) <= 65504.0f);
+            bits = __half_as_ushort(__float2half_rn(fminf(fmaxf(val, -65504.0f), 65504.0f)));
           }
+          sOut[q * kBM + r] = bits;
         }
+        epi_sync();
+        // 16 token rows x 128 columns x 2 bytes = 256 chunks of 16 bytes
+        for (int c = r; c < 16 * (kBM / 8); c += 128) {
+          const int q = c / (kBM / 8), ch = c % (kBM / 8);
+          const int n = n0 + q, col = col0 + ch * 8;
+          if (n < t.nrows && col < out_cols)
+            *reinterpret_cast<uint4 *>(out + ((int64_t)t.row0 + n) * out_cols + col) =
+                *reinterpret_cast<const uint4 *>(sOut + q * kBM + ch * 8);
+        }
+        epi_sync();
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[buf]);
     }
+    if (range_bad) atomicOr(status, kStatusRange);
   }
 
   __syncthreads();
@@ -352,7 +391,7 @@ cudaError_t launch_gemm(const moe_layer_desc_t &d, const void *w, const void *w_
                         const __nv_bfloat16 *act, const int32_t *plan, const float *w_perm,
                         void *out, uint32_t *status, cudaStream_t s) {
   using C = Cfg<kGateUp, BN, STAGES>;
-  static_assert(BN == kBN, "the tile plan assumes kBN-row token chunks");
+  static_assert(BN == (kGateUp ? kBNGateUp : kBNDown), "the tile plan's token chunks");
   const int shared = d.has_shared_expert ? 1 : 0;
   const int nseg = d.E + shared;
   const int64_t Na = (int64_t)d.T * d.k;
@@ -393,14 +432,14 @@ cudaError_t launch_gemm(const moe_layer_desc_t &d, const void *w, const void *w_
 cudaError_t launch_expert_gateup(const moe_layer_desc_t &d, const void *w13, const void *w13_shared,
                                  const __nv_bfloat16 *x_perm, const int32_t *plan,
                                  __nv_bfloat16 *h, uint32_t *status, cudaStream_t s) {
-  return launch_gemm<true, kBN, kStagesGateUp>(d, w13, w13_shared, x_perm, plan, nullptr, h,
+  return launch_gemm<true, kBNGateUp, kStagesGateUp>(d, w13, w13_shared, x_perm, plan, nullptr, h,
                                                status, s);
 }
 
 cudaError_t launch_expert_down(const moe_layer_desc_t &d, const void *w2, const void *w2_shared,
                                const __nv_bfloat16 *h, const int32_t *plan, const float *w_perm,
-                               float *out_perm, uint32_t *status, cudaStream_t s) {
-  return launch_gemm<false, kBN, kStagesDown>(d, w2, w2_shared, h, plan, w_perm, out_perm, status,
+                               __half *out_perm, uint32_t *status, cudaStream_t s) {
+  return launch_gemm<false, kBNDown, kStagesDown>(d, w2, w2_shared, h, plan, w_perm, out_perm, status,
                                               s);
 }
 

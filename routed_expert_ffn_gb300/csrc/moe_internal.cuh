@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -33,11 +34,24 @@ inline int64_t dispatch_chunk(int64_t Na) {
   return c < kDispatchThreads ? kDispatchThreads : c;
 }
 
-// Expert GEMMs (tcgen05): weight rows per tile, K per pipeline stage, token
-// rows per tile.
+// Expert GEMMs (tcgen05): weight rows per tile, K per pipeline stage, and the
+// token rows per tile (chunk) of each GEMM, with its smem pipeline depth.
+#ifndef MOE_BN_GATEUP
+#define MOE_BN_GATEUP 128
+#endif
+#ifndef MOE_BN_DOWN
+#define MOE_BN_DOWN 128
+#endif
+#ifndef MOE_STAGES_GATEUP
+#define MOE_STAGES_GATEUP 4
+#endif
+#ifndef MOE_STAGES_DOWN
+#define MOE_STAGES_DOWN 6
+#endif
 constexpr int kBM = 128;
 constexpr int kBK = 64;
-constexpr int kBN = 128;
+constexpr int kBNGateUp = MOE_BN_GATEUP;
+constexpr int kBNDown = MOE_BN_DOWN;
 
 // Status word bits (latched with atomicOr).
 constexpr uint32_t kStatusBadExpertId = 1u << 0;
@@ -45,6 +59,7 @@ constexpr uint32_t kStatusTimeoutGateUp = 1u << 1;
 constexpr uint32_t kStatusTimeoutDown = 1u << 2;
 constexpr uint32_t kStatusBadOffsets = 1u << 3;
 constexpr uint32_t kStatusTimeoutRouter = 1u << 4;
+constexpr uint32_t kStatusRange = 1u << 5;  // a gate-weighted expert output beyond fp16 range
 
 // A bounded pipeline wait gives up after this long (the longest legitimate
 // wait is one tile's mainloop, well under a millisecond).
@@ -93,8 +108,8 @@ cudaError_t launch_expert_gateup(const moe_layer_desc_t &d, const void *w13, con
                                  __nv_bfloat16 *h, uint32_t *status, cudaStream_t s);
 cudaError_t launch_expert_down(const moe_layer_desc_t &d, const void *w2, const void *w2_shared,
                                const __nv_bfloat16 *h, const int32_t *plan, const float *w_perm,
-                               float *out_perm, uint32_t *status, cudaStream_t s);
-cudaError_t launch_combine(const float *out_perm, const int32_t *inv_pos,
+                               __half *out_perm, uint32_t *status, cudaStream_t s);
+cudaError_t launch_combine(const __half *out_perm, const int32_t *inv_pos,
                            const float *topk_w, int T, int k, int H, int shared, __nv_bfloat16 *y,
                            cudaStream_t s);
 

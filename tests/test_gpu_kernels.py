@@ -170,7 +170,7 @@ def test_grouped_ffn_and_combine(T, H, I, E, k, shared, skew):
     inv = torch.empty(T * k, dtype=torch.int32, device="cuda")
     wp = torch.empty(T * k, dtype=torch.float32, device="cuda")
     R = T * k + (T if shared else 0)
-    out = torch.empty((R, H), dtype=torch.float32, device="cuda")
+    out = torch.empty((R, H), dtype=torch.float16, device="cuda")
     y = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
     moe.moe_build_dispatch(d, dev(ids), dev(w), counts, offsets, perm, inv, wp, ws)
     moe.moe_grouped_swiglu_ffn(d, dev(x), perm, offsets, wp, dev(w13), dev(w2), dev(w13s), dev(w2s),
@@ -198,7 +198,7 @@ def test_combine_exact_sum():
     T, k, H, E = 50, 4, 256, 16
     ids = synth.random_ids(T, k, E, 1).numpy()
     _, _, rp, ri = oracle.dispatch(ids, E)
-    rows = synth.normal((T * k + T, H), 1, 9, 1.0, torch.float32)
+    rows = synth.normal((T * k + T, H), 1, 9, 1.0, torch.float16)
     tw = synth.normal((T, k), 1, 10, 1.0, torch.float32)
     for shared in (False, True):
         d = moe.desc(T, H, E, k, 64, 0, shared)
@@ -214,3 +214,26 @@ def test_combine_exact_sum():
                 ref[t] += r[T * k + t]
         got = bf16_np(y)
         assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-5)
+
+
+def test_out_of_fp16_range_output_is_clamped_and_flagged():
+    # an expert whose output exceeds the fp16 range of out_perm: the element is
+    # clamped (never inf) and the status word reports a device check
+    T, H, I, E, k = 8, 128, 64, 2, 1
+    x, w13, w2, _, _, _, _ = _ffn_case(T, H, I, E, k, seed=3)
+    w2 = (w2.float() * 1.0e6).to(torch.bfloat16)
+    ids = torch.zeros((T, k), dtype=torch.int32)
+    w = torch.ones((T, k), dtype=torch.float32)
+    d = moe.desc(T, H, E, k, I, 0)
+    ws = moe.alloc_workspace(d)
+    z = lambda n, dt: torch.empty(n, dtype=dt, device="cuda")
+    counts, offsets, perm, inv, wp = (z(E, torch.int32), z(E + 1, torch.int32), z(T * k, torch.int32),
+                                      z(T * k, torch.int32), z(T * k, torch.float32))
+    out = z((T * k, H), torch.float16)
+    moe.moe_build_dispatch(d, ids.cuda(), w.cuda(), counts, offsets, perm, inv, wp, ws)
+    moe.moe_grouped_swiglu_ffn(d, x.cuda(), perm, offsets, wp, w13.cuda(), w2.cuda(), None, None,
+                               out, ws)
+    st, raw = moe.moe_get_device_status(ws)
+    assert st == moe.MOE_ERR_DEVICE_CHECK and raw & (1 << 5)
+    o = out.float()
+    assert torch.isfinite(o).all() and o.abs().max().item() == 65504.0
