@@ -18,6 +18,8 @@ __global__ void __launch_bounds__(256)
     combine_kernel(const __half *__restrict__ out_perm, const int32_t *__restrict__ inv_pos,
                    const float *__restrict__ topk_w, int T, int k, int H, int shared,
                    __nv_bfloat16 *__restrict__ y) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int t = blockIdx.x;
   const int v = blockIdx.y * blockDim.x + threadIdx.x;
   const int nv = H / 8;
@@ -57,8 +59,8 @@ cudaError_t launch_combine(const __half *out_perm, const int32_t *inv_pos,
                            cudaStream_t s) {
   const int nv = H / 8;
   dim3 grid(T, (nv + 255) / 256);
-  combine_kernel<<<grid, 256, 0, s>>>(out_perm, inv_pos, topk_w, T, k, H, shared, y);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, grid, dim3(256), 0, s, out_perm, inv_pos, topk_w, T, k, H,
+                    shared, y);
 }
 
 }  // namespace moe

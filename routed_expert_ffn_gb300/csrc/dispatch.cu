@@ -24,6 +24,8 @@ constexpr int kWarps = kDispatchThreads / 32;
 __global__ void __launch_bounds__(kDispatchThreads)
     dispatch_hist_kernel(const int32_t *__restrict__ ids, int64_t Na, int64_t chunk, int E,
                          int32_t *__restrict__ blk_counts, uint32_t *__restrict__ status) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ int cnt[kMaxE];
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
@@ -74,6 +76,8 @@ __global__ void __launch_bounds__(kMaxE)
     dispatch_scan_kernel(const int32_t *__restrict__ blk_counts, int nblk, int E,
                          int32_t *__restrict__ blk_base, int32_t *__restrict__ counts,
                          int32_t *__restrict__ offsets) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ int warp_tot[32];
   __shared__ int total;
   const int e = threadIdx.x;
@@ -99,6 +103,8 @@ __global__ void __launch_bounds__(kDispatchThreads)
                             const int32_t *__restrict__ blk_base,
                             int32_t *__restrict__ perm_src, int32_t *__restrict__ inv_pos,
                             float *__restrict__ w_perm) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ int base[kMaxE];
   __shared__ int wcnt[kWarps][kMaxE];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -140,6 +146,8 @@ __global__ void __launch_bounds__(256)
                        const int32_t *__restrict__ offsets, int T, int k, int E, int H, int I,
                        int shared, __nv_bfloat16 *__restrict__ x_perm, int32_t *__restrict__ plan,
                        uint32_t *__restrict__ status) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t Na = (int64_t)T * k;
   const int64_t R = Na + (shared ? T : 0);
   if (blockIdx.x == gridDim.x - 1) {
@@ -212,6 +220,73 @@ __global__ void __launch_bounds__(256)
   for (int v = lane; v < nv; v += 32) dst[v] = s[v];
 }
 
+// Small batches (N_a <= kSmallDispatch): histogram, scan and stable scatter
+// in one block, so the dispatch is one launch.  The ranking is the same as
+// the multi-block path's: chunks of the block size in order, warps in order
+// inside a chunk (per-warp counts), lanes in order inside a warp
+// (__match_any_sync).
+constexpr int kSmallThreads = 512;
+constexpr int kSmallWarps = kSmallThreads / 32;
+
+__global__ void __launch_bounds__(kSmallThreads)
+    dispatch_small_kernel(const int32_t *__restrict__ ids, const float *__restrict__ topk_w,
+                          int64_t Na, int E, int32_t *__restrict__ counts,
+                          int32_t *__restrict__ offsets, int32_t *__restrict__ perm_src,
+                          int32_t *__restrict__ inv_pos, float *__restrict__ w_perm,
+                          uint32_t *__restrict__ status) {
+  pdl_wait();
+  pdl_launch_dependents();
+  __shared__ int base[kMaxE];
+  __shared__ int wcnt[kSmallWarps][kMaxE];
+  __shared__ int warp_tot[32];
+  __shared__ int total;
+  const int w = threadIdx.x >> 5;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) base[e] = 0;
+  __syncthreads();
+  bool bad = false;
+  for (int64_t a = threadIdx.x; a < Na; a += blockDim.x) {
+    const int e = ids[a];
+    if (e >= 0 && e < E)
+      atomicAdd(&base[e], 1);
+    else
+      bad = true;
+  }
+  if (bad) atomicOr(status, kStatusBadExpertId);
+  __syncthreads();
+  const int cnt = (threadIdx.x < E) ? base[threadIdx.x] : 0;
+  const int excl = block_exclusive_scan(cnt, warp_tot, &total);
+  if (threadIdx.x < E) {
+    counts[threadIdx.x] = cnt;
+    offsets[threadIdx.x] = excl;
+    base[threadIdx.x] = excl;
+  }
+  if (threadIdx.x == 0) offsets[E] = total;
+  __syncthreads();
+  for (int64_t sub = 0; sub < Na; sub += kSmallThreads) {
+    for (int i = threadIdx.x; i < kSmallWarps * E; i += blockDim.x) wcnt[i / E][i % E] = 0;
+    __syncthreads();
+    const int64_t a = sub + threadIdx.x;
+    int e = (a < Na) ? ids[a] : -1;
+    if (e < 0 || e >= E) e = -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    const uint32_t below = peers & lanemask_lt();
+    const bool leader = (below == 0);
+    if (e >= 0 && leader) wcnt[w][e] = __popc(peers);
+    __syncthreads();
+    if (e >= 0) {
+      int before = 0;
+      for (int ww = 0; ww < w; ++ww) before += wcnt[ww][e];
+      const int pos = base[e] + before + __popc(below);
+      perm_src[pos] = (int32_t)a;
+      inv_pos[a] = pos;
+      if (w_perm != nullptr) w_perm[pos] = topk_w[a];
+    }
+    __syncthreads();
+    if (e >= 0 && leader) atomicAdd(&base[e], __popc(peers));
+    __syncthreads();
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_dispatch(const int32_t *ids, const float *topk_w, int T, int k, int E,
@@ -219,13 +294,21 @@ cudaError_t launch_dispatch(const int32_t *ids, const float *topk_w, int T, int 
                             int32_t *offsets, int32_t *perm_src, int32_t *inv_pos, float *w_perm,
                             uint32_t *status, cudaStream_t s) {
   const int64_t Na = (int64_t)T * k;
+  if (Na <= kSmallDispatch) {
+    return launch_pdl(dispatch_small_kernel, dim3(1), dim3(kSmallThreads), 0, s, ids, topk_w, Na, E,
+                      counts, offsets, perm_src, inv_pos, w_perm, status);
+  }
   const int64_t chunk = dispatch_chunk(Na);
   const int nblk = (int)((Na + chunk - 1) / chunk);
-  dispatch_hist_kernel<<<nblk, kDispatchThreads, 0, s>>>(ids, Na, chunk, E, blk_counts, status);
-  dispatch_scan_kernel<<<1, kMaxE, 0, s>>>(blk_counts, nblk, E, blk_base, counts, offsets);
-  dispatch_scatter_kernel<<<nblk, kDispatchThreads, 0, s>>>(ids, topk_w, Na, chunk, E, blk_base,
-                                                            perm_src, inv_pos, w_perm);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(dispatch_hist_kernel, dim3(nblk), dim3(kDispatchThreads), 0, s, ids,
+                             Na, chunk, E, blk_counts, status);
+  if (e == cudaSuccess)
+    e = launch_pdl(dispatch_scan_kernel, dim3(1), dim3(kMaxE), 0, s, blk_counts, nblk, E, blk_base,
+                   counts, offsets);
+  if (e == cudaSuccess)
+    e = launch_pdl(dispatch_scatter_kernel, dim3(nblk), dim3(kDispatchThreads), 0, s, ids, topk_w,
+                   Na, chunk, E, blk_base, perm_src, inv_pos, w_perm);
+  return e;
 }
 
 cudaError_t launch_gather_plan(const __nv_bfloat16 *x, const int32_t *perm_src,
@@ -234,9 +317,8 @@ cudaError_t launch_gather_plan(const __nv_bfloat16 *x, const int32_t *perm_src,
                                cudaStream_t s) {
   const int64_t R = (int64_t)T * k + (shared ? T : 0);
   const int blocks = (int)((R + 7) / 8) + 1;
-  gather_plan_kernel<<<blocks, 256, 0, s>>>(x, perm_src, offsets, T, k, E, H, I, shared, x_perm,
-                                            plan, status);
-  return cudaGetLastError();
+  return launch_pdl(gather_plan_kernel, dim3(blocks), dim3(256), 0, s, x, perm_src, offsets, T, k,
+                    E, H, I, shared, x_perm, plan, status);
 }
 
 }  // namespace moe

@@ -188,11 +188,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t *pref = seg_row + nseg + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int32_t *g_pref = plan + (kGateUp ? 1 : 2) * (nseg + 1);
-  for (int i = threadIdx.x; i <= nseg; i += blockDim.x) {
-    seg_row[i] = plan[i];
-    pref[i] = g_pref[i];
-  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
@@ -214,6 +209,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_a);
     tma_prefetch_desc(&tm_a_sh);
     tma_prefetch_desc(&tm_b);
+  }
+  // everything above is independent of earlier kernels' outputs
+  pdl_wait();
+  pdl_launch_dependents();
+  const int32_t *g_pref = plan + (kGateUp ? 1 : 2) * (nseg + 1);
+  for (int i = threadIdx.x; i <= nseg; i += blockDim.x) {
+    seg_row[i] = plan[i];
+    pref[i] = g_pref[i];
   }
   tc_fence_before();
   __syncthreads();
@@ -423,8 +426,8 @@ cudaError_t launch_gemm(const moe_layer_desc_t &d, const void *w, const void *w_
   const int nj = (rows + kBM - 1) / kBM;
   const int64_t max_tiles = ((R + BN - 1) / BN + nseg) * (int64_t)nj;
   const int grid = (int)(max_tiles < num_sms() ? max_tiles : num_sms());
-  kern<<<grid, kThreads, smem, s>>>(ma, msh, mb, plan, nseg, d.E, K, rows, Na, w_perm, out, status);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, ma, msh, mb, plan, nseg, d.E, K, rows,
+                    Na, w_perm, out, status);
 }
 
 }  // namespace

@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -27,6 +29,7 @@ constexpr int kRouteMaxSplits = 16;
 // list (a multiple of the block size, chosen so there are at most
 // kDispatchMaxBlocks blocks).
 constexpr int kDispatchThreads = 256;
+constexpr int64_t kSmallDispatch = 2048;  // N_a up to this: one-block dispatch
 constexpr int kDispatchMaxBlocks = 1024;
 inline int64_t dispatch_chunk(int64_t Na) {
   int64_t c = (Na + kDispatchMaxBlocks - 1) / kDispatchMaxBlocks;
@@ -122,6 +125,33 @@ bool encode_bf16_map(CUtensorMap *m, const void *base, int rank, const cuuint64_
                      const cuuint64_t *strides, const cuuint32_t *box);
 
 // ----------------------------------------------------- device helpers --
+
+// Programmatic dependent launch.  Every kernel of the path is launched with
+// programmatic stream serialization, so its launch and its input-independent
+// prologue (barrier set-up, TMEM allocation, descriptor prefetch) overlap the
+// previous kernel's tail.  Each kernel calls pdl_wait() before it reads
+// memory that an earlier stream operation wrote, then
+// pdl_launch_dependents() so that the next kernel may launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

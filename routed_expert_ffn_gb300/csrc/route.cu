@@ -25,22 +25,38 @@ __global__ void __launch_bounds__(256) topk_gating_kernel(
     const float *__restrict__ partial, int splits, const float *__restrict__ sel_bias, int T,
     int E, int k, int gating, float *__restrict__ logits, int32_t *__restrict__ ids,
     float *__restrict__ wout, float *__restrict__ gap) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;  // whole warp leaves together
 
   float s[NV], key[NV];
 #pragma unroll
+  for (int i = 0; i < NV; ++i) s[i] = 0.f;
+  // sum the router's K-split partials in split order; four splits' loads are
+  // issued together
+  for (int z0 = 0; z0 < splits; z0 += 4) {
+    float p[NV][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const int e = lane + 32 * i;
+        p[i][u] = (e < E && z0 + u < splits) ? partial[((size_t)(z0 + u) * T + t) * E + e] : 0.f;
+      }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int i = 0; i < NV; ++i) s[i] += p[i][u];
+  }
+#pragma unroll
   for (int i = 0; i < NV; ++i) {
     const int e = lane + 32 * i;
-    s[i] = 0.f;
     key[i] = -FLT_MAX;
     if (e < E) {
-      float v = 0.f;
-      for (int zz = 0; zz < splits; ++zz) v += partial[((size_t)zz * T + t) * E + e];
-      s[i] = v;
-      logits[(size_t)t * E + e] = v;
-      key[i] = (gating == MOE_GATE_SIGMOID_BIAS_RENORM) ? sigmoidf_(v) + sel_bias[e] : v;
+      logits[(size_t)t * E + e] = s[i];
+      key[i] = (gating == MOE_GATE_SIGMOID_BIAS_RENORM) ? sigmoidf_(s[i]) + sel_bias[e] : s[i];
     }
   }
 
@@ -119,22 +135,23 @@ cudaError_t launch_topk_gating(const float *partial, int splits, const float *se
                                float *gap, cudaStream_t s) {
   const int blocks = (T + 7) / 8;
   const int nv = (E + 31) / 32;
+  cudaError_t e;
   if (nv <= 1)
-    topk_gating_kernel<1><<<blocks, 256, 0, s>>>(partial, splits, sel_bias, T, E, k, gating, logits,
+    e = launch_pdl(topk_gating_kernel<1>, dim3(blocks), dim3(256), 0, s, partial, splits, sel_bias, T, E, k, gating, logits,
                                                  ids, w, gap);
   else if (nv <= 2)
-    topk_gating_kernel<2><<<blocks, 256, 0, s>>>(partial, splits, sel_bias, T, E, k, gating, logits,
+    e = launch_pdl(topk_gating_kernel<2>, dim3(blocks), dim3(256), 0, s, partial, splits, sel_bias, T, E, k, gating, logits,
                                                  ids, w, gap);
   else if (nv <= 4)
-    topk_gating_kernel<4><<<blocks, 256, 0, s>>>(partial, splits, sel_bias, T, E, k, gating, logits,
+    e = launch_pdl(topk_gating_kernel<4>, dim3(blocks), dim3(256), 0, s, partial, splits, sel_bias, T, E, k, gating, logits,
                                                  ids, w, gap);
   else if (nv <= 8)
-    topk_gating_kernel<8><<<blocks, 256, 0, s>>>(partial, splits, sel_bias, T, E, k, gating, logits,
+    e = launch_pdl(topk_gating_kernel<8>, dim3(blocks), dim3(256), 0, s, partial, splits, sel_bias, T, E, k, gating, logits,
                                                  ids, w, gap);
   else
-    topk_gating_kernel<16><<<blocks, 256, 0, s>>>(partial, splits, sel_bias, T, E, k, gating,
+    e = launch_pdl(topk_gating_kernel<16>, dim3(blocks), dim3(256), 0, s, partial, splits, sel_bias, T, E, k, gating,
                                                   logits, ids, w, gap);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace moe

@@ -40,6 +40,8 @@ constexpr size_t kRSmem = 1024 + (size_t)kRStages * kRStage + 256;
 
 __global__ void __launch_bounds__(256)
     router_split_kernel(const float4 *__restrict__ w, int64_t n4, __nv_bfloat16 *__restrict__ out) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t n = n4 * 4;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -110,6 +112,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
     tma_prefetch_desc(&tm_w);
     tma_prefetch_desc(&tm_x);
   }
+  pdl_wait();
+  pdl_launch_dependents();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -246,9 +250,8 @@ cudaError_t launch_router_logits(const __nv_bfloat16 *x, const float *w_router, 
   const int64_t n4 = (int64_t)E * H / 4;
   int blocks = (int)((n4 + 255) / 256);
   if (blocks > 4 * num_sms()) blocks = 4 * num_sms();
-  router_split_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4 *>(w_router), n4,
-                                             w_split);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(router_split_kernel, dim3(blocks), dim3(256), 0, s,
+                             reinterpret_cast<const float4 *>(w_router), n4, w_split);
   if (e != cudaSuccess) return e;
 
   CUtensorMap mw, mx;
@@ -277,8 +280,8 @@ cudaError_t launch_router_logits(const __nv_bfloat16 *x, const float *w_router, 
   const int nkb = H / kBK;
   const int per = (nkb + splits - 1) / splits;
   dim3 grid((E + kBM - 1) / kBM, (T + kRBN - 1) / kRBN, splits);
-  router_tc_kernel<<<grid, kRThreads, kRSmem, s>>>(mw, mx, T, E, per, nkb, partial, status);
-  return cudaGetLastError();
+  return launch_pdl(router_tc_kernel, grid, dim3(kRThreads), kRSmem, s, mw, mx, T, E, per, nkb,
+                    partial, status);
 }
 
 }  // namespace moe
