@@ -418,10 +418,11 @@ def run_gpu(args):
 
 
 def launches_per_step(cfg, T):
-    """Kernels one moe_layer_forward launches: router split + router + gating,
+    """Kernels one moe_layer_forward launches: router (one fused kernel up to 32
+    tokens, else W_r split + tensor-core router + gating),
     dispatch (one kernel up to 2048 assignments, else three), gather + plan,
     gate/up GEMM, down GEMM, combine."""
-    return 3 + (1 if T * cfg.k <= 2048 else 3) + 4
+    return (1 if T <= 32 else 3) + (1 if T * cfg.k <= 2048 else 3) + 4
 
 
 def kernel_sources_sha():

@@ -118,6 +118,24 @@ T *at(void *ws, size_t off) {
 }
 
 const __nv_bfloat16 *bf(const void *p) { return static_cast<const __nv_bfloat16 *>(p); }
+
+// Router + gating: one fused launch for small batches, else the tensor-core
+// router (split-K partials) followed by the gating kernel.
+cudaError_t route(const moe_layer_desc_t &d, const Layout &L, const __nv_bfloat16 *x,
+                  const float *w_router, const float *sel_bias, float *logits, int32_t *ids,
+                  float *w, float *gap, void *workspace, cudaStream_t s) {
+  uint32_t *status = at<uint32_t>(workspace, L.status);
+  if (d.T <= kSmallRouteT)
+    return launch_route_small(x, w_router, sel_bias, d.T, d.H, d.E, d.k, d.gating, logits, ids, w,
+                              gap, status + kRouteCounterWord, s);
+  float *part = at<float>(workspace, L.route_part);
+  cudaError_t e = launch_router_logits(x, w_router, d.T, d.H, d.E, L.route_splits,
+                                       at<__nv_bfloat16>(workspace, L.router_w), part, status, s);
+  if (e == cudaSuccess)
+    e = launch_topk_gating(part, L.route_splits, sel_bias, d.T, d.E, d.k, d.gating, logits, ids, w,
+                           gap, s);
+  return e;
+}
 __nv_bfloat16 *bfw(void *p) { return static_cast<__nv_bfloat16 *>(p); }
 
 }  // namespace
@@ -206,15 +224,8 @@ moe_status_t moe_route(const moe_layer_desc_t *d, const void *x, const float *w_
     return MOE_ERR_INVALID_ARG;
   if (d->gating == MOE_GATE_SIGMOID_BIAS_RENORM && !ok_ptr(sel_bias)) return MOE_ERR_INVALID_ARG;
   if ((st = check_device()) != MOE_OK) return st;
-  cudaStream_t s = (cudaStream_t)stream;
-  float *part = at<float>(workspace, L.route_part);
-  cudaError_t e = launch_router_logits(bf(x), w_router, d->T, d->H, d->E, L.route_splits,
-                                       at<__nv_bfloat16>(workspace, L.router_w), part,
-                                       at<uint32_t>(workspace, L.status), s);
-  if (e == cudaSuccess)
-    e = launch_topk_gating(part, L.route_splits, sel_bias, d->T, d->E, d->k, d->gating, logits,
-                           topk_ids, topk_w, boundary_gap, s);
-  return cuda_status(e);
+  return cuda_status(route(*d, L, bf(x), w_router, sel_bias, logits, topk_ids, topk_w,
+                           boundary_gap, workspace, (cudaStream_t)stream));
 }
 
 moe_status_t moe_build_dispatch(const moe_layer_desc_t *d, const int32_t *topk_ids,
@@ -310,15 +321,10 @@ moe_status_t moe_layer_forward(const moe_layer_desc_t *d, const moe_layer_weight
   __nv_bfloat16 *x_perm = at<__nv_bfloat16>(workspace, L.x_perm);
   __nv_bfloat16 *h = at<__nv_bfloat16>(workspace, L.h);
   __half *out_perm = at<__half>(workspace, L.out_perm);
-  float *part = at<float>(workspace, L.route_part);
-
   cudaError_t e = mark(0);
   if (e == cudaSuccess)
-    e = launch_router_logits(bf(x), w->w_router, d->T, d->H, d->E, L.route_splits,
-                             at<__nv_bfloat16>(workspace, L.router_w), part, status, s);
-  if (e == cudaSuccess)
-    e = launch_topk_gating(part, L.route_splits, w->sel_bias, d->T, d->E, d->k, d->gating, logits,
-                           ids, tw, at<float>(workspace, L.gap), s);
+    e = route(*d, L, bf(x), w->w_router, w->sel_bias, logits, ids, tw, at<float>(workspace, L.gap),
+              workspace, s);
   if (e == cudaSuccess) e = mark(1);
   if (e == cudaSuccess)
     e = launch_dispatch(ids, tw, d->T, d->k, d->E, at<int32_t>(workspace, L.blk_counts),

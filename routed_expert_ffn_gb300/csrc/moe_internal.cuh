@@ -22,8 +22,14 @@ constexpr int kMaxK = 32;           // experts per token
 constexpr int kMaxT = 1 << 20;
 constexpr int64_t kMaxAssign = 1 << 24;
 
-// Router: at most this many K splits (summed by the gating kernel).
+// Router: at most this many K splits (summed by the gating kernel); batches of
+// up to kSmallRouteT tokens take the one-launch small-batch router.
 constexpr int kRouteMaxSplits = 16;
+constexpr int kSmallRouteT = 32;
+
+// 32-bit words inside the workspace's 256-byte status block (zeroed by
+// moe_workspace_init).
+constexpr int kRouteCounterWord = 16;  // small-batch router: CTAs finished
 
 // Dispatch: threads per block; each block takes a chunk of the assignment
 // list (a multiple of the block size, chosen so there are at most
@@ -95,6 +101,10 @@ inline int plan_ints(int nseg) { return 3 * (nseg + 1); }
 cudaError_t launch_router_logits(const __nv_bfloat16 *x, const float *w_router, int T, int H, int E,
                                  int splits, __nv_bfloat16 *w_split, float *partial,
                                  uint32_t *status, cudaStream_t s);
+cudaError_t launch_route_small(const __nv_bfloat16 *x, const float *w_router,
+                               const float *sel_bias, int T, int H, int E, int k, int gating,
+                               float *logits, int32_t *ids, float *w, float *gap,
+                               uint32_t *counter, cudaStream_t s);
 cudaError_t launch_topk_gating(const float *partial, int splits, const float *sel_bias, int T,
                                int E, int k, int gating, float *logits, int32_t *ids, float *w,
                                float *gap, cudaStream_t s);
