@@ -38,12 +38,13 @@ Layout make_layout(const moe_layer_desc_t &d) {
   L.route_splits = route_splits(d.T, d.E, d.H);
   const int64_t chunk = dispatch_chunk(Na);
   L.nblk = (int)((Na + chunk - 1) / chunk);
-  L.status = take(256);
+  L.status = take(kStatusBlockBytes);
   L.route_part = take((size_t)L.route_splits * d.T * d.E * 4);
   L.router_w = take((size_t)3 * d.E * d.H * 2);
   L.blk_counts = take((size_t)L.nblk * d.E * 4);
   L.blk_base = take((size_t)L.nblk * d.E * 4);
   L.plan = take((size_t)plan_ints(L.nseg) * 4);
+  L.split_part = take((size_t)kMaxSplitTiles * 2 * kBM * kSplitMaxRows * 4);
   L.logits = take((size_t)d.T * d.E * 4);
   L.topk_ids = take((size_t)Na * 4);
   L.topk_w = take((size_t)Na * 4);
@@ -170,10 +171,10 @@ moe_status_t moe_workspace_layout(const moe_layer_desc_t *d, moe_workspace_layou
 }
 
 moe_status_t moe_workspace_init(void *workspace, size_t ws_bytes, moe_stream_t stream) {
-  if (workspace == nullptr || ws_bytes < 256 ||
+  if (workspace == nullptr || ws_bytes < kStatusBlockBytes ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return MOE_ERR_INVALID_ARG;
-  return cuda_status(cudaMemsetAsync(workspace, 0, 256, (cudaStream_t)stream));
+  return cuda_status(cudaMemsetAsync(workspace, 0, kStatusBlockBytes, (cudaStream_t)stream));
 }
 
 moe_status_t moe_get_device_status(void *workspace, size_t ws_bytes, moe_stream_t stream,
@@ -270,12 +271,16 @@ moe_status_t moe_grouped_swiglu_ffn(const moe_layer_desc_t *d, const void *x,
   int32_t *plan = at<int32_t>(workspace, L.plan);
   __nv_bfloat16 *x_perm = at<__nv_bfloat16>(workspace, L.x_perm);
   __nv_bfloat16 *h = at<__nv_bfloat16>(workspace, L.h);
+  float *split_part = at<float>(workspace, L.split_part);
+  uint32_t *split_cnt = at<uint32_t>(workspace, L.status) + kSplitCounterWord;
   cudaError_t e = launch_gather_plan(bf(x), perm_src, offsets, d->T, d->k, d->E, d->H, d->I,
                                      d->has_shared_expert, x_perm, plan, status, s);
-  if (e == cudaSuccess) e = launch_expert_gateup(*d, w13, w13_shared, x_perm, plan, h, status, s);
   if (e == cudaSuccess)
-    e = launch_expert_down(*d, w2, w2_shared, h, plan, w_perm, static_cast<__half *>(out_perm),
-                           status, s);
+    e = launch_expert_gateup(*d, w13, w13_shared, x_perm, plan, split_part, split_cnt, h, status,
+                             s);
+  if (e == cudaSuccess)
+    e = launch_expert_down(*d, w2, w2_shared, h, plan, w_perm, split_part,
+                           split_cnt + kMaxSplitTiles, static_cast<__half *>(out_perm), status, s);
   return cuda_status(e);
 }
 
@@ -321,6 +326,8 @@ moe_status_t moe_layer_forward(const moe_layer_desc_t *d, const moe_layer_weight
   __nv_bfloat16 *x_perm = at<__nv_bfloat16>(workspace, L.x_perm);
   __nv_bfloat16 *h = at<__nv_bfloat16>(workspace, L.h);
   __half *out_perm = at<__half>(workspace, L.out_perm);
+  float *split_part = at<float>(workspace, L.split_part);
+  uint32_t *split_cnt = at<uint32_t>(workspace, L.status) + kSplitCounterWord;
   cudaError_t e = mark(0);
   if (e == cudaSuccess)
     e = route(*d, L, bf(x), w->w_router, w->sel_bias, logits, ids, tw, at<float>(workspace, L.gap),
@@ -335,10 +342,13 @@ moe_status_t moe_layer_forward(const moe_layer_desc_t *d, const moe_layer_weight
     e = launch_gather_plan(bf(x), perm_src, offsets, d->T, d->k, d->E, d->H, d->I,
                            d->has_shared_expert, x_perm, plan, status, s);
   if (e == cudaSuccess) e = mark(3);
-  if (e == cudaSuccess) e = launch_expert_gateup(*d, w->w13, w->w13_shared, x_perm, plan, h, status, s);
+  if (e == cudaSuccess)
+    e = launch_expert_gateup(*d, w->w13, w->w13_shared, x_perm, plan, split_part, split_cnt, h,
+                             status, s);
   if (e == cudaSuccess) e = mark(4);
   if (e == cudaSuccess)
-    e = launch_expert_down(*d, w->w2, w->w2_shared, h, plan, w_perm, out_perm, status, s);
+    e = launch_expert_down(*d, w->w2, w->w2_shared, h, plan, w_perm, split_part,
+                           split_cnt + kMaxSplitTiles, out_perm, status, s);
   if (e == cudaSuccess) e = mark(5);
   if (e == cudaSuccess)
     e = launch_combine(out_perm, inv_pos, nullptr, d->T, d->k, d->H, d->has_shared_expert, bfw(y), s);

@@ -138,6 +138,35 @@ __global__ void __launch_bounds__(kDispatchThreads)
   (void)lane;
 }
 
+// Split-K factor of one GEMM: with `total` tiles of `nkb` K blocks on
+// `num_sms` SMs, the S that minimises the K blocks the busiest SM streams
+// (ties to the smaller S), with at least two K blocks per piece.  Only small
+// batches split (every tile has at most kSplitMaxRows token rows).
+// Cost model, in K blocks streamed by the busiest SM: each piece also pays a
+// fixed epilogue cost (partial store, fence, arrival, barriers) worth
+// kSplitPieceCost K blocks, and the last piece reads S partials.  A split is
+// taken only if it saves at least a fifth.
+__device__ int choose_split(int total, int nkb, int num_sms, int max_m) {
+  // 32-bit arithmetic throughout: total*pieces <= kMaxSplitTiles is checked
+  // before any product that could grow, nkb <= 512
+  constexpr int kSplitPieceCost = 8;
+  if (total <= 0 || max_m > kSplitMaxRows || total > kMaxSplitTiles / 2) return 1;
+  const int base = (total + num_sms - 1) / num_sms * nkb;
+  int best = 1, best_cost = base;
+  for (int S = 2; S <= kMaxSplit; ++S) {
+    const int kbs = (nkb + S - 1) / S;
+    if (kbs < 2) break;
+    const int pieces = (nkb + kbs - 1) / kbs;  // no empty piece
+    if (total * pieces > kMaxSplitTiles) break;
+    const int cost = (total * pieces + num_sms - 1) / num_sms * (kbs + kSplitPieceCost) + pieces;
+    if (cost < best_cost) {
+      best = pieces;
+      best_cost = cost;
+    }
+  }
+  return (best_cost * 5 <= base * 4) ? best : 1;
+}
+
 // Rows [0, Na): x_perm[p] = x[perm_src[p] / k]; rows [Na, Na+T) (shared
 // expert): x_perm[Na+t] = x[t].  One warp per row, 16-byte vectors.  The last
 // block instead writes the tile plan of the grouped GEMMs.
@@ -145,7 +174,7 @@ __global__ void __launch_bounds__(256)
     gather_plan_kernel(const __nv_bfloat16 *__restrict__ x, const int32_t *__restrict__ perm_src,
                        const int32_t *__restrict__ offsets, int T, int k, int E, int H, int I,
                        int shared, __nv_bfloat16 *__restrict__ x_perm, int32_t *__restrict__ plan,
-                       uint32_t *__restrict__ status) {
+                       int num_sms, uint32_t *__restrict__ status) {
   pdl_wait();
   pdl_launch_dependents();
   const int64_t Na = (int64_t)T * k;
@@ -153,10 +182,13 @@ __global__ void __launch_bounds__(256)
   if (blockIdx.x == gridDim.x - 1) {
     // ---- tile plan ----
     __shared__ int warp_tot[32];
-    __shared__ int tot_gu, tot_dn, bad;
+    __shared__ int tot_gu, tot_dn, bad, max_m;
     const int nseg = E + (shared ? 1 : 0);
     const int nj_gu = (I + kBM - 1) / kBM, nj_dn = (H + kBM - 1) / kBM;
-    if (threadIdx.x == 0) bad = 0;
+    if (threadIdx.x == 0) {
+      bad = 0;
+      max_m = 0;
+    }
     __syncthreads();
     // validate the offsets (caller-provided in the standalone call)
     for (int e = threadIdx.x; e < E; e += blockDim.x)
@@ -174,6 +206,7 @@ __global__ void __launch_bounds__(256)
       const int s = s0 + q;
       int m = 0;
       if (!bad && s < nseg) m = (s < E) ? offsets[s + 1] - offsets[s] : T;
+      if (m > 0) atomicMax(&max_m, m);
       gu[q] = (m + kBNGateUp - 1) / kBNGateUp * nj_gu;
       dn[q] = (m + kBNDown - 1) / kBNDown * nj_dn;
       sum_gu += gu[q];
@@ -196,6 +229,8 @@ __global__ void __launch_bounds__(256)
       seg_row[nseg] = bad ? 0 : (int)R;
       pref_gu[nseg] = tot_gu;
       pref_dn[nseg] = tot_dn;
+      plan[3 * (nseg + 1)] = choose_split(tot_gu, H / kBK, num_sms, max_m);
+      plan[3 * (nseg + 1) + 1] = choose_split(tot_dn, I / kBK, num_sms, max_m);
     }
     return;
   }
@@ -318,7 +353,7 @@ cudaError_t launch_gather_plan(const __nv_bfloat16 *x, const int32_t *perm_src,
   const int64_t R = (int64_t)T * k + (shared ? T : 0);
   const int blocks = (int)((R + 7) / 8) + 1;
   return launch_pdl(gather_plan_kernel, dim3(blocks), dim3(256), 0, s, x, perm_src, offsets, T, k,
-                    E, H, I, shared, x_perm, plan, status);
+                    E, H, I, shared, x_perm, plan, num_sms(), status);
 }
 
 }  // namespace moe

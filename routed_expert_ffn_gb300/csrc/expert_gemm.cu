@@ -162,6 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tm_b,     // activations [R, K] (2D)
                        const int32_t *__restrict__ plan, int nseg, int E, int K, int out_cols,
                        int64_t Na, const float *__restrict__ w_perm, void *__restrict__ out_,
+                       float *__restrict__ split_part, uint32_t *__restrict__ split_cnt,
                        uint32_t *__restrict__ status) {
   using C = Cfg<kGateUp, BN, STAGES>;
   // gate/up writes h in bf16 (the next GEMM's operand); down writes the
@@ -184,6 +185,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *fin = tempty + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  volatile int *s_flag = reinterpret_cast<volatile int *>(tmem_slot + 2);  // last split piece
+  int *s_split = reinterpret_cast<int *>(tmem_slot + 3);                   // split-K factor
   int32_t *seg_row = reinterpret_cast<int32_t *>(tmem_slot + 4);
   int32_t *pref = seg_row + nseg + 1;
 
@@ -218,26 +221,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     seg_row[i] = plan[i];
     pref[i] = g_pref[i];
   }
+  if (threadIdx.x == 0) *s_split = plan[3 * (nseg + 1) + (kGateUp ? 0 : 1)];
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total = pref[nseg];
   const int nkb = K / kBK;
+  // work unit = one K piece of a tile (S == 1: the whole tile)
+  const int S = *s_split;
+  const int kbs = (nkb + S - 1) / S;
+  const int total_pieces = total * S;
 
   if (warp == 4) {
     // ------------------------------------------------------ TMA producer --
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      for (int pc = blockIdx.x; ok && pc < total_pieces; pc += gridDim.x) {
+        const int tile = pc / S, z = pc - tile * S;
         const Tile t = decode_tile<BN>(tile, seg_row, pref, nseg);
+        const int kb0 = z * kbs, kb1 = min(nkb, kb0 + kbs);
         const bool sh = (t.seg >= E);
         const CUtensorMap *ma = sh ? &tm_a_sh : &tm_a;
         const int ecoord = sh ? 0 : t.seg;
         const int nb16 = (t.nrows + 15) >> 4;
         const uint32_t bytes = C::NA * C::A_BYTES + (uint32_t)nb16 * C::B16_BYTES;
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int st = (int)(it % STAGES);
           const uint32_t ph = (it / STAGES) & 1u;
           if (!mbar_wait(&empty[st], ph ^ 1u, abort_flag, status, kCode)) {
@@ -263,15 +273,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t it = 0, tl = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++tl) {
+      for (int pc = blockIdx.x; ok && pc < total_pieces; pc += gridDim.x, ++tl) {
+        const int tile = pc / S, z = pc - tile * S;
         const Tile t = decode_tile<BN>(tile, seg_row, pref, nseg);
+        const int kb0 = z * kbs, kb1 = min(nkb, kb0 + kbs);
         const int N = (t.nrows + 15) & ~15;
         const uint32_t idesc = idesc_bf16_f32(kBM, N);
         const uint32_t buf = tl & 1u, use = tl >> 1;
         if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, status, kCode)) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + buf * C::ACC_COLS;
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int st = (int)(it % STAGES);
           if (!mbar_wait(&full[st], (it / STAGES) & 1u, abort_flag, status, kCode)) {
             ok = false;
@@ -285,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int ks = 0; ks < kBK / 16; ++ks) {
             // advance 16 bf16 (32 bytes) along K inside the swizzled row
-            const uint32_t acc = (kb | ks) ? 1u : 0u;
+            const uint32_t acc = (kb != kb0 || ks != 0) ? 1u : 0u;
             umma_bf16(d0, adesc + 2 * ks, bdesc + 2 * ks, idesc, acc);
             if (kGateUp) {
               const uint64_t adesc_up = sdesc_k_sw128(a_addr + C::A_BYTES);
@@ -306,11 +318,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Per 16-token slice: tcgen05.ld of the thread's weight row (16 token
     // columns), fused SiLU(gate)*up or gate weighting, the slice written
     // transposed into smem, then stored as token rows with 16-byte vector
-    // stores by all 128 epilogue threads.
+    // stores by all 128 epilogue threads.  A split-K piece instead writes its
+    // fp32 partial; the last piece of the tile adds the S partials in split
+    // order and runs the same epilogue.
     const int r = warp * 32 + lane;  // TMEM lane = weight row of the tile
     uint32_t tl = 0;
     bool range_bad = false;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++tl) {
+    auto emit16 = [&](const Tile &t, int n0, const float(&g)[16], const float(&u)[16]) {
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        uint16_t bits;
+        if (kGateUp) {
+          bits = __bfloat16_as_ushort(__float2bfloat16_rn(g[q] / (1.0f + __expf(-g[q])) * u[q]));
+        } else {
+          const float val = g[q] * sW[n0 + q];
+          range_bad |= !(fabsf(val) <= 65504.0f);
+          bits = __half_as_ushort(__float2half_rn(fminf(fmaxf(val, -65504.0f), 65504.0f)));
+        }
+        sOut[q * kBM + r] = bits;
+      }
+      epi_sync();
+      // 16 token rows x 128 columns x 2 bytes = 256 chunks of 16 bytes
+      const int col0 = t.j * kBM;
+      for (int c = r; c < 16 * (kBM / 8); c += 128) {
+        const int q = c / (kBM / 8), ch = c % (kBM / 8);
+        const int n = n0 + q, col = col0 + ch * 8;
+        if (n < t.nrows && col < out_cols)
+          *reinterpret_cast<uint4 *>(out + ((int64_t)t.row0 + n) * out_cols + col) =
+              *reinterpret_cast<const uint4 *>(sOut + q * kBM + ch * 8);
+      }
+      epi_sync();
+    };
+    constexpr int kSlot = C::NA * kBM * kSplitMaxRows;  // floats of one piece's partial
+    for (int pc = blockIdx.x; pc < total_pieces; pc += gridDim.x, ++tl) {
+      const int tile = pc / S, z = pc - tile * S;
       const Tile t = decode_tile<BN>(tile, seg_row, pref, nseg);
       const uint32_t buf = tl & 1u, use = tl >> 1;
       const bool waited = mbar_wait(&tfull[buf], use & 1u, abort_flag, status, kCode);
@@ -326,40 +367,81 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint32_t tb = tmem_base + ((uint32_t)(warp * 32) << 16) + buf * C::ACC_COLS;
       const int N = (t.nrows + 15) & ~15;
-      const int col0 = t.j * kBM;
+      if (S == 1) {
+        for (int n0 = 0; n0 < N; n0 += 16) {
+          uint32_t v0[16], v1[16];
+          tmem_ld16(tb + n0, v0);
+          if (kGateUp) tmem_ld16(tb + BN + n0, v1);
+          tmem_ld_wait();
+          float g[16], u[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            g[q] = __uint_as_float(v0[q]);
+            u[q] = kGateUp ? __uint_as_float(v1[q]) : 0.f;
+          }
+          emit16(t, n0, g, u);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[buf]);
+        continue;
+      }
+      // ---- split-K piece (N <= kSplitMaxRows): fp32 partial to global ----
+      float *slot = split_part + (size_t)(tile * S + z) * kSlot + (size_t)r * kSplitMaxRows;
       for (int n0 = 0; n0 < N; n0 += 16) {
         uint32_t v0[16], v1[16];
         tmem_ld16(tb + n0, v0);
         if (kGateUp) tmem_ld16(tb + BN + n0, v1);
         tmem_ld_wait();
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          uint16_t bits;
-          if (kGateUp) {
-            const float g = __uint_as_float(v0[q]);
-            const float u = __uint_as_float(v1[q]);
-            bits = __bfloat16_as_ushort(__float2bfloat16_rn(g / (1.0f + __expf(-g)) * u));
-          } else {
-            const float val = __uint_as_float(v0[q]) * sW[n0 + q];
-            range_bad |= !(fabsf(val) <= 65504.0f);
-            bits = __half_as_ushort(__float2half_rn(fminf(fmaxf(val, -65504.0f), 65504.0f)));
-          }
-          sOut[q * kBM + r] = bits;
+        for (int q = 0; q < 16; q += 4) {
+          *reinterpret_cast<float4 *>(slot + n0 + q) =
+              make_float4(__uint_as_float(v0[q]), __uint_as_float(v0[q + 1]),
+                          __uint_as_float(v0[q + 2]), __uint_as_float(v0[q + 3]));
+          if (kGateUp)
+            *reinterpret_cast<float4 *>(slot + kBM * kSplitMaxRows + n0 + q) =
+                make_float4(__uint_as_float(v1[q]), __uint_as_float(v1[q + 1]),
+                            __uint_as_float(v1[q + 2]), __uint_as_float(v1[q + 3]));
         }
-        epi_sync();
-        // 16 token rows x 128 columns x 2 bytes = 256 chunks of 16 bytes
-        for (int c = r; c < 16 * (kBM / 8); c += 128) {
-          const int q = c / (kBM / 8), ch = c % (kBM / 8);
-          const int n = n0 + q, col = col0 + ch * 8;
-          if (n < t.nrows && col < out_cols)
-            *reinterpret_cast<uint4 *>(out + ((int64_t)t.row0 + n) * out_cols + col) =
-                *reinterpret_cast<const uint4 *>(sOut + q * kBM + ch * 8);
-        }
-        epi_sync();
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[buf]);
+      epi_sync();  // every partial store of this CTA precedes the fence below
+      // release the partial, arrive; atomicInc wraps to 0 at the last piece,
+      // so the counter is ready for the next call
+      if (r == 0) {
+        __threadfence();
+        *s_flag = (atomicInc(&split_cnt[tile], S - 1) == (unsigned)(S - 1));
+      }
+      epi_sync();
+      if (!*s_flag) continue;
+      __threadfence();
+      for (int n0 = 0; n0 < N; n0 += 16) {
+        float g[16], u[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) g[q] = u[q] = 0.f;
+        for (int zz = 0; zz < S; ++zz) {
+          const float *p =
+              split_part + (size_t)(tile * S + zz) * kSlot + (size_t)r * kSplitMaxRows + n0;
+#pragma unroll
+          for (int q = 0; q < 16; q += 4) {
+            const float4 a = __ldcg(reinterpret_cast<const float4 *>(p + q));
+            g[q] += a.x;
+            g[q + 1] += a.y;
+            g[q + 2] += a.z;
+            g[q + 3] += a.w;
+            if (kGateUp) {
+              const float4 b = __ldcg(reinterpret_cast<const float4 *>(p + kBM * kSplitMaxRows + q));
+              u[q] += b.x;
+              u[q + 1] += b.y;
+              u[q + 2] += b.z;
+              u[q + 3] += b.w;
+            }
+          }
+        }
+        emit16(t, n0, g, u);
+      }
     }
     if (range_bad) atomicOr(status, kStatusRange);
   }
@@ -392,7 +474,8 @@ bool act_map(CUtensorMap *m, const void *a, int K, int64_t R) {
 template <bool kGateUp, int BN, int STAGES>
 cudaError_t launch_gemm(const moe_layer_desc_t &d, const void *w, const void *w_sh,
                         const __nv_bfloat16 *act, const int32_t *plan, const float *w_perm,
-                        void *out, uint32_t *status, cudaStream_t s) {
+                        void *out, float *split_part, uint32_t *split_cnt, uint32_t *status,
+                        cudaStream_t s) {
   using C = Cfg<kGateUp, BN, STAGES>;
   static_assert(BN == (kGateUp ? kBNGateUp : kBNDown), "the tile plan's token chunks");
   const int shared = d.has_shared_expert ? 1 : 0;
@@ -423,27 +506,29 @@ cudaError_t launch_gemm(const moe_layer_desc_t &d, const void *w, const void *w_
     if (e != cudaSuccess) return e;
     configured[dev] = smem;
   }
-  const int nj = (rows + kBM - 1) / kBM;
-  const int64_t max_tiles = ((R + BN - 1) / BN + nseg) * (int64_t)nj;
-  const int grid = (int)(max_tiles < num_sms() ? max_tiles : num_sms());
+  // one CTA per SM: the device-side plan decides the tiles (and split-K
+  // pieces); CTAs without work leave at once
+  const int grid = num_sms();
   return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, ma, msh, mb, plan, nseg, d.E, K, rows,
-                    Na, w_perm, out, status);
+                    Na, w_perm, out, split_part, split_cnt, status);
 }
 
 }  // namespace
 
 cudaError_t launch_expert_gateup(const moe_layer_desc_t &d, const void *w13, const void *w13_shared,
                                  const __nv_bfloat16 *x_perm, const int32_t *plan,
-                                 __nv_bfloat16 *h, uint32_t *status, cudaStream_t s) {
+                                 float *split_part, uint32_t *split_cnt, __nv_bfloat16 *h,
+                                 uint32_t *status, cudaStream_t s) {
   return launch_gemm<true, kBNGateUp, kStagesGateUp>(d, w13, w13_shared, x_perm, plan, nullptr, h,
-                                               status, s);
+                                                     split_part, split_cnt, status, s);
 }
 
 cudaError_t launch_expert_down(const moe_layer_desc_t &d, const void *w2, const void *w2_shared,
                                const __nv_bfloat16 *h, const int32_t *plan, const float *w_perm,
-                               __half *out_perm, uint32_t *status, cudaStream_t s) {
-  return launch_gemm<false, kBNDown, kStagesDown>(d, w2, w2_shared, h, plan, w_perm, out_perm, status,
-                                              s);
+                               float *split_part, uint32_t *split_cnt, __half *out_perm,
+                               uint32_t *status, cudaStream_t s) {
+  return launch_gemm<false, kBNDown, kStagesDown>(d, w2, w2_shared, h, plan, w_perm, out_perm,
+                                                  split_part, split_cnt, status, s);
 }
 
 }  // namespace moe

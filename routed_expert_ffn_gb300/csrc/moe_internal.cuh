@@ -27,9 +27,12 @@ constexpr int64_t kMaxAssign = 1 << 24;
 constexpr int kRouteMaxSplits = 16;
 constexpr int kSmallRouteT = 32;
 
-// 32-bit words inside the workspace's 256-byte status block (zeroed by
-// moe_workspace_init).
+// The workspace starts with a status block zeroed by moe_workspace_init:
+// 32-bit words [0, 64) hold the status word and the small-batch router's
+// arrival counter; then 2 x kMaxSplitTiles split-K arrival counters (gate/up,
+// down).  Every counter returns to zero when its kernel completes.
 constexpr int kRouteCounterWord = 16;  // small-batch router: CTAs finished
+constexpr int kSplitCounterWord = 64;  // first split-K counter
 
 // Dispatch: threads per block; each block takes a chunk of the assignment
 // list (a multiple of the block size, chosen so there are at most
@@ -78,6 +81,7 @@ constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;
 
 struct Layout {
   size_t status, route_part, router_w, blk_counts, blk_base, plan, x_perm, h, out_perm;
+  size_t split_part;
   size_t logits, topk_ids, topk_w, gap, counts, offsets, perm_src, inv_pos, w_perm;
   size_t total;
   int route_splits;
@@ -94,7 +98,18 @@ int route_splits(int T, int E, int H);
 //   [0, nseg]                 segment row offsets (nseg+1)
 //   [nseg+1, 2nseg+1]         gate/up tile prefix (nseg+1)
 //   [2nseg+2, 3nseg+2]        down tile prefix (nseg+1)
-inline int plan_ints(int nseg) { return 3 * (nseg + 1); }
+//   [3nseg+3], [3nseg+4]      split-K factor S of the gate/up and down GEMM
+inline int plan_ints(int nseg) { return 3 * (nseg + 1) + 2; }
+
+// Split-K for small batches: when every tile has at most kSplitMaxRows token
+// rows and there are too few tiles to occupy the GPU, each tile's K range is
+// cut into S pieces (S <= kMaxSplit, at most kMaxSplitTiles pieces in all);
+// each piece writes an fp32 partial [NA][kBM][kSplitMaxRows] and the last to
+// finish adds them in split order.
+constexpr int kSplitMaxRows = 32;
+constexpr int kMaxSplit = 16;
+constexpr int kMaxSplitTiles = 1024;
+constexpr size_t kStatusBlockBytes = 256 + 2 * kMaxSplitTiles * 4;
 
 // ------------------------------------------------------------- launches --
 // Each returns cudaSuccess or the launch error.
@@ -116,12 +131,16 @@ cudaError_t launch_gather_plan(const __nv_bfloat16 *x, const int32_t *perm_src,
                                const int32_t *offsets, int T, int k, int E, int H, int I,
                                int shared, __nv_bfloat16 *x_perm, int32_t *plan, uint32_t *status,
                                cudaStream_t s);
+// split_part: kMaxSplitTiles x 2 x kBM x kSplitMaxRows fp32; split_cnt: the
+// GEMM's kMaxSplitTiles arrival counters (in the workspace status block).
 cudaError_t launch_expert_gateup(const moe_layer_desc_t &d, const void *w13, const void *w13_shared,
                                  const __nv_bfloat16 *x_perm, const int32_t *plan,
-                                 __nv_bfloat16 *h, uint32_t *status, cudaStream_t s);
+                                 float *split_part, uint32_t *split_cnt, __nv_bfloat16 *h,
+                                 uint32_t *status, cudaStream_t s);
 cudaError_t launch_expert_down(const moe_layer_desc_t &d, const void *w2, const void *w2_shared,
                                const __nv_bfloat16 *h, const int32_t *plan, const float *w_perm,
-                               __half *out_perm, uint32_t *status, cudaStream_t s);
+                               float *split_part, uint32_t *split_cnt, __half *out_perm,
+                               uint32_t *status, cudaStream_t s);
 cudaError_t launch_combine(const __half *out_perm, const int32_t *inv_pos,
                            const float *topk_w, int T, int k, int H, int shared, __nv_bfloat16 *y,
                            cudaStream_t s);
