@@ -41,8 +41,7 @@ def _stale(obj: str, src: str) -> bool:
 def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False,
           defines=None, lib_path: str = None) -> str:
     """Compile the library.  ``defines`` ({name: value}) override the kernels'
-    compile-time tile parameters (MOE_BN_GATEUP, MOE_BN_DOWN, MOE_STAGES_GATEUP,
-    MOE_STAGES_DOWN); such a variant is built in its own directory into
+    compile-time parameters (``-D`` macros of the sources); such a variant is built in its own directory into
     ``lib_path``."""
     build_dir, lib = BUILD, LIB
     extra = []

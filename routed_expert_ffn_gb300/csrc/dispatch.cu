@@ -138,33 +138,33 @@ __global__ void __launch_bounds__(kDispatchThreads)
   (void)lane;
 }
 
-// Split-K factor of one GEMM: with `total` tiles of `nkb` K blocks on
-// `num_sms` SMs, the S that minimises the K blocks the busiest SM streams
-// (ties to the smaller S), with at least two K blocks per piece.  Only small
-// batches split (every tile has at most kSplitMaxRows token rows).
-// Cost model, in K blocks streamed by the busiest SM: each piece also pays a
-// fixed epilogue cost (partial store, fence, arrival, barriers) worth
-// kSplitPieceCost K blocks, and the last piece reads S partials.  A split is
-// taken only if it saves at least a fifth.
+// Split-K of one GEMM, as the number of K blocks per piece: nkb (no split)
+// or an even number below nkb (the GEMM streams K in steps of two blocks).
+// With `total` tiles on `num_sms` SMs it minimises the K blocks the busiest
+// SM streams.  Only small batches split (every tile has at most
+// kSplitMaxRows token rows).  Cost model, in K blocks streamed by the busiest
+// SM: each piece also pays a fixed epilogue cost (partial store, fence,
+// arrival, barriers) worth kSplitPieceCost K blocks, and the last piece reads
+// the partials.  A split is taken only if it saves at least a fifth.
 __device__ int choose_split(int total, int nkb, int num_sms, int max_m) {
   // 32-bit arithmetic throughout: total*pieces <= kMaxSplitTiles is checked
   // before any product that could grow, nkb <= 512
   constexpr int kSplitPieceCost = 8;
-  if (total <= 0 || max_m > kSplitMaxRows || total > kMaxSplitTiles / 2) return 1;
+  if (total <= 0 || max_m > kSplitMaxRows || total > kMaxSplitTiles / 2) return nkb;
   const int base = (total + num_sms - 1) / num_sms * nkb;
-  int best = 1, best_cost = base;
+  int best = nkb, best_cost = base;
   for (int S = 2; S <= kMaxSplit; ++S) {
-    const int kbs = (nkb + S - 1) / S;
-    if (kbs < 2) break;
+    const int kbs = 2 * ((nkb + 2 * S - 1) / (2 * S));  // even, >= 2
+    if (kbs >= nkb) continue;
     const int pieces = (nkb + kbs - 1) / kbs;  // no empty piece
     if (total * pieces > kMaxSplitTiles) break;
     const int cost = (total * pieces + num_sms - 1) / num_sms * (kbs + kSplitPieceCost) + pieces;
     if (cost < best_cost) {
-      best = pieces;
+      best = kbs;
       best_cost = cost;
     }
   }
-  return (best_cost * 5 <= base * 4) ? best : 1;
+  return (best_cost * 5 <= base * 4) ? best : nkb;
 }
 
 // Rows [0, Na): x_perm[p] = x[perm_src[p] / k]; rows [Na, Na+T) (shared
@@ -182,12 +182,14 @@ __global__ void __launch_bounds__(256)
   if (blockIdx.x == gridDim.x - 1) {
     // ---- tile plan ----
     __shared__ int warp_tot[32];
-    __shared__ int tot_gu, tot_dn, bad, max_m;
+    __shared__ int tot_gu, tot_dn, bad, max_m, n_chunks, n_wide;
     const int nseg = E + (shared ? 1 : 0);
     const int nj_gu = (I + kBM - 1) / kBM, nj_dn = (H + kBM - 1) / kBM;
     if (threadIdx.x == 0) {
       bad = 0;
       max_m = 0;
+      n_chunks = 0;
+      n_wide = 0;
     }
     __syncthreads();
     // validate the offsets (caller-provided in the standalone call)
@@ -206,9 +208,14 @@ __global__ void __launch_bounds__(256)
       const int s = s0 + q;
       int m = 0;
       if (!bad && s < nseg) m = (s < E) ? offsets[s + 1] - offsets[s] : T;
-      if (m > 0) atomicMax(&max_m, m);
-      gu[q] = (m + kBNGateUp - 1) / kBNGateUp * nj_gu;
-      dn[q] = (m + kBNDown - 1) / kBNDown * nj_dn;
+      if (m > 0) {
+        atomicMax(&max_m, m);
+        // down-GEMM token chunks; "wide" ones have more than 128 rows
+        atomicAdd(&n_chunks, (m + kTileRowsDown - 1) / kTileRowsDown);
+        atomicAdd(&n_wide, m / kTileRowsDown + (m % kTileRowsDown > 128 ? 1 : 0));
+      }
+      gu[q] = (m + kTileRowsGateUp - 1) / kTileRowsGateUp * nj_gu;
+      dn[q] = (m + kTileRowsDown - 1) / kTileRowsDown * nj_dn;
       sum_gu += gu[q];
       sum_dn += dn[q];
       if (s < nseg) seg_row[s] = bad ? 0 : ((s < E) ? offsets[s] : (int)Na);
@@ -231,6 +238,9 @@ __global__ void __launch_bounds__(256)
       pref_dn[nseg] = tot_dn;
       plan[3 * (nseg + 1)] = choose_split(tot_gu, H / kBK, num_sms, max_m);
       plan[3 * (nseg + 1) + 1] = choose_split(tot_dn, I / kBK, num_sms, max_m);
+      // down-GEMM pipeline layout: stages of weights + 256 token rows when
+      // most chunks are wide, else weights + 128 rows
+      plan[3 * (nseg + 1) + 2] = (n_wide > 0 && 2 * n_wide >= n_chunks) ? 1 : 0;
     }
     return;
   }

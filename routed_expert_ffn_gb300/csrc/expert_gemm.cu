@@ -10,33 +10,42 @@
 //   down:     out[p, r] = w_perm[p] * sum_i W2[e][r][i] h[p][i]
 //
 // Orientation ("swap AB"): the weight rows are the MMA's M = 128 dimension and
-// the expert's token rows its N dimension (16..128, rounded up to 16).  In
-// the decode regime an expert sees only a handful of rows, yet every weight
-// byte is read from HBM once per (expert, 128-row token chunk) and streamed
-// through the tensor cores at full M; in the prefill regime tiles are full
-// 128 x 128.
+// the expert's token rows its N dimension.  In the decode regime an expert
+// sees only a handful of rows, yet every weight byte is read from HBM once
+// per (expert, 256-row token chunk) and streamed through the tensor cores at
+// full M; in the prefill regime tiles are 128 x 256.
 //
 // Work unit (tile) = (segment s, weight-row block j, token chunk c); segments
-// are the E experts (+ the shared expert, all T tokens).  The tile plan (a
-// prefix sum of tiles per segment, computed on the device from the dispatch
-// offsets) is read by a persistent kernel, one CTA per SM, which walks tiles
-// blockIdx.x, blockIdx.x + gridDim.x, ...  Tiles of one weight block are
-// adjacent (chunk index innermost) so CTAs working at the same time share
-// weight tiles through L2; experts with no rows have no tiles, so their
-// weights are never read.
+// are the E experts (+ the shared expert, all T tokens).  A gate/up tile holds
+// 64 gate rows and the 64 up rows of the same h columns (TMEM lanes [0, 64)
+// and [64, 128)), so SiLU(gate)*up is formed in the epilogue and the two
+// accumulators of a tile fit next to each other in TMEM; a down tile holds
+// 128 rows of W2.  The tile plan (a prefix sum of tiles per segment, computed
+// on the device from the dispatch offsets) is read by a persistent kernel,
+// one CTA per SM, which walks tiles blockIdx.x, blockIdx.x + gridDim.x, ...
+// Tiles of one weight block are adjacent (chunk index innermost) so CTAs
+// working at the same time share weight tiles through L2; experts with no
+// rows have no tiles, so their weights are never read.
 //
 // CTA = 6 warps:
-//   warp 4      TMA producer: weight tile(s) [128 x 64] and token tile
-//               [16-row boxes x 64] per K step into a STAGES-deep ring
-//               (128-byte swizzle), completion on the stage's mbarrier;
+//   warp 4      TMA producer: a ring of pipeline stages (128-byte swizzle),
+//               one per K step: the weight tile [128 x 64] and the tile's
+//               token rows [16-row boxes, or whole 128-row halves, x 64];
+//               completion on the stage's mbarrier.  Mostly-wide launches
+//               (most token chunks over 128 rows) run 4 stages of 48 KB,
+//               one per K step; others 6 stages of 32 KB, one per K step and
+//               128-row half (decided on the device from the dispatch
+//               counts);
 //   warp 5      TMEM allocator and MMA issuer: one thread issues
-//               tcgen05.mma (bf16 in, fp32 accumulate in TMEM), commits the
-//               stage back to the producer and the finished accumulator to
-//               the epilogue; two accumulator buffers let the epilogue of one
-//               tile overlap the mainloop of the next;
-//   warps 0-3   epilogue: tcgen05.ld of their 32 TMEM lanes (= 32 weight
-//               rows), fused SiLU(gate)*up (gate/up GEMM) or gate weighting
-//               (down GEMM), bf16 (h) or fp16 (out_perm) stores.
+//               tcgen05.mma (bf16 in, fp32 accumulate in TMEM; one MMA per
+//               128-token half and K16 step) and one tcgen05.commit per K
+//               step, which frees the stage; the finished accumulator is
+//               committed to the epilogue; two accumulator buffers of 256
+//               columns let the epilogue of one tile overlap the mainloop of
+//               the next;
+//   warps 0-3   epilogue: tcgen05.ld of their 32 TMEM lanes, fused
+//               SiLU(gate)*up (gate/up GEMM) or gate weighting (down GEMM),
+//               bf16 (h) or fp16 (out_perm) stores.
 // Every wait is bounded; on expiry the CTA records MOE_ERR_TIMEOUT's status
 // bit, drains its copies and MMAs in flight, frees TMEM and returns.
 #include <stdio.h>
@@ -84,30 +93,35 @@ bool encode_bf16_map(CUtensorMap *m, const void *base, int rank, const cuuint64_
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kStagesGateUp = MOE_STAGES_GATEUP;
-constexpr int kStagesDown = MOE_STAGES_DOWN;
+constexpr uint32_t kChunkBytes = kBM * kBK * 2;  // 16 KB: 128 rows x 64 bf16
+constexpr uint32_t kTmemCols = 512;              // two accumulators of 256 columns
+constexpr uint32_t kAccCols = kTmemCols / 2;
+constexpr int kMaxStages = 3;
+static_assert(kStageKB == 2, "stages are pairs of K blocks");
+static_assert(kRingBytes == 2 * (2 * kStageKB * kChunkBytes + kStageKB * kChunkBytes) &&
+                  kRingBytes == 3 * (2 * kStageKB * kChunkBytes) &&
+                  kRingBytes == 2 * (3 * kStageKB * kChunkBytes),
+              "the ring holds whole stages of every layout");
 
-__host__ __device__ constexpr uint32_t tmem_cols_pow2(uint32_t n) {
-  return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : n <= 256 ? 256 : 512;
-}
+// Token-row tensor maps with box heights 16, 32, ..., 128 rows (x 2 K blocks).
+struct TokenMaps {
+  CUtensorMap m[8];
+};
 
-template <bool kGateUp, int BN, int STAGES>
+template <bool kGateUp>
 struct Cfg {
-  static constexpr int NA = kGateUp ? 2 : 1;               // weight tiles per stage
-  static constexpr uint32_t A_BYTES = kBM * kBK * 2;       // 16 KB
-  static constexpr uint32_t B_BYTES = BN * kBK * 2;        // BN rows of 128 B
-  static constexpr uint32_t B16_BYTES = 16 * kBK * 2;      // one 16-row box
-  static constexpr uint32_t STAGE_BYTES = NA * A_BYTES + B_BYTES;
-  static constexpr uint32_t ACC_COLS = NA * BN;            // TMEM columns per tile
-  static constexpr uint32_t TMEM_COLS = tmem_cols_pow2(2 * ACC_COLS);
-  static constexpr uint32_t BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
-  static constexpr uint32_t STAGE_OUT_BYTES = 16 * kBM * 2;  // one 16-token output slice
-  static size_t smem_bytes(int nseg) {
-    return 1024 + (size_t)STAGES * STAGE_BYTES + STAGE_OUT_BYTES + (size_t)BN * 4 + BAR_BYTES +
+  static constexpr int NA = kGateUp ? 2 : 1;                     // weight blocks per tile
+  static constexpr int TILE_ROWS = kGateUp ? kTileRowsGateUp : kTileRowsDown;
+  static constexpr uint32_t STAGE_A = NA * kStageKB * kChunkBytes;  // weights of a stage
+  static constexpr uint32_t STAGE_HALF = kStageKB * kChunkBytes;    // 128 token rows of a stage
+  static constexpr uint32_t SOUT_BYTES = 16 * kBM * 2;           // one 16-token slice
+  static constexpr uint32_t BAR_BYTES = (2 * kMaxStages + 5) * 8 + 16;
+  static constexpr size_t smem_bytes(int nseg) {
+    return 1024 + (size_t)kRingBytes + 2 * SOUT_BYTES + (size_t)TILE_ROWS * 4 + BAR_BYTES +
            (size_t)2 * (nseg + 1) * 4;
   }
-  static_assert(2 * ACC_COLS <= 512, "accumulators exceed TMEM");
-  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "bad token tile");
+  static_assert(smem_bytes(kMaxE + 1) <= 232448, "shared memory per CTA");
+  static_assert(NA * (TILE_ROWS > 128 ? 256 : 128) <= (int)kAccCols, "accumulator columns");
 };
 
 struct Tile {
@@ -132,7 +146,7 @@ __device__ __forceinline__ bool epi_all(bool p) {
   return r != 0;
 }
 
-template <int BN>
+template <int kTileRows>
 __device__ __forceinline__ Tile decode_tile(int tile, const int32_t *seg_row, const int32_t *pref,
                                             int nseg) {
   int lo = 0, hi = nseg;  // pref[lo] <= tile < pref[hi]
@@ -147,24 +161,35 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int32_t *seg_row, co
   t.seg = lo;
   const int local = tile - pref[lo];
   const int m = seg_row[lo + 1] - seg_row[lo];
-  const int chunks = (m + BN - 1) / BN;
+  const int chunks = (m + kTileRows - 1) / kTileRows;
   t.j = local / chunks;
   const int c = local - t.j * chunks;
-  t.row0 = seg_row[lo] + c * BN;
-  t.nrows = min(BN, m - c * BN);
+  t.row0 = seg_row[lo] + c * kTileRows;
+  t.nrows = min(kTileRows, m - c * kTileRows);
   return t;
 }
 
-template <bool kGateUp, int BN, int STAGES>
+// Four MMAs: one 64-deep K block, 16 bf16 (32 bytes) per step inside the
+// swizzled rows.
+__device__ __forceinline__ void umma_kblock(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                            uint32_t acc) {
+  umma_bf16(d, a, b, idesc, acc);
+  umma_bf16(d, a + 2, b + 2, idesc, 1u);
+  umma_bf16(d, a + 4, b + 4, idesc, 1u);
+  umma_bf16(d, a + 6, b + 6, idesc, 1u);
+}
+
+template <bool kGateUp>
 __global__ void __launch_bounds__(kThreads, 1)
-    expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,     // routed weights (4D)
-                       const __grid_constant__ CUtensorMap tm_a_sh,  // shared-expert weights (4D)
-                       const __grid_constant__ CUtensorMap tm_b,     // activations [R, K] (2D)
+    expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,     // routed weights (5D)
+                       const __grid_constant__ CUtensorMap tm_a_sh,  // shared-expert weights (5D)
+                       const __grid_constant__ TokenMaps tm_b,       // activations [R, K] (3D)
                        const int32_t *__restrict__ plan, int nseg, int E, int K, int out_cols,
                        int64_t Na, const float *__restrict__ w_perm, void *__restrict__ out_,
                        float *__restrict__ split_part, uint32_t *__restrict__ split_cnt,
                        uint32_t *__restrict__ status) {
-  using C = Cfg<kGateUp, BN, STAGES>;
+  using C = Cfg<kGateUp>;
+  constexpr int kTR = C::TILE_ROWS;
   // gate/up writes h in bf16 (the next GEMM's operand); down writes the
   // gate-weighted rows in fp16: 11 significant bits (8x finer than bf16) at
   // the same bandwidth; magnitudes past the fp16 range are clamped and
@@ -174,25 +199,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
-  uint8_t *sA = smem;                                  // [STAGES][NA][A_BYTES]
-  uint8_t *sB = sA + (size_t)STAGES * C::NA * C::A_BYTES;  // [STAGES][B_BYTES]
-  uint16_t *sOut = reinterpret_cast<uint16_t *>(sB + (size_t)STAGES * C::B_BYTES);  // [16][kBM]
-  float *sW = reinterpret_cast<float *>(sOut + 16 * kBM);  // [BN] gate weights (down)
-  uint64_t *full = reinterpret_cast<uint64_t *>(sW + BN);
-  uint64_t *empty = full + STAGES;
-  uint64_t *tfull = empty + STAGES;
+  uint8_t *ring = smem;  // [stages][weights | token rows]
+  uint16_t *sOut = reinterpret_cast<uint16_t *>(ring + kRingBytes);  // [2][16][kBM]
+  float *sW = reinterpret_cast<float *>(sOut + 2 * 16 * kBM);         // [kTR] (down)
+  uint64_t *full = reinterpret_cast<uint64_t *>(sW + kTR);            // [kMaxStages]
+  uint64_t *empty = full + kMaxStages;
+  uint64_t *tfull = empty + kMaxStages;
   uint64_t *tempty = tfull + 2;
   uint64_t *fin = tempty + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   volatile int *s_flag = reinterpret_cast<volatile int *>(tmem_slot + 2);  // last split piece
-  int *s_split = reinterpret_cast<int *>(tmem_slot + 3);                   // split-K factor
+  int *s_kbs = reinterpret_cast<int *>(tmem_slot + 3);                     // K blocks per piece
   int32_t *seg_row = reinterpret_cast<int32_t *>(tmem_slot + 4);
   int32_t *pref = seg_row + nseg + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < kMaxStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -205,13 +229,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 5) {
-    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
   if (warp == 4 && lane == 0) {
     tma_prefetch_desc(&tm_a);
     tma_prefetch_desc(&tm_a_sh);
-    tma_prefetch_desc(&tm_b);
+    for (int i = 0; i < 8; ++i) tma_prefetch_desc(&tm_b.m[i]);
   }
   // everything above is independent of earlier kernels' outputs
   pdl_wait();
@@ -221,90 +245,139 @@ __global__ void __launch_bounds__(kThreads, 1)
     seg_row[i] = plan[i];
     pref[i] = g_pref[i];
   }
-  if (threadIdx.x == 0) *s_split = plan[3 * (nseg + 1) + (kGateUp ? 0 : 1)];
+  if (threadIdx.x == 0) *s_kbs = plan[3 * (nseg + 1) + (kGateUp ? 0 : 1)];
+  // Stage layout.  Gate/up: 2 stages of [2 K blocks][gate | up 128 rows] +
+  // [2][<= 128 token rows].  Down (chosen by the tile plan): 2 stages of
+  // [2][128 rows] + [2][<= 256 token rows], one per K step of a tile, or 3
+  // stages of [2][128 rows] + [2][<= 128 token rows], one per K step and
+  // 128-row half of a tile (the weights are then loaded once per half; the
+  // second load hits L2).
+  const bool wide = !kGateUp && plan[3 * (nseg + 1) + 2] != 0;
+  const uint32_t nst = (kGateUp || wide) ? 2u : 3u;
+  const uint32_t stage_bytes = C::STAGE_A + (wide ? 2 : 1) * C::STAGE_HALF;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total = pref[nseg];
   const int nkb = K / kBK;
-  // work unit = one K piece of a tile (S == 1: the whole tile)
-  const int S = *s_split;
-  const int kbs = (nkb + S - 1) / S;
+  // work unit = one K piece of a tile: kbs K blocks (the whole tile, or an
+  // even number when the plan splits K)
+  const int kbs = *s_kbs;
+  const int S = (nkb + kbs - 1) / kbs;
   const int total_pieces = total * S;
 
   if (warp == 4) {
     // ------------------------------------------------------ TMA producer --
+    // A stage holds two K blocks: the weight tile(s) [2][NA x 128 x 64] in one
+    // copy and the token rows [2][h x 64] of one 128-row half (or of both
+    // halves in the wide layout) in one copy per half, h = rows rounded up
+    // to 16.
     if (lane == 0) {
-      uint32_t it = 0;
+      uint32_t st = 0, ph = 0, issued = 0;  // stage, parity of its use, stages issued
       bool ok = true;
       for (int pc = blockIdx.x; ok && pc < total_pieces; pc += gridDim.x) {
         const int tile = pc / S, z = pc - tile * S;
-        const Tile t = decode_tile<BN>(tile, seg_row, pref, nseg);
+        const Tile t = decode_tile<kTR>(tile, seg_row, pref, nseg);
         const int kb0 = z * kbs, kb1 = min(nkb, kb0 + kbs);
         const bool sh = (t.seg >= E);
         const CUtensorMap *ma = sh ? &tm_a_sh : &tm_a;
         const int ecoord = sh ? 0 : t.seg;
-        const int nb16 = (t.nrows + 15) >> 4;
-        const uint32_t bytes = C::NA * C::A_BYTES + (uint32_t)nb16 * C::B16_BYTES;
-        for (int kb = kb0; kb < kb1; ++kb, ++it) {
-          const int st = (int)(it % STAGES);
-          const uint32_t ph = (it / STAGES) & 1u;
-          if (!mbar_wait(&empty[st], ph ^ 1u, abort_flag, status, kCode)) {
-            ok = false;
-            break;
+        const int h0 = min(128, (t.nrows + 15) & ~15);        // rows of half 0, padded
+        const int h1 = max(0, ((t.nrows + 15) & ~15) - 128);  // rows of half 1, padded
+        const int nu = (!wide && h1 > 0) ? 2 : 1;  // stages per K step
+        for (int kb = kb0; ok && kb < kb1; kb += kStageKB) {
+          for (int u = 0; u < nu; ++u) {
+            if (!mbar_wait(&empty[st], ph ^ 1u, abort_flag, status, kCode)) {
+              ok = false;
+              break;
+            }
+            uint8_t *dst = ring + st * stage_bytes;
+            const int hb = (u == 0) ? h0 : h1;  // token rows of this stage's first copy
+            const bool second = (nu == 1 && h1 > 0);
+            mbar_arrive_expect_tx(&full[st], C::STAGE_A + (uint32_t)(hb + (second ? h1 : 0)) *
+                                                              (kStageKB * kBK * 2));
+            // [2 K blocks][P][128 rows][64]: gate/up P = 2 (gate, then the
+            // same up rows), down P = 1
+            tma_load_5d(dst, ma, &full[st], 0, t.j * kBM, 0, kb, ecoord);
+            tma_load_3d(dst + C::STAGE_A, &tm_b.m[(hb >> 4) - 1], &full[st], 0, t.row0 + u * 128,
+                        kb);
+            if (second)
+              tma_load_3d(dst + C::STAGE_A + C::STAGE_HALF, &tm_b.m[(h1 >> 4) - 1], &full[st], 0,
+                          t.row0 + 128, kb);
+            ++issued;
+            if (++st == nst) {
+              st = 0;
+              ph ^= 1u;
+            }
           }
-          mbar_arrive_expect_tx(&full[st], bytes);
-          uint8_t *a0 = sA + (size_t)st * C::NA * C::A_BYTES;
-          tma_load_4d(a0, ma, &full[st], kb * kBK, t.j * kBM, 0, ecoord);
-          if (kGateUp) tma_load_4d(a0 + C::A_BYTES, ma, &full[st], kb * kBK, t.j * kBM, 1, ecoord);
-          uint8_t *b0 = sB + (size_t)st * C::B_BYTES;
-          for (int q = 0; q < nb16; ++q)
-            tma_load_2d(b0 + q * C::B16_BYTES, &tm_b, &full[st], kb * kBK, t.row0 + q * 16);
         }
       }
       // Drain: every issued copy must land before the CTA may exit.
-      const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
-      for (uint32_t i = first; i < it; ++i) mbar_wait_drain(&full[i % STAGES], (i / STAGES) & 1u);
+      const uint32_t n = issued < nst ? issued : nst;
+      for (uint32_t i = 0; i < n; ++i) {
+        // the n most recent uses, newest first
+        st = st == 0 ? nst - 1 : st - 1;
+        if (st == nst - 1) ph ^= 1u;
+        mbar_wait_drain(&full[st], ph);
+      }
     }
     __syncwarp();
   } else if (warp == 5) {
     // ------------------------------------------------------- MMA issuer --
     if (lane == 0) {
-      uint32_t it = 0, tl = 0;
+      uint32_t st = 0, ph = 0, tl = 0;  // stage, parity, tiles
+      // stage descriptors differ only in the start-address field (16-byte units)
+      const uint64_t desc0 = sdesc_k_sw128(smem_u32(ring));
+      const uint32_t dstage = stage_bytes >> 4;
       bool ok = true;
       for (int pc = blockIdx.x; ok && pc < total_pieces; pc += gridDim.x, ++tl) {
         const int tile = pc / S, z = pc - tile * S;
-        const Tile t = decode_tile<BN>(tile, seg_row, pref, nseg);
+        const Tile t = decode_tile<kTR>(tile, seg_row, pref, nseg);
         const int kb0 = z * kbs, kb1 = min(nkb, kb0 + kbs);
-        const int N = (t.nrows + 15) & ~15;
-        const uint32_t idesc = idesc_bf16_f32(kBM, N);
+        const int h0 = min(128, (t.nrows + 15) & ~15);
+        const int h1 = max(0, ((t.nrows + 15) & ~15) - 128);
+        const int nu = (!wide && h1 > 0) ? 2 : 1;
+        // down: token half 0 -> accumulator columns [0, 128), half 1 ->
+        // [128, 256); gate/up: gate rows -> [0, 128), up rows -> [128, 256)
+        const uint32_t idesc0 = idesc_bf16_f32(kBM, h0);
+        const uint32_t idesc1 = idesc_bf16_f32(kBM, h1 > 0 ? h1 : 16);
         const uint32_t buf = tl & 1u, use = tl >> 1;
         if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, status, kCode)) break;
         tc_fence_after();
-        const uint32_t d0 = tmem_base + buf * C::ACC_COLS;
-        for (int kb = kb0; kb < kb1; ++kb, ++it) {
-          const int st = (int)(it % STAGES);
-          if (!mbar_wait(&full[st], (it / STAGES) & 1u, abort_flag, status, kCode)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a_addr = smem_u32(sA + (size_t)st * C::NA * C::A_BYTES);
-          const uint32_t b_addr = smem_u32(sB + (size_t)st * C::B_BYTES);
-          const uint64_t adesc = sdesc_k_sw128(a_addr);
-          const uint64_t bdesc = sdesc_k_sw128(b_addr);
-#pragma unroll
-          for (int ks = 0; ks < kBK / 16; ++ks) {
-            // advance 16 bf16 (32 bytes) along K inside the swizzled row
-            const uint32_t acc = (kb != kb0 || ks != 0) ? 1u : 0u;
-            umma_bf16(d0, adesc + 2 * ks, bdesc + 2 * ks, idesc, acc);
-            if (kGateUp) {
-              const uint64_t adesc_up = sdesc_k_sw128(a_addr + C::A_BYTES);
-              umma_bf16(d0 + BN, adesc_up + 2 * ks, bdesc + 2 * ks, idesc, acc);
+        const uint32_t d0 = tmem_base + buf * kAccCols;
+        for (int kb = kb0; ok && kb < kb1; kb += kStageKB) {
+          const int nc = min(kStageKB, kb1 - kb);  // K blocks of this piece in the stage
+          for (int u = 0; u < nu; ++u) {
+            if (!mbar_wait(&full[st], ph, abort_flag, status, kCode)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t adesc = desc0 + st * dstage;
+            const uint64_t bdesc = adesc + (C::STAGE_A >> 4);
+            const int hb = (u == 0) ? h0 : h1;
+            for (int c = 0; c < nc; ++c) {
+              const uint32_t acc = (kb != kb0 || c != 0) ? 1u : 0u;
+              const uint64_t ac = adesc + c * (C::NA * kChunkBytes >> 4);
+              const uint64_t bc = bdesc + c * ((uint32_t)hb * (kBK * 2) >> 4);
+              if (kGateUp) {
+                umma_kblock(d0, ac, bc, idesc0, acc);                              // gate
+                umma_kblock(d0 + 128, ac + (kChunkBytes >> 4), bc, idesc0, acc);  // up
+              } else {
+                umma_kblock(d0 + (uint32_t)u * 128, ac, bc, u == 0 ? idesc0 : idesc1, acc);
+                if (nu == 1 && h1 > 0)
+                  umma_kblock(d0 + 128, ac,
+                              bdesc + (C::STAGE_HALF >> 4) + c * ((uint32_t)h1 * (kBK * 2) >> 4),
+                              idesc1, acc);
+              }
+            }
+            umma_commit(&empty[st]);  // the stage is free once these MMAs have read it
+            if (++st == nst) {
+              st = 0;
+              ph ^= 1u;
             }
           }
-          umma_commit(&empty[st]);  // stage free once these MMAs have read it
         }
         if (!ok) break;
         umma_commit(&tfull[buf]);  // accumulator complete
@@ -315,16 +388,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // --------------------------------------------------------- epilogue --
-    // Per 16-token slice: tcgen05.ld of the thread's weight row (16 token
-    // columns), fused SiLU(gate)*up or gate weighting, the slice written
-    // transposed into smem, then stored as token rows with 16-byte vector
-    // stores by all 128 epilogue threads.  A split-K piece instead writes its
-    // fp32 partial; the last piece of the tile adds the S partials in split
-    // order and runs the same epilogue.
+    // Per 16-token slice: tcgen05.ld of the thread's accumulator row(s) (16
+    // token columns), fused SiLU(gate)*up or gate weighting, the slice
+    // written transposed into smem (two buffers, alternating), then stored
+    // as token rows with 16-byte vector stores by all 128 epilogue threads.
+    // A split-K piece instead writes its fp32 partial; the last piece of the
+    // tile adds the S partials in split order and runs the same epilogue.
     const int r = warp * 32 + lane;  // TMEM lane = weight row of the tile
-    uint32_t tl = 0;
+    uint32_t tl = 0, slice = 0;
     bool range_bad = false;
     auto emit16 = [&](const Tile &t, int n0, const float(&g)[16], const float(&u)[16]) {
+      uint16_t *so = sOut + (slice & 1u) * (16 * kBM);
 #pragma unroll
       for (int q = 0; q < 16; ++q) {
         uint16_t bits;
@@ -335,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           range_bad |= !(fabsf(val) <= 65504.0f);
           bits = __half_as_ushort(__float2half_rn(fminf(fmaxf(val, -65504.0f), 65504.0f)));
         }
-        sOut[q * kBM + r] = bits;
+        so[q * kBM + r] = bits;
       }
       epi_sync();
       // 16 token rows x 128 columns x 2 bytes = 256 chunks of 16 bytes
@@ -345,33 +419,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = n0 + q, col = col0 + ch * 8;
         if (n < t.nrows && col < out_cols)
           *reinterpret_cast<uint4 *>(out + ((int64_t)t.row0 + n) * out_cols + col) =
-              *reinterpret_cast<const uint4 *>(sOut + q * kBM + ch * 8);
+              *reinterpret_cast<const uint4 *>(so + q * kBM + ch * 8);
       }
-      epi_sync();
+      ++slice;
     };
     constexpr int kSlot = C::NA * kBM * kSplitMaxRows;  // floats of one piece's partial
     for (int pc = blockIdx.x; pc < total_pieces; pc += gridDim.x, ++tl) {
       const int tile = pc / S, z = pc - tile * S;
-      const Tile t = decode_tile<BN>(tile, seg_row, pref, nseg);
+      const Tile t = decode_tile<kTR>(tile, seg_row, pref, nseg);
       const uint32_t buf = tl & 1u, use = tl >> 1;
       const bool waited = mbar_wait(&tfull[buf], use & 1u, abort_flag, status, kCode);
       // one decision for all 128 epilogue threads: they share named barriers
       if (!epi_all(waited && !*abort_flag)) break;
       tc_fence_after();
       if (!kGateUp) {
-        for (int n = r; n < BN; n += 128) {
+        for (int n = r; n < kTR; n += 128) {
           const int64_t row = (int64_t)t.row0 + n;
           sW[n] = (n < t.nrows && w_perm != nullptr && row < Na) ? w_perm[row] : 1.0f;
         }
         epi_sync();
       }
-      const uint32_t tb = tmem_base + ((uint32_t)(warp * 32) << 16) + buf * C::ACC_COLS;
+      const uint32_t tb = tmem_base + ((uint32_t)(warp * 32) << 16) + buf * kAccCols;
       const int N = (t.nrows + 15) & ~15;
       if (S == 1) {
         for (int n0 = 0; n0 < N; n0 += 16) {
           uint32_t v0[16], v1[16];
           tmem_ld16(tb + n0, v0);
-          if (kGateUp) tmem_ld16(tb + BN + n0, v1);
+          if (kGateUp) tmem_ld16(tb + 128 + n0, v1);
           tmem_ld_wait();
           float g[16], u[16];
 #pragma unroll
@@ -387,19 +461,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       // ---- split-K piece (N <= kSplitMaxRows): fp32 partial to global ----
-      float *slot = split_part + (size_t)(tile * S + z) * kSlot + (size_t)r * kSplitMaxRows;
+      float *part = split_part + (size_t)(tile * S + z) * kSlot + (size_t)r * kSplitMaxRows;
       for (int n0 = 0; n0 < N; n0 += 16) {
         uint32_t v0[16], v1[16];
         tmem_ld16(tb + n0, v0);
-        if (kGateUp) tmem_ld16(tb + BN + n0, v1);
+        if (kGateUp) tmem_ld16(tb + 128 + n0, v1);
         tmem_ld_wait();
 #pragma unroll
         for (int q = 0; q < 16; q += 4) {
-          *reinterpret_cast<float4 *>(slot + n0 + q) =
+          *reinterpret_cast<float4 *>(part + n0 + q) =
               make_float4(__uint_as_float(v0[q]), __uint_as_float(v0[q + 1]),
                           __uint_as_float(v0[q + 2]), __uint_as_float(v0[q + 3]));
           if (kGateUp)
-            *reinterpret_cast<float4 *>(slot + kBM * kSplitMaxRows + n0 + q) =
+            *reinterpret_cast<float4 *>(part + kBM * kSplitMaxRows + n0 + q) =
                 make_float4(__uint_as_float(v1[q]), __uint_as_float(v1[q + 1]),
                             __uint_as_float(v1[q + 2]), __uint_as_float(v1[q + 3]));
         }
@@ -449,35 +523,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 5) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
+    tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
 // ---------------------------------------------------------------- host --
 
-// Weight map viewed as [E][P][rows][K] (P = 2 halves of W13, or 1 for W2).
-bool weight_map(CUtensorMap *m, const void *w, int K, int rows, int P, int E) {
-  const cuuint64_t dims[4] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)P, (cuuint64_t)E};
+// Weight map: W viewed as [E][P][rows][K] (P = 2 halves of W13, or 1 for
+// W2) with K split into 64-element blocks, the block index ordered after the
+// rows: dims {64, rows, P, K/64, E}.  A box [kStageKB][P][box_rows][64] lands
+// in shared memory as kStageKB consecutive 128-row K-major tiles.
+bool weight_map(CUtensorMap *m, const void *w, int K, int rows, int P, int E, int box_rows) {
+  const cuuint64_t dims[5] = {(cuuint64_t)kBK, (cuuint64_t)rows, (cuuint64_t)P,
+                              (cuuint64_t)(K / kBK), (cuuint64_t)E};
   const cuuint64_t rs = (cuuint64_t)K * 2;
-  const cuuint64_t strides[3] = {rs, rs * rows, rs * rows * P};
-  const cuuint32_t box[4] = {(cuuint32_t)kBK, (cuuint32_t)kBM, 1, 1};
-  return encode_bf16_map(m, w, 4, dims, strides, box);
+  const cuuint64_t strides[4] = {rs, rs * rows, (cuuint64_t)kBK * 2, rs * rows * P};
+  const cuuint32_t box[5] = {(cuuint32_t)kBK, (cuuint32_t)box_rows, (cuuint32_t)P,
+                             (cuuint32_t)kStageKB, 1};
+  return encode_bf16_map(m, w, 5, dims, strides, box);
 }
 
-bool act_map(CUtensorMap *m, const void *a, int K, int64_t R) {
-  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)R};
-  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kBK, 16};
-  return encode_bf16_map(m, a, 2, dims, strides, box);
+// Token rows [R][K] viewed as dims {64, R, K/64}; a box [kStageKB][h][64].
+bool act_map(CUtensorMap *m, const void *a, int K, int64_t R, int box_rows) {
+  const cuuint64_t dims[3] = {(cuuint64_t)kBK, (cuuint64_t)R, (cuuint64_t)(K / kBK)};
+  const cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)kBK * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)kBK, (cuuint32_t)box_rows, (cuuint32_t)kStageKB};
+  return encode_bf16_map(m, a, 3, dims, strides, box);
 }
 
-template <bool kGateUp, int BN, int STAGES>
+template <bool kGateUp>
 cudaError_t launch_gemm(const moe_layer_desc_t &d, const void *w, const void *w_sh,
                         const __nv_bfloat16 *act, const int32_t *plan, const float *w_perm,
                         void *out, float *split_part, uint32_t *split_cnt, uint32_t *status,
                         cudaStream_t s) {
-  using C = Cfg<kGateUp, BN, STAGES>;
-  static_assert(BN == (kGateUp ? kBNGateUp : kBNDown), "the tile plan's token chunks");
+  using C = Cfg<kGateUp>;
   const int shared = d.has_shared_expert ? 1 : 0;
   const int nseg = d.E + shared;
   const int64_t Na = (int64_t)d.T * d.k;
@@ -485,17 +564,20 @@ cudaError_t launch_gemm(const moe_layer_desc_t &d, const void *w, const void *w_
   const int K = kGateUp ? d.H : d.I;
   const int rows = kGateUp ? d.I : d.H;  // weight rows per half = output columns
   const int P = kGateUp ? 2 : 1;
-  CUtensorMap ma, msh, mb;
-  if (!weight_map(&ma, w, K, rows, P, d.E)) return cudaErrorInvalidValue;
+  const int box_rows = kBM;  // rows of each half of W13 / of W2 per tile
+  CUtensorMap ma, msh;
+  TokenMaps mb;
+  if (!weight_map(&ma, w, K, rows, P, d.E, box_rows)) return cudaErrorInvalidValue;
   if (shared) {
-    if (!weight_map(&msh, w_sh, K, rows, P, 1)) return cudaErrorInvalidValue;
+    if (!weight_map(&msh, w_sh, K, rows, P, 1, box_rows)) return cudaErrorInvalidValue;
   } else {
     msh = ma;
   }
-  if (!act_map(&mb, act, K, R)) return cudaErrorInvalidValue;
+  for (int i = 0; i < 8; ++i)
+    if (!act_map(&mb.m[i], act, K, R, 16 * (i + 1))) return cudaErrorInvalidValue;
 
   const size_t smem = C::smem_bytes(nseg);
-  auto kern = expert_gemm_kernel<kGateUp, BN, STAGES>;
+  auto kern = expert_gemm_kernel<kGateUp>;
   static size_t configured[64] = {};  // per device
   int dev = 0;
   cudaGetDevice(&dev);
@@ -519,16 +601,16 @@ cudaError_t launch_expert_gateup(const moe_layer_desc_t &d, const void *w13, con
                                  const __nv_bfloat16 *x_perm, const int32_t *plan,
                                  float *split_part, uint32_t *split_cnt, __nv_bfloat16 *h,
                                  uint32_t *status, cudaStream_t s) {
-  return launch_gemm<true, kBNGateUp, kStagesGateUp>(d, w13, w13_shared, x_perm, plan, nullptr, h,
-                                                     split_part, split_cnt, status, s);
+  return launch_gemm<true>(d, w13, w13_shared, x_perm, plan, nullptr, h, split_part, split_cnt,
+                          status, s);
 }
 
 cudaError_t launch_expert_down(const moe_layer_desc_t &d, const void *w2, const void *w2_shared,
                                const __nv_bfloat16 *h, const int32_t *plan, const float *w_perm,
                                float *split_part, uint32_t *split_cnt, __half *out_perm,
                                uint32_t *status, cudaStream_t s) {
-  return launch_gemm<false, kBNDown, kStagesDown>(d, w2, w2_shared, h, plan, w_perm, out_perm,
-                                                  split_part, split_cnt, status, s);
+  return launch_gemm<false>(d, w2, w2_shared, h, plan, w_perm, out_perm, split_part, split_cnt,
+                           status, s);
 }
 
 }  // namespace moe

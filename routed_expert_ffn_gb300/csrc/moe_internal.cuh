@@ -46,24 +46,19 @@ inline int64_t dispatch_chunk(int64_t Na) {
   return c < kDispatchThreads ? kDispatchThreads : c;
 }
 
-// Expert GEMMs (tcgen05): weight rows per tile, K per pipeline stage, and the
-// token rows per tile (chunk) of each GEMM, with its smem pipeline depth.
-#ifndef MOE_BN_GATEUP
-#define MOE_BN_GATEUP 128
-#endif
-#ifndef MOE_BN_DOWN
-#define MOE_BN_DOWN 128
-#endif
-#ifndef MOE_STAGES_GATEUP
-#define MOE_STAGES_GATEUP 4
-#endif
-#ifndef MOE_STAGES_DOWN
-#define MOE_STAGES_DOWN 6
-#endif
+// Expert GEMMs (tcgen05), stepped through K in blocks of kBK, two blocks per
+// pipeline stage.  Gate/up tile: 128 gate rows and the same 128 up rows of
+// W13 (128 columns of h) by up to kTileRowsGateUp token rows; 2 stages of
+// 96 KB.  Down tile: 128 rows of W2 (128 output columns) by up to
+// kTileRowsDown token rows; 3 stages of weights + 128 token rows (a wider
+// tile runs one stage per 128-row half), or -- when most tiles are wider --
+// 2 stages of weights + 256 token rows.
 constexpr int kBM = 128;
 constexpr int kBK = 64;
-constexpr int kBNGateUp = MOE_BN_GATEUP;
-constexpr int kBNDown = MOE_BN_DOWN;
+constexpr int kTileRowsGateUp = 128;
+constexpr int kTileRowsDown = 256;
+constexpr int kStageKB = 2;
+constexpr int kRingBytes = 3 * 65536;  // = 2 * 98304
 
 // Status word bits (latched with atomicOr).
 constexpr uint32_t kStatusBadExpertId = 1u << 0;
@@ -99,12 +94,13 @@ int route_splits(int T, int E, int H);
 //   [nseg+1, 2nseg+1]         gate/up tile prefix (nseg+1)
 //   [2nseg+2, 3nseg+2]        down tile prefix (nseg+1)
 //   [3nseg+3], [3nseg+4]      split-K factor S of the gate/up and down GEMM
-inline int plan_ints(int nseg) { return 3 * (nseg + 1) + 2; }
+inline int plan_ints(int nseg) { return 3 * (nseg + 1) + 3; }
 
 // Split-K for small batches: when every tile has at most kSplitMaxRows token
 // rows and there are too few tiles to occupy the GPU, each tile's K range is
 // cut into S pieces (S <= kMaxSplit, at most kMaxSplitTiles pieces in all);
-// each piece writes an fp32 partial [NA][kBM][kSplitMaxRows] and the last to
+// each piece writes an fp32 partial [NA][kBM][kSplitMaxRows] (NA = 2 for
+// gate/up, 1 for down) and the last to
 // finish adds them in split order.
 constexpr int kSplitMaxRows = 32;
 constexpr int kMaxSplit = 16;
@@ -275,15 +271,14 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *m, uin
       "l"(m), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
-__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *m, uint64_t *bar, int c0,
-                                            int c1, int c2, int c3) {
+__device__ __forceinline__ void tma_load_5d(void *dst, const CUtensorMap *m, uint64_t *bar, int c0,
+                                            int c1, int c2, int c3, int c4) {
   asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(m), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(m), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
       : "memory");
 }
-
 // --- tcgen05: tensor memory, MMA, loads ---
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
