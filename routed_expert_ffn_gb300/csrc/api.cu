@@ -4,6 +4,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -35,7 +37,7 @@ Layout make_layout(const moe_layer_desc_t &d) {
   const int shared = d.has_shared_expert ? 1 : 0;
   L.rows = Na + (shared ? d.T : 0);
   L.nseg = d.E + shared;
-  L.route_splits = route_splits(d.T, d.E, d.H);
+  L.route_splits = route_splits(d.T, d.E, d.H, kRouteSizingSms);  // the most a launch uses
   const int64_t chunk = dispatch_chunk(Na);
   L.nblk = (int)((Na + chunk - 1) / chunk);
   L.status = take(kStatusBlockBytes);
@@ -130,11 +132,11 @@ cudaError_t route(const moe_layer_desc_t &d, const Layout &L, const __nv_bfloat1
     return launch_route_small(x, w_router, sel_bias, d.T, d.H, d.E, d.k, d.gating, logits, ids, w,
                               gap, status + kRouteCounterWord, s);
   float *part = at<float>(workspace, L.route_part);
-  cudaError_t e = launch_router_logits(x, w_router, d.T, d.H, d.E, L.route_splits,
+  const int splits = route_splits(d.T, d.E, d.H, std::min(num_sms(), kRouteSizingSms));
+  cudaError_t e = launch_router_logits(x, w_router, d.T, d.H, d.E, splits,
                                        at<__nv_bfloat16>(workspace, L.router_w), part, status, s);
   if (e == cudaSuccess)
-    e = launch_topk_gating(part, L.route_splits, sel_bias, d.T, d.E, d.k, d.gating, logits, ids, w,
-                           gap, s);
+    e = launch_topk_gating(part, splits, sel_bias, d.T, d.E, d.k, d.gating, logits, ids, w, gap, s);
   return e;
 }
 __nv_bfloat16 *bfw(void *p) { return static_cast<__nv_bfloat16 *>(p); }

@@ -28,8 +28,7 @@ __global__ void __launch_bounds__(256)
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-  auto add_row = [&](int64_t row, float wt) {
-    const uint4 raw = reinterpret_cast<const uint4 *>(out_perm + row * H)[v];
+  auto add = [&](const uint4 &raw, float wt) {
     const __half2 *p = reinterpret_cast<const __half2 *>(&raw);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -38,13 +37,31 @@ __global__ void __launch_bounds__(256)
       acc[2 * i + 1] = fmaf(wt, f.y, acc[2 * i + 1]);
     }
   };
-  for (int j = 0; j < k; ++j) {
-    const int64_t a = (int64_t)t * k + j;
-    const int32_t p = inv_pos[a];
-    if (p < 0 || p >= Na) continue;
-    add_row(p, topk_w != nullptr ? topk_w[a] : 1.0f);
+  // up to kBatch expert rows in flight, added in slot order
+  constexpr int kBatch = 8;
+  for (int j0 = 0; j0 < k; j0 += kBatch) {
+    uint4 raw[kBatch];
+    float wt[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      wt[i] = 0.f;
+      raw[i] = make_uint4(0, 0, 0, 0);
+      const int j = j0 + i;
+      if (j < k) {
+        const int64_t a = (int64_t)t * k + j;
+        const int32_t p = inv_pos[a];
+        if (p >= 0 && p < Na) {
+          wt[i] = topk_w != nullptr ? topk_w[a] : 1.0f;
+          raw[i] = reinterpret_cast<const uint4 *>(out_perm + (int64_t)p * H)[v];
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      if (j0 + i < k) add(raw[i], wt[i]);
+    }
   }
-  if (shared) add_row(Na + t, 1.0f);
+  if (shared) add(reinterpret_cast<const uint4 *>(out_perm + (Na + t) * H)[v], 1.0f);
   uint4 o;
   __nv_bfloat162 *q = reinterpret_cast<__nv_bfloat162 *>(&o);
 #pragma unroll

@@ -87,7 +87,10 @@ struct Layout {
 
 // Host: workspace layout of a (validated) descriptor.
 Layout make_layout(const moe_layer_desc_t &d);
-int route_splits(int T, int E, int H);
+// K splits of the tensor-core router for `nsm` SMs (monotone in nsm); the
+// workspace is sized for kRouteSizingSms, launches use min(SMs, that).
+int route_splits(int T, int E, int H, int nsm);
+constexpr int kRouteSizingSms = 256;
 
 // Tile plan layout inside the plan buffer (int32):
 //   [0, nseg]                 segment row offsets (nseg+1)

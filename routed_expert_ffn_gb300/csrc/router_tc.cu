@@ -231,10 +231,11 @@ __global__ void __launch_bounds__(kRThreads, 1)
 
 }  // namespace
 
-int route_splits(int T, int E, int H) {
+int route_splits(int T, int E, int H, int nsm) {
   const int tiles = ((E + kBM - 1) / kBM) * ((T + kRBN - 1) / kRBN);
   const int nkb = H / kBK;
-  int want = (304 + tiles - 1) / tiles;
+  // at most one CTA per SM (each holds all of TMEM): one wave
+  int want = nsm / tiles;
   int cap = nkb / 4;  // at least 4 K blocks per split
   if (cap > kRouteMaxSplits) cap = kRouteMaxSplits;
   if (cap < 1) cap = 1;
