@@ -96,16 +96,17 @@ constexpr int kThreads = 192;
 constexpr uint32_t kChunkBytes = kBM * kBK * 2;  // 16 KB: 128 rows x 64 bf16
 constexpr uint32_t kTmemCols = 512;              // two accumulators of 256 columns
 constexpr uint32_t kAccCols = kTmemCols / 2;
-constexpr int kMaxStages = 3;
-static_assert(kStageKB == 2, "stages are pairs of K blocks");
-static_assert(kRingBytes == 2 * (2 * kStageKB * kChunkBytes + kStageKB * kChunkBytes) &&
-                  kRingBytes == 3 * (2 * kStageKB * kChunkBytes) &&
-                  kRingBytes == 2 * (3 * kStageKB * kChunkBytes),
+// stage sizes (in units of kStageKB * 16 KB): gate/up 3, down 2 (narrow) or 3
+constexpr int kMaxStages = kRingBytes / (2 * kStageKB * kChunkBytes);
+static_assert(kStageKB == 1 || kStageKB == 2, "one or two K blocks per stage");
+static_assert(kRingBytes % (2 * kStageKB * kChunkBytes) == 0 &&
+                  kRingBytes % (3 * kStageKB * kChunkBytes) == 0,
               "the ring holds whole stages of every layout");
 
-// Token-row tensor maps with box heights 16, 32, ..., 128 rows (x 2 K blocks).
+// Token-row tensor maps with box heights 16, 32, ..., 256 rows (x kStageKB K
+// blocks).
 struct TokenMaps {
-  CUtensorMap m[8];
+  CUtensorMap m[16];
 };
 
 template <bool kGateUp>
@@ -235,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 4 && lane == 0) {
     tma_prefetch_desc(&tm_a);
     tma_prefetch_desc(&tm_a_sh);
-    for (int i = 0; i < 8; ++i) tma_prefetch_desc(&tm_b.m[i]);
+    for (int i = 0; i < 16; ++i) tma_prefetch_desc(&tm_b.m[i]);
   }
   // everything above is independent of earlier kernels' outputs
   pdl_wait();
@@ -253,8 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // 128-row half of a tile (the weights are then loaded once per half; the
   // second load hits L2).
   const bool wide = !kGateUp && plan[3 * (nseg + 1) + 2] != 0;
-  const uint32_t nst = (kGateUp || wide) ? 2u : 3u;
   const uint32_t stage_bytes = C::STAGE_A + (wide ? 2 : 1) * C::STAGE_HALF;
+  const uint32_t nst = kRingBytes / stage_bytes;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -293,18 +294,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             uint8_t *dst = ring + st * stage_bytes;
-            const int hb = (u == 0) ? h0 : h1;  // token rows of this stage's first copy
-            const bool second = (nu == 1 && h1 > 0);
-            mbar_arrive_expect_tx(&full[st], C::STAGE_A + (uint32_t)(hb + (second ? h1 : 0)) *
-                                                              (kStageKB * kBK * 2));
-            // [2 K blocks][P][128 rows][64]: gate/up P = 2 (gate, then the
+            // token rows of this stage: one 128-row unit, or (nu == 1) the
+            // whole tile, up to 256 rows in the wide layout
+            const int hb = (nu == 2) ? (u == 0 ? h0 : h1) : h0 + h1;
+            mbar_arrive_expect_tx(&full[st], C::STAGE_A + (uint32_t)hb * (kStageKB * kBK * 2));
+            // [K blocks][P][128 rows][64]: gate/up P = 2 (gate, then the
             // same up rows), down P = 1
             tma_load_5d(dst, ma, &full[st], 0, t.j * kBM, 0, kb, ecoord);
             tma_load_3d(dst + C::STAGE_A, &tm_b.m[(hb >> 4) - 1], &full[st], 0, t.row0 + u * 128,
                         kb);
-            if (second)
-              tma_load_3d(dst + C::STAGE_A + C::STAGE_HALF, &tm_b.m[(h1 >> 4) - 1], &full[st], 0,
-                          t.row0 + 128, kb);
             ++issued;
             if (++st == nst) {
               st = 0;
@@ -338,9 +336,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h0 = min(128, (t.nrows + 15) & ~15);
         const int h1 = max(0, ((t.nrows + 15) & ~15) - 128);
         const int nu = (!wide && h1 > 0) ? 2 : 1;
-        // down: token half 0 -> accumulator columns [0, 128), half 1 ->
-        // [128, 256); gate/up: gate rows -> [0, 128), up rows -> [128, 256)
-        const uint32_t idesc0 = idesc_bf16_f32(kBM, h0);
+        // down: token column n -> accumulator column n (a wide tile in the
+        // narrow layout as two 128-row units); gate/up: gate rows -> columns
+        // [0, 128), up rows -> [128, 256)
+        const uint32_t idesc0 = idesc_bf16_f32(kBM, nu == 2 ? h0 : h0 + h1);
         const uint32_t idesc1 = idesc_bf16_f32(kBM, h1 > 0 ? h1 : 16);
         const uint32_t buf = tl & 1u, use = tl >> 1;
         if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, status, kCode)) break;
@@ -356,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint64_t adesc = desc0 + st * dstage;
             const uint64_t bdesc = adesc + (C::STAGE_A >> 4);
-            const int hb = (u == 0) ? h0 : h1;
+            const int hb = (nu == 2) ? (u == 0 ? h0 : h1) : h0 + h1;
             for (int c = 0; c < nc; ++c) {
               const uint32_t acc = (kb != kb0 || c != 0) ? 1u : 0u;
               const uint64_t ac = adesc + c * (C::NA * kChunkBytes >> 4);
@@ -365,11 +364,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma_kblock(d0, ac, bc, idesc0, acc);                              // gate
                 umma_kblock(d0 + 128, ac + (kChunkBytes >> 4), bc, idesc0, acc);  // up
               } else {
+                // one MMA over all of the stage's token rows (N <= 256)
                 umma_kblock(d0 + (uint32_t)u * 128, ac, bc, u == 0 ? idesc0 : idesc1, acc);
-                if (nu == 1 && h1 > 0)
-                  umma_kblock(d0 + 128, ac,
-                              bdesc + (C::STAGE_HALF >> 4) + c * ((uint32_t)h1 * (kBK * 2) >> 4),
-                              idesc1, acc);
               }
             }
             umma_commit(&empty[st]);  // the stage is free once these MMAs have read it
@@ -573,7 +569,7 @@ cudaError_t launch_gemm(const moe_layer_desc_t &d, const void *w, const void *w_
   } else {
     msh = ma;
   }
-  for (int i = 0; i < 8; ++i)
+  for (int i = 0; i < 16; ++i)
     if (!act_map(&mb.m[i], act, K, R, 16 * (i + 1))) return cudaErrorInvalidValue;
 
   const size_t smem = C::smem_bytes(nseg);

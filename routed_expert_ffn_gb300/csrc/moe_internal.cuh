@@ -57,7 +57,10 @@ constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr int kTileRowsGateUp = 128;
 constexpr int kTileRowsDown = 256;
-constexpr int kStageKB = 2;
+#ifndef MOE_STAGE_KB
+#define MOE_STAGE_KB 2
+#endif
+constexpr int kStageKB = MOE_STAGE_KB;
 constexpr int kRingBytes = 3 * 65536;  // = 2 * 98304
 
 // Status word bits (latched with atomicOr).
