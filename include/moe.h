@@ -127,6 +127,16 @@ typedef struct {
   size_t x_perm;       /* [R,H] bf16 tokens grouped by expert             */
   size_t h;            /* [R,I] bf16 SiLU(gate)*up                        */
   size_t out_perm;     /* [R,H] fp16 gate-weighted expert outputs         */
+  size_t plan;         /* int32 tile plan of the grouped GEMMs, nseg =
+                        * E (+1 with a shared expert) segments:
+                        * [0, nseg]            first permuted row of each
+                        *                      segment, then R
+                        * [nseg+1, 2(nseg+1))  gate/up tile prefix sum
+                        * [2(nseg+1), 3(nseg+1)) down tile prefix sum
+                        * 3(nseg+1) + 0 / 1    K blocks (of 64) per split-K
+                        *                      piece, gate/up / down
+                        * 3(nseg+1) + 2 / 3    pipeline layout, gate/up /
+                        *                      down: 1 = wide, 0 = narrow */
   size_t total;        /* == moe_workspace_size(desc)                     */
 } moe_workspace_layout_t;
 

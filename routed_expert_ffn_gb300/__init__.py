@@ -57,7 +57,7 @@ class LayerWeights(ctypes.Structure):
 
 
 _LAYOUT_FIELDS = ("status", "logits", "topk_ids", "topk_w", "gap", "counts", "offsets",
-                  "perm_src", "inv_pos", "w_perm", "x_perm", "h", "out_perm", "total")
+                  "perm_src", "inv_pos", "w_perm", "x_perm", "h", "out_perm", "plan", "total")
 
 
 class WorkspaceLayout(ctypes.Structure):

@@ -168,6 +168,7 @@ moe_status_t moe_workspace_layout(const moe_layer_desc_t *d, moe_workspace_layou
   out->x_perm = L.x_perm;
   out->h = L.h;
   out->out_perm = L.out_perm;
+  out->plan = L.plan;
   out->total = L.total;
   return MOE_OK;
 }
@@ -275,8 +276,8 @@ moe_status_t moe_grouped_swiglu_ffn(const moe_layer_desc_t *d, const void *x,
   __nv_bfloat16 *h = at<__nv_bfloat16>(workspace, L.h);
   float *split_part = at<float>(workspace, L.split_part);
   uint32_t *split_cnt = at<uint32_t>(workspace, L.status) + kSplitCounterWord;
-  cudaError_t e = launch_gather_plan(bf(x), perm_src, offsets, d->T, d->k, d->E, d->H, d->I,
-                                     d->has_shared_expert, x_perm, plan, status, s);
+  cudaError_t e = launch_gather_plan(bf(x), perm_src, nullptr, offsets, d->T, d->k, d->E, d->H,
+                                     d->I, d->has_shared_expert, x_perm, plan, status, s);
   if (e == cudaSuccess)
     e = launch_expert_gateup(*d, w13, w13_shared, x_perm, plan, split_part, split_cnt, h, status,
                              s);
@@ -341,8 +342,12 @@ moe_status_t moe_layer_forward(const moe_layer_desc_t *d, const moe_layer_weight
                         offsets, perm_src, inv_pos, w_perm, status, s);
   if (e == cudaSuccess) e = mark(2);
   if (e == cudaSuccess)
-    e = launch_gather_plan(bf(x), perm_src, offsets, d->T, d->k, d->E, d->H, d->I,
-                           d->has_shared_expert, x_perm, plan, status, s);
+    // token-order gather (x read once) once x is too large to stay in L2
+    // between its k reads; row order keeps more warps busy for small batches
+    e = launch_gather_plan(bf(x), perm_src,
+                           (int64_t)d->T * d->H * 2 > kGatherByTokenBytes ? inv_pos : nullptr,
+                           offsets, d->T, d->k, d->E, d->H, d->I, d->has_shared_expert, x_perm,
+                           plan, status, s);
   if (e == cudaSuccess) e = mark(3);
   if (e == cudaSuccess)
     e = launch_expert_gateup(*d, w->w13, w->w13_shared, x_perm, plan, split_part, split_cnt, h,

@@ -168,13 +168,18 @@ __device__ int choose_split(int total, int nkb, int num_sms, int max_m) {
 }
 
 // Rows [0, Na): x_perm[p] = x[perm_src[p] / k]; rows [Na, Na+T) (shared
-// expert): x_perm[Na+t] = x[t].  One warp per row, 16-byte vectors.  The last
-// block instead writes the tile plan of the grouped GEMMs.
+// expert): x_perm[Na+t] = x[t].  16-byte vectors.  With inv_pos (the layer
+// forward) one warp per token reads its row of x once and writes it to the
+// token's k positions (and its shared-expert row), so x is read once even
+// when it does not fit in L2; without (the standalone FFN call) one warp per
+// x_perm row.  The last block instead writes the tile plan of the grouped
+// GEMMs.
 __global__ void __launch_bounds__(256)
     gather_plan_kernel(const __nv_bfloat16 *__restrict__ x, const int32_t *__restrict__ perm_src,
-                       const int32_t *__restrict__ offsets, int T, int k, int E, int H, int I,
-                       int shared, __nv_bfloat16 *__restrict__ x_perm, int32_t *__restrict__ plan,
-                       int num_sms, uint32_t *__restrict__ status) {
+                       const int32_t *__restrict__ inv_pos, const int32_t *__restrict__ offsets,
+                       int T, int k, int E, int H, int I, int shared,
+                       __nv_bfloat16 *__restrict__ x_perm, int32_t *__restrict__ plan, int num_sms,
+                       uint32_t *__restrict__ status) {
   pdl_wait();
   pdl_launch_dependents();
   const int64_t Na = (int64_t)T * k;
@@ -182,14 +187,16 @@ __global__ void __launch_bounds__(256)
   if (blockIdx.x == gridDim.x - 1) {
     // ---- tile plan ----
     __shared__ int warp_tot[32];
-    __shared__ int tot_gu, tot_dn, bad, max_m, n_chunks, n_wide;
+    __shared__ int tot_gu, tot_dn, bad, max_m, n_chunks, n_wide, st_narrow, st_wide;
     const int nseg = E + (shared ? 1 : 0);
-    const int nj_gu = (I + kBM - 1) / kBM, nj_dn = (H + kBM - 1) / kBM;
+    const int nj_dn = (H + kBM - 1) / kBM;
     if (threadIdx.x == 0) {
       bad = 0;
       max_m = 0;
       n_chunks = 0;
       n_wide = 0;
+      st_narrow = 0;
+      st_wide = 0;
     }
     __syncthreads();
     // validate the offsets (caller-provided in the standalone call)
@@ -202,23 +209,45 @@ __global__ void __launch_bounds__(256)
     // each thread owns up to 3 consecutive segments (nseg <= 513 < 3*256)
     constexpr int kPer = 3;
     const int s0 = threadIdx.x * kPer;
-    int gu[kPer], dn[kPer], sum_gu = 0, sum_dn = 0;
+    int ms[kPer];
 #pragma unroll
     for (int q = 0; q < kPer; ++q) {
       const int s = s0 + q;
       int m = 0;
       if (!bad && s < nseg) m = (s < E) ? offsets[s + 1] - offsets[s] : T;
+      ms[q] = m;
       if (m > 0) {
         atomicMax(&max_m, m);
-        // down-GEMM token chunks; "wide" ones have more than 128 rows
+        // 256-row token chunks; "wide" ones have more than 128 rows
         atomicAdd(&n_chunks, (m + kTileRowsDown - 1) / kTileRowsDown);
         atomicAdd(&n_wide, m / kTileRowsDown + (m % kTileRowsDown > 128 ? 1 : 0));
+        // gate/up pipeline stages per 128 weight rows and K step: narrow tiles
+        // (128 + 128 rows by <= 128 tokens) vs wide (64 + 64 rows by <= 256)
+        atomicAdd(&st_narrow, (m + kTileRowsGateUp - 1) / kTileRowsGateUp);
+        atomicAdd(&st_wide, 2 * ((m + kTileRowsDown - 1) / kTileRowsDown));
       }
-      gu[q] = (m + kTileRowsGateUp - 1) / kTileRowsGateUp * nj_gu;
-      dn[q] = (m + kTileRowsDown - 1) / kTileRowsDown * nj_dn;
+      if (s < nseg) seg_row[s] = bad ? 0 : ((s < E) ? offsets[s] : (int)Na);
+    }
+    __syncthreads();
+    // Pipeline layouts.  Down: "wide" (stages of 256 token rows) when most
+    // 256-row chunks have more than 128 rows.  Gate/up: wide tiles (64 gate +
+    // 64 up rows by <= 256 token rows, one N <= 256 MMA per K16 step) when
+    // they need at most 9/8 the stages of narrow tiles (128 + 128 rows by
+    // <= 128 token rows, two MMAs per K16 step).  Measured: a wide stage costs
+    // about 0.9 of a narrow one (Mixtral T=4096, ratio 1.04: wide 7% faster;
+    // DeepSeek-V3 T=8192, ratio 1.29: wide 10% slower).
+    const bool wide_dn = n_wide > 0 && 2 * n_wide >= n_chunks;
+    const bool wide_gu = st_narrow > 0 && 8 * st_wide <= 9 * st_narrow;
+    const int tr_gu = wide_gu ? kTileRowsDown : kTileRowsGateUp;
+    const int nj_gu =
+        wide_gu ? (I + kGateUpColsWide - 1) / kGateUpColsWide : (I + kBM - 1) / kBM;
+    int gu[kPer], dn[kPer], sum_gu = 0, sum_dn = 0;
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      gu[q] = (ms[q] + tr_gu - 1) / tr_gu * nj_gu;
+      dn[q] = (ms[q] + kTileRowsDown - 1) / kTileRowsDown * nj_dn;
       sum_gu += gu[q];
       sum_dn += dn[q];
-      if (s < nseg) seg_row[s] = bad ? 0 : ((s < E) ? offsets[s] : (int)Na);
     }
     int run_gu = block_exclusive_scan(sum_gu, warp_tot, &tot_gu);
     int run_dn = block_exclusive_scan(sum_dn, warp_tot, &tot_dn);
@@ -238,14 +267,50 @@ __global__ void __launch_bounds__(256)
       pref_dn[nseg] = tot_dn;
       plan[3 * (nseg + 1)] = choose_split(tot_gu, H / kBK, num_sms, max_m);
       plan[3 * (nseg + 1) + 1] = choose_split(tot_dn, I / kBK, num_sms, max_m);
-      // down-GEMM pipeline layout: stages of weights + 256 token rows when
-      // most chunks are wide, else weights + 128 rows
-      plan[3 * (nseg + 1) + 2] = (n_wide > 0 && 2 * n_wide >= n_chunks) ? 1 : 0;
+      plan[3 * (nseg + 1) + 2] = wide_gu ? 1 : 0;
+      plan[3 * (nseg + 1) + 3] = wide_dn ? 1 : 0;
     }
     return;
   }
   // ---- gather ----
   const int lane = threadIdx.x & 31;
+  constexpr int kBatch = 8;  // 16-byte loads in flight per lane before their stores
+  const int nv = H / 8;
+  if (inv_pos != nullptr) {
+    const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= T) return;
+    // lane j < k holds the destination of assignment t*k+j (checked against
+    // perm_src: only a position the dispatch gave this assignment is written)
+    int32_t myp = -1;
+    if (lane < k) {
+      const int64_t a = t * k + lane;
+      const int32_t p = inv_pos[a];
+      if (p >= 0 && p < Na && perm_src[p] == a) myp = p;
+    }
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + t * H);
+    for (int v0 = lane; v0 < nv; v0 += 32 * kBatch) {
+      uint4 r[kBatch];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i)
+        if (v0 + 32 * i < nv) r[i] = src[v0 + 32 * i];
+      for (int j = 0; j <= k; ++j) {
+        int64_t row;
+        if (j < k) {
+          const int32_t p = __shfl_sync(0xffffffffu, myp, j < 32 ? j : 0);
+          if (p < 0) continue;
+          row = p;
+        } else {
+          if (!shared) break;
+          row = Na + t;
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(x_perm + row * H);
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i)
+          if (v0 + 32 * i < nv) dst[v0 + 32 * i] = r[i];
+      }
+    }
+    return;
+  }
   const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (row >= R) return;
   int64_t src = -1;
@@ -256,14 +321,11 @@ __global__ void __launch_bounds__(256)
     src = row - Na;
   }
   uint4 *dst = reinterpret_cast<uint4 *>(x_perm + row * H);
-  const int nv = H / 8;
   if (src < 0) {
     for (int v = lane; v < nv; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
     return;
   }
   const uint4 *s = reinterpret_cast<const uint4 *>(x + src * H);
-  // eight 16-byte loads in flight per lane before their stores
-  constexpr int kBatch = 8;
   for (int v0 = lane; v0 < nv; v0 += 32 * kBatch) {
     uint4 r[kBatch];
 #pragma unroll
@@ -367,13 +429,14 @@ cudaError_t launch_dispatch(const int32_t *ids, const float *topk_w, int T, int 
 }
 
 cudaError_t launch_gather_plan(const __nv_bfloat16 *x, const int32_t *perm_src,
-                               const int32_t *offsets, int T, int k, int E, int H, int I,
-                               int shared, __nv_bfloat16 *x_perm, int32_t *plan, uint32_t *status,
-                               cudaStream_t s) {
-  const int64_t R = (int64_t)T * k + (shared ? T : 0);
-  const int blocks = (int)((R + 7) / 8) + 1;
-  return launch_pdl(gather_plan_kernel, dim3(blocks), dim3(256), 0, s, x, perm_src, offsets, T, k,
-                    E, H, I, shared, x_perm, plan, num_sms(), status);
+                               const int32_t *inv_pos, const int32_t *offsets, int T, int k, int E,
+                               int H, int I, int shared, __nv_bfloat16 *x_perm, int32_t *plan,
+                               uint32_t *status, cudaStream_t s) {
+  // eight warps per block: one per token (with inv_pos) or per x_perm row
+  const int64_t units = inv_pos != nullptr ? (int64_t)T : (int64_t)T * k + (shared ? T : 0);
+  const int blocks = (int)((units + 7) / 8) + 1;
+  return launch_pdl(gather_plan_kernel, dim3(blocks), dim3(256), 0, s, x, perm_src, inv_pos,
+                    offsets, T, k, E, H, I, shared, x_perm, plan, num_sms(), status);
 }
 
 }  // namespace moe

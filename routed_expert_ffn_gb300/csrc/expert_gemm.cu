@@ -111,18 +111,16 @@ struct TokenMaps {
 
 template <bool kGateUp>
 struct Cfg {
-  static constexpr int NA = kGateUp ? 2 : 1;                     // weight blocks per tile
-  static constexpr int TILE_ROWS = kGateUp ? kTileRowsGateUp : kTileRowsDown;
-  static constexpr uint32_t STAGE_A = NA * kStageKB * kChunkBytes;  // weights of a stage
-  static constexpr uint32_t STAGE_HALF = kStageKB * kChunkBytes;    // 128 token rows of a stage
-  static constexpr uint32_t SOUT_BYTES = 16 * kBM * 2;           // one 16-token slice
+  static constexpr uint32_t STAGE_UNIT = kStageKB * kChunkBytes;  // 128 rows of a stage
+  static constexpr uint32_t SOUT_BYTES = 16 * kBM * 2;            // one 16-token slice
+  // gate/up, wide layout: up-row values handed to the gate rows' threads
+  static constexpr uint32_t SUP_BYTES = kGateUp ? 16 * kGateUpColsWide * 4 : 0;
   static constexpr uint32_t BAR_BYTES = (2 * kMaxStages + 5) * 8 + 16;
   static constexpr size_t smem_bytes(int nseg) {
-    return 1024 + (size_t)kRingBytes + 2 * SOUT_BYTES + (size_t)TILE_ROWS * 4 + BAR_BYTES +
-           (size_t)2 * (nseg + 1) * 4;
+    return 1024 + (size_t)kRingBytes + 2 * SOUT_BYTES + 2 * SUP_BYTES +
+           (size_t)kTileRowsDown * 4 + BAR_BYTES + (size_t)2 * (nseg + 1) * 4;
   }
   static_assert(smem_bytes(kMaxE + 1) <= 232448, "shared memory per CTA");
-  static_assert(NA * (TILE_ROWS > 128 ? 256 : 128) <= (int)kAccCols, "accumulator columns");
 };
 
 struct Tile {
@@ -147,9 +145,8 @@ __device__ __forceinline__ bool epi_all(bool p) {
   return r != 0;
 }
 
-template <int kTileRows>
-__device__ __forceinline__ Tile decode_tile(int tile, const int32_t *seg_row, const int32_t *pref,
-                                            int nseg) {
+__device__ __forceinline__ Tile decode_tile(int tile, int kTileRows, const int32_t *seg_row,
+                                            const int32_t *pref, int nseg) {
   int lo = 0, hi = nseg;  // pref[lo] <= tile < pref[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -184,13 +181,14 @@ template <bool kGateUp>
 __global__ void __launch_bounds__(kThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,     // routed weights (5D)
                        const __grid_constant__ CUtensorMap tm_a_sh,  // shared-expert weights (5D)
+                       const __grid_constant__ CUtensorMap tm_aw,    // gate/up, wide: 64-row box
+                       const __grid_constant__ CUtensorMap tm_aw_sh,
                        const __grid_constant__ TokenMaps tm_b,       // activations [R, K] (3D)
                        const int32_t *__restrict__ plan, int nseg, int E, int K, int out_cols,
                        int64_t Na, const float *__restrict__ w_perm, void *__restrict__ out_,
                        float *__restrict__ split_part, uint32_t *__restrict__ split_cnt,
                        uint32_t *__restrict__ status) {
   using C = Cfg<kGateUp>;
-  constexpr int kTR = C::TILE_ROWS;
   // gate/up writes h in bf16 (the next GEMM's operand); down writes the
   // gate-weighted rows in fp16: 11 significant bits (8x finer than bf16) at
   // the same bandwidth; magnitudes past the fp16 range are clamped and
@@ -202,8 +200,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                               ~static_cast<uintptr_t>(1023));
   uint8_t *ring = smem;  // [stages][weights | token rows]
   uint16_t *sOut = reinterpret_cast<uint16_t *>(ring + kRingBytes);  // [2][16][kBM]
-  float *sW = reinterpret_cast<float *>(sOut + 2 * 16 * kBM);         // [kTR] (down)
-  uint64_t *full = reinterpret_cast<uint64_t *>(sW + kTR);            // [kMaxStages]
+  float *sUp = reinterpret_cast<float *>(sOut + 2 * 16 * kBM);        // [2][16][64] (gate/up)
+  float *sW = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(sUp) + 2 * C::SUP_BYTES);
+  uint64_t *full = reinterpret_cast<uint64_t *>(sW + kTileRowsDown);  // [kMaxStages]
   uint64_t *empty = full + kMaxStages;
   uint64_t *tfull = empty + kMaxStages;
   uint64_t *tempty = tfull + 2;
@@ -236,6 +235,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 4 && lane == 0) {
     tma_prefetch_desc(&tm_a);
     tma_prefetch_desc(&tm_a_sh);
+    if (kGateUp) {
+      tma_prefetch_desc(&tm_aw);
+      tma_prefetch_desc(&tm_aw_sh);
+    }
     for (int i = 0; i < 16; ++i) tma_prefetch_desc(&tm_b.m[i]);
   }
   // everything above is independent of earlier kernels' outputs
@@ -247,15 +250,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     pref[i] = g_pref[i];
   }
   if (threadIdx.x == 0) *s_kbs = plan[3 * (nseg + 1) + (kGateUp ? 0 : 1)];
-  // Stage layout.  Gate/up: 2 stages of [2 K blocks][gate | up 128 rows] +
-  // [2][<= 128 token rows].  Down (chosen by the tile plan): 2 stages of
-  // [2][128 rows] + [2][<= 256 token rows], one per K step of a tile, or 3
-  // stages of [2][128 rows] + [2][<= 128 token rows], one per K step and
-  // 128-row half of a tile (the weights are then loaded once per half; the
-  // second load hits L2).
-  const bool wide = !kGateUp && plan[3 * (nseg + 1) + 2] != 0;
-  const uint32_t stage_bytes = C::STAGE_A + (wide ? 2 : 1) * C::STAGE_HALF;
+  // Stage layout of this launch (chosen by the tile plan).  Each stage holds
+  // kStageKB K blocks of weights [K blocks][P][rows][64] and of token rows
+  // [K blocks][rows][64]:
+  //  - narrow: gate/up 128 gate + 128 up rows with <= 128 token rows; down
+  //    128 rows with <= 128 token rows, a wider down tile then running one
+  //    stage per 128-row half (its weights loaded once per half; the second
+  //    load hits L2);
+  //  - wide: gate/up 64 gate + 64 up rows, down 128 rows, with <= 256 token
+  //    rows in one stage and one MMA per K16 step.
+  const bool wide = plan[3 * (nseg + 1) + (kGateUp ? 2 : 3)] != 0;
+  const int tile_rows = (kGateUp && !wide) ? kTileRowsGateUp : kTileRowsDown;
+  const int out_w = (kGateUp && wide) ? kGateUpColsWide : kBM;  // output columns per tile
+  const uint32_t chunk_a = (kGateUp && !wide) ? 2 * kChunkBytes : kChunkBytes;  // per K block
+  const uint32_t stage_a = kStageKB * chunk_a;
+  const uint32_t stage_bytes = stage_a + (wide ? 2 : 1) * C::STAGE_UNIT;
   const uint32_t nst = kRingBytes / stage_bytes;
+  const CUtensorMap *ma_r = (kGateUp && wide) ? &tm_aw : &tm_a;
+  const CUtensorMap *ma_s = (kGateUp && wide) ? &tm_aw_sh : &tm_a_sh;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -270,19 +282,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 4) {
     // ------------------------------------------------------ TMA producer --
-    // A stage holds two K blocks: the weight tile(s) [2][NA x 128 x 64] in one
-    // copy and the token rows [2][h x 64] of one 128-row half (or of both
-    // halves in the wide layout) in one copy per half, h = rows rounded up
-    // to 16.
+    // Per stage: the weight rows of the tile in one copy and its token rows
+    // [K blocks][h][64] in one copy, h = rows rounded up to 16 (a 128-row
+    // half of a wider down tile in the narrow layout).
     if (lane == 0) {
       uint32_t st = 0, ph = 0, issued = 0;  // stage, parity of its use, stages issued
       bool ok = true;
       for (int pc = blockIdx.x; ok && pc < total_pieces; pc += gridDim.x) {
         const int tile = pc / S, z = pc - tile * S;
-        const Tile t = decode_tile<kTR>(tile, seg_row, pref, nseg);
+        const Tile t = decode_tile(tile, tile_rows, seg_row, pref, nseg);
         const int kb0 = z * kbs, kb1 = min(nkb, kb0 + kbs);
         const bool sh = (t.seg >= E);
-        const CUtensorMap *ma = sh ? &tm_a_sh : &tm_a;
+        const CUtensorMap *ma = sh ? ma_s : ma_r;
         const int ecoord = sh ? 0 : t.seg;
         const int h0 = min(128, (t.nrows + 15) & ~15);        // rows of half 0, padded
         const int h1 = max(0, ((t.nrows + 15) & ~15) - 128);  // rows of half 1, padded
@@ -297,12 +308,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // token rows of this stage: one 128-row unit, or (nu == 1) the
             // whole tile, up to 256 rows in the wide layout
             const int hb = (nu == 2) ? (u == 0 ? h0 : h1) : h0 + h1;
-            mbar_arrive_expect_tx(&full[st], C::STAGE_A + (uint32_t)hb * (kStageKB * kBK * 2));
-            // [K blocks][P][128 rows][64]: gate/up P = 2 (gate, then the
-            // same up rows), down P = 1
-            tma_load_5d(dst, ma, &full[st], 0, t.j * kBM, 0, kb, ecoord);
-            tma_load_3d(dst + C::STAGE_A, &tm_b.m[(hb >> 4) - 1], &full[st], 0, t.row0 + u * 128,
-                        kb);
+            mbar_arrive_expect_tx(&full[st], stage_a + (uint32_t)hb * (kStageKB * kBK * 2));
+            // [K blocks][P][rows][64]: gate/up P = 2 (gate rows, then the same
+            // up rows), down P = 1
+            tma_load_5d(dst, ma, &full[st], 0, t.j * out_w, 0, kb, ecoord);
+            tma_load_3d(dst + stage_a, &tm_b.m[(hb >> 4) - 1], &full[st], 0, t.row0 + u * 128, kb);
             ++issued;
             if (++st == nst) {
               st = 0;
@@ -331,14 +341,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int pc = blockIdx.x; ok && pc < total_pieces; pc += gridDim.x, ++tl) {
         const int tile = pc / S, z = pc - tile * S;
-        const Tile t = decode_tile<kTR>(tile, seg_row, pref, nseg);
+        const Tile t = decode_tile(tile, tile_rows, seg_row, pref, nseg);
         const int kb0 = z * kbs, kb1 = min(nkb, kb0 + kbs);
         const int h0 = min(128, (t.nrows + 15) & ~15);
         const int h1 = max(0, ((t.nrows + 15) & ~15) - 128);
         const int nu = (!wide && h1 > 0) ? 2 : 1;
-        // down: token column n -> accumulator column n (a wide tile in the
-        // narrow layout as two 128-row units); gate/up: gate rows -> columns
-        // [0, 128), up rows -> [128, 256)
+        // token column n -> accumulator column n (a wide down tile in the
+        // narrow layout as two 128-row units); gate/up, narrow: gate rows ->
+        // columns [0, 128), up rows -> [128, 256) of the same token; gate/up,
+        // wide: one accumulator, gate rows in lanes [0, 64), up in [64, 128)
         const uint32_t idesc0 = idesc_bf16_f32(kBM, nu == 2 ? h0 : h0 + h1);
         const uint32_t idesc1 = idesc_bf16_f32(kBM, h1 > 0 ? h1 : 16);
         const uint32_t buf = tl & 1u, use = tl >> 1;
@@ -354,13 +365,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const uint64_t adesc = desc0 + st * dstage;
-            const uint64_t bdesc = adesc + (C::STAGE_A >> 4);
+            const uint64_t bdesc = adesc + (stage_a >> 4);
             const int hb = (nu == 2) ? (u == 0 ? h0 : h1) : h0 + h1;
             for (int c = 0; c < nc; ++c) {
               const uint32_t acc = (kb != kb0 || c != 0) ? 1u : 0u;
-              const uint64_t ac = adesc + c * (C::NA * kChunkBytes >> 4);
+              const uint64_t ac = adesc + c * (chunk_a >> 4);
               const uint64_t bc = bdesc + c * ((uint32_t)hb * (kBK * 2) >> 4);
-              if (kGateUp) {
+              if (kGateUp && !wide) {
                 umma_kblock(d0, ac, bc, idesc0, acc);                              // gate
                 umma_kblock(d0 + 128, ac + (kChunkBytes >> 4), bc, idesc0, acc);  // up
               } else {
@@ -419,17 +430,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ++slice;
     };
-    constexpr int kSlot = C::NA * kBM * kSplitMaxRows;  // floats of one piece's partial
+    // gate/up, wide layout: the thread holds a gate row (r < 64) or the up row
+    // r - 64 of the same h column; the up values pass through smem.
+    auto emit16_wide = [&](const Tile &t, int n0, const float(&v)[16]) {
+      constexpr int W = kGateUpColsWide;
+      uint16_t *so = sOut + (slice & 1u) * (16 * kBM);  // [16][W]
+      float *su = sUp + (slice & 1u) * (16 * W);
+      if (r >= W) {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) su[q * W + (r - W)] = v[q];
+      }
+      epi_sync();
+      if (r < W) {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const float g = v[q], u = su[q * W + r];
+          so[q * W + r] = __bfloat16_as_ushort(__float2bfloat16_rn(g / (1.0f + __expf(-g)) * u));
+        }
+      }
+      epi_sync();
+      // 16 token rows x 64 columns x 2 bytes = 128 chunks of 16 bytes
+      const int q = r / (W / 8), ch = r % (W / 8);
+      const int n = n0 + q, col = t.j * W + ch * 8;
+      if (n < t.nrows && col < out_cols)
+        *reinterpret_cast<uint4 *>(out + ((int64_t)t.row0 + n) * out_cols + col) =
+            *reinterpret_cast<const uint4 *>(so + q * W + ch * 8);
+      ++slice;
+    };
+    // floats of one split-K piece's partial (a split launch is never wide:
+    // the plan splits only when every tile has <= kSplitMaxRows rows)
+    constexpr int kSlot = (kGateUp ? 2 : 1) * kBM * kSplitMaxRows;
     for (int pc = blockIdx.x; pc < total_pieces; pc += gridDim.x, ++tl) {
       const int tile = pc / S, z = pc - tile * S;
-      const Tile t = decode_tile<kTR>(tile, seg_row, pref, nseg);
+      const Tile t = decode_tile(tile, tile_rows, seg_row, pref, nseg);
       const uint32_t buf = tl & 1u, use = tl >> 1;
       const bool waited = mbar_wait(&tfull[buf], use & 1u, abort_flag, status, kCode);
       // one decision for all 128 epilogue threads: they share named barriers
       if (!epi_all(waited && !*abort_flag)) break;
       tc_fence_after();
       if (!kGateUp) {
-        for (int n = r; n < kTR; n += 128) {
+        for (int n = r; n < kTileRowsDown; n += 128) {
           const int64_t row = (int64_t)t.row0 + n;
           sW[n] = (n < t.nrows && w_perm != nullptr && row < Na) ? w_perm[row] : 1.0f;
         }
@@ -437,6 +477,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint32_t tb = tmem_base + ((uint32_t)(warp * 32) << 16) + buf * kAccCols;
       const int N = (t.nrows + 15) & ~15;
+      if (kGateUp && wide) {
+        for (int n0 = 0; n0 < N; n0 += 16) {
+          uint32_t v0[16];
+          tmem_ld16(tb + n0, v0);
+          tmem_ld_wait();
+          float v[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) v[q] = __uint_as_float(v0[q]);
+          emit16_wide(t, n0, v);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[buf]);
+        continue;
+      }
       if (S == 1) {
         for (int n0 = 0; n0 < N; n0 += 16) {
           uint32_t v0[16], v1[16];
@@ -560,14 +615,26 @@ cudaError_t launch_gemm(const moe_layer_desc_t &d, const void *w, const void *w_
   const int K = kGateUp ? d.H : d.I;
   const int rows = kGateUp ? d.I : d.H;  // weight rows per half = output columns
   const int P = kGateUp ? 2 : 1;
-  const int box_rows = kBM;  // rows of each half of W13 / of W2 per tile
-  CUtensorMap ma, msh;
+  // rows of each half of W13 / of W2 per tile; gate/up in the wide layout
+  // takes kGateUpColsWide rows of each half
+  CUtensorMap ma, msh, maw, mawsh;
   TokenMaps mb;
-  if (!weight_map(&ma, w, K, rows, P, d.E, box_rows)) return cudaErrorInvalidValue;
+  if (!weight_map(&ma, w, K, rows, P, d.E, kBM)) return cudaErrorInvalidValue;
   if (shared) {
-    if (!weight_map(&msh, w_sh, K, rows, P, 1, box_rows)) return cudaErrorInvalidValue;
+    if (!weight_map(&msh, w_sh, K, rows, P, 1, kBM)) return cudaErrorInvalidValue;
   } else {
     msh = ma;
+  }
+  if (kGateUp) {
+    if (!weight_map(&maw, w, K, rows, P, d.E, kGateUpColsWide)) return cudaErrorInvalidValue;
+    if (shared) {
+      if (!weight_map(&mawsh, w_sh, K, rows, P, 1, kGateUpColsWide)) return cudaErrorInvalidValue;
+    } else {
+      mawsh = maw;
+    }
+  } else {
+    maw = ma;
+    mawsh = msh;
   }
   for (int i = 0; i < 16; ++i)
     if (!act_map(&mb.m[i], act, K, R, 16 * (i + 1))) return cudaErrorInvalidValue;
@@ -587,8 +654,8 @@ cudaError_t launch_gemm(const moe_layer_desc_t &d, const void *w, const void *w_
   // one CTA per SM: the device-side plan decides the tiles (and split-K
   // pieces); CTAs without work leave at once
   const int grid = num_sms();
-  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, ma, msh, mb, plan, nseg, d.E, K, rows,
-                    Na, w_perm, out, split_part, split_cnt, status);
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, ma, msh, maw, mawsh, mb, plan, nseg,
+                    d.E, K, rows, Na, w_perm, out, split_part, split_cnt, status);
 }
 
 }  // namespace

@@ -46,17 +46,18 @@ inline int64_t dispatch_chunk(int64_t Na) {
   return c < kDispatchThreads ? kDispatchThreads : c;
 }
 
-// Expert GEMMs (tcgen05), stepped through K in blocks of kBK, two blocks per
-// pipeline stage.  Gate/up tile: 128 gate rows and the same 128 up rows of
-// W13 (128 columns of h) by up to kTileRowsGateUp token rows; 2 stages of
-// 96 KB.  Down tile: 128 rows of W2 (128 output columns) by up to
-// kTileRowsDown token rows; 3 stages of weights + 128 token rows (a wider
-// tile runs one stage per 128-row half), or -- when most tiles are wider --
-// 2 stages of weights + 256 token rows.
+// Expert GEMMs (tcgen05), stepped through K in blocks of kBK, kStageKB blocks
+// per pipeline stage, in one of two layouts chosen per launch by the tile
+// plan.  Narrow (most token chunks <= 128 rows): gate/up tile = 128 gate rows
+// and the same 128 up rows of W13 by <= kTileRowsGateUp token rows; down tile
+// = 128 rows of W2 by <= kTileRowsDown token rows, run one 128-row half per
+// stage.  Wide: gate/up tile = kGateUpColsWide gate + the same up rows by
+// <= kTileRowsDown token rows; down tile as above in one stage.
 constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr int kTileRowsGateUp = 128;
 constexpr int kTileRowsDown = 256;
+constexpr int kGateUpColsWide = 64;
 #ifndef MOE_STAGE_KB
 #define MOE_STAGE_KB 2
 #endif
@@ -100,7 +101,7 @@ constexpr int kRouteSizingSms = 256;
 //   [nseg+1, 2nseg+1]         gate/up tile prefix (nseg+1)
 //   [2nseg+2, 3nseg+2]        down tile prefix (nseg+1)
 //   [3nseg+3], [3nseg+4]      split-K factor S of the gate/up and down GEMM
-inline int plan_ints(int nseg) { return 3 * (nseg + 1) + 3; }
+inline int plan_ints(int nseg) { return 3 * (nseg + 1) + 4; }
 
 // Split-K for small batches: when every tile has at most kSplitMaxRows token
 // rows and there are too few tiles to occupy the GPU, each tile's K range is
@@ -129,10 +130,13 @@ cudaError_t launch_dispatch(const int32_t *ids, const float *topk_w, int T, int 
                             int32_t *blk_counts, int32_t *blk_base, int32_t *counts,
                             int32_t *offsets, int32_t *perm_src, int32_t *inv_pos, float *w_perm,
                             uint32_t *status, cudaStream_t s);
+// inv_pos may be null: then one warp per x_perm row (the standalone FFN call,
+// and layer forwards whose x is at most kGatherByTokenBytes).
+constexpr int64_t kGatherByTokenBytes = 8ll << 20;
 cudaError_t launch_gather_plan(const __nv_bfloat16 *x, const int32_t *perm_src,
-                               const int32_t *offsets, int T, int k, int E, int H, int I,
-                               int shared, __nv_bfloat16 *x_perm, int32_t *plan, uint32_t *status,
-                               cudaStream_t s);
+                               const int32_t *inv_pos, const int32_t *offsets, int T, int k, int E,
+                               int H, int I, int shared, __nv_bfloat16 *x_perm, int32_t *plan,
+                               uint32_t *status, cudaStream_t s);
 // split_part: kMaxSplitTiles x 2 x kBM x kSplitMaxRows fp32; split_cnt: the
 // GEMM's kMaxSplitTiles arrival counters (in the workspace status block).
 cudaError_t launch_expert_gateup(const moe_layer_desc_t &d, const void *w13, const void *w13_shared,

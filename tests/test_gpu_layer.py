@@ -120,3 +120,67 @@ def test_output_independent_of_batch_neighbours():
                                 big.w13, big.w2)
         y1 = LayerRun(one).forward()
         assert_output_close(bf16_np(y1[0]), bf16_np(y_big[t]), "batch independence")
+
+
+def _split_kbs(total, nkb, num_sms, max_m):
+    """K blocks per split-K piece, by the rule the tile plan documents: split only
+    when every tile has <= 32 token rows and the busiest SM's K blocks (plus a
+    fixed cost of 8 K blocks per piece, plus the pieces) drop by at least a fifth;
+    pieces are even numbers of K blocks."""
+    if total <= 0 or max_m > 32 or total > 512:
+        return nkb
+    base = -(-total // num_sms) * nkb
+    best, best_cost = nkb, base
+    for S in range(2, 17):
+        kbs = 2 * (-(-nkb // (2 * S)))
+        if kbs >= nkb:
+            continue
+        pieces = -(-nkb // kbs)
+        if total * pieces > 1024:
+            break
+        cost = -(-(total * pieces) // num_sms) * (kbs + 8) + pieces
+        if cost < best_cost:
+            best, best_cost = kbs, cost
+    return best if best_cost * 5 <= base * 4 else nkb
+
+
+@pytest.mark.parametrize("name,T", [("qwen3", 1), ("qwen3", 1024), ("mixtral", 4096),
+                                    ("qwen3_tp8", 8)])
+def test_tile_plan(name, T):
+    """The device-side tile plan (segments, tile prefixes, split-K pieces, layouts)
+    is an integer function of the dispatch counts: recomputed here from the rules
+    and compared exactly."""
+    inputs = layer_inputs(name, T)
+    cfg = inputs.cfg
+    run = LayerRun(inputs)
+    run.forward()
+    counts = run.metadata()["counts"].tolist()
+    ms = counts + ([T] if cfg.shared else [])
+    nseg = len(ms)
+    plan = run.view("plan", torch.int32, (3 * (nseg + 1) + 4,)).cpu().numpy().tolist()
+    cdiv = lambda a, b: -(-a // b)
+    Na = T * cfg.k
+    seg_row = np.concatenate([[0], np.cumsum(counts)]).tolist()[:cfg.E]
+    if cfg.shared:
+        seg_row.append(Na)
+    seg_row.append(Na + (T if cfg.shared else 0))
+    live = [m for m in ms if m > 0]
+    n_chunks = sum(cdiv(m, 256) for m in live)
+    n_wide = sum(m // 256 + (1 if m % 256 > 128 else 0) for m in live)
+    st_narrow = sum(cdiv(m, 128) for m in live)
+    st_wide = sum(2 * cdiv(m, 256) for m in live)
+    wide_dn = n_wide > 0 and 2 * n_wide >= n_chunks
+    wide_gu = st_narrow > 0 and 8 * st_wide <= 9 * st_narrow
+    tr_gu, nj_gu = (256, cdiv(cfg.I, 64)) if wide_gu else (128, cdiv(cfg.I, 128))
+    gu = [cdiv(m, tr_gu) * nj_gu for m in ms]
+    dn = [cdiv(m, 256) * cdiv(cfg.H, 128) for m in ms]
+    pref = lambda v: np.concatenate([[0], np.cumsum(v)]).astype(int).tolist()
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    want = (seg_row + pref(gu) + pref(dn) +
+            [_split_kbs(sum(gu), cfg.H // 64, nsm, max(ms)),
+             _split_kbs(sum(dn), cfg.I // 64, nsm, max(ms)), int(wide_gu), int(wide_dn)])
+    assert plan == want
+    if name == "mixtral":
+        assert wide_gu and wide_dn   # uniform prefill: both GEMMs run wide
+    if (name, T) == ("qwen3", 1024):
+        assert not wide_gu and not wide_dn
