@@ -24,7 +24,7 @@ constexpr int64_t kMaxAssign = 1 << 24;
 
 // Router: at most this many K splits (summed by the gating kernel); batches of
 // up to kSmallRouteT tokens take the one-launch small-batch router.
-constexpr int kRouteMaxSplits = 16;
+constexpr int kRouteMaxSplits = 32;
 constexpr int kSmallRouteT = 32;
 
 // The workspace starts with a status block zeroed by moe_workspace_init:

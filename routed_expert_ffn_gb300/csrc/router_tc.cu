@@ -6,8 +6,10 @@
 // (each subtraction is exact -- Sterbenz -- and the last residual has at most
 // 8 significant bits, so hi + mid + lo == w exactly).  A bf16 x bf16 product
 // has a 16-bit significand, so every product the tensor core forms is exact,
-// and the three partial logits are accumulated in fp32 in TMEM:
-//   s = (x.lo + x.mid) + x.hi
+// and two partial logits are accumulated in fp32 in TMEM, one of the hi
+// products and one of the mid and lo products (whose sum is 2^-8 of the hi
+// sum, so its rounding is negligible):
+//   s = (x.mid + x.lo) + x.hi
 // Summation is blocked: the tensor core accumulates one chunk of kChunkKB
 // K blocks (512 products per logit and term) in TMEM, and the epilogue adds
 // the chunks in fp32 registers.  A plain fp32 chain over H = 7168 terms with
@@ -15,7 +17,7 @@
 // error of the long accumulation (and the tensor core's accumulation bias)
 // to one chunk.
 //
-// Tile = 128 experts (MMA M) x up to 64 tokens (MMA N) x one K range of H;
+// Tile = 128 experts (MMA M) x up to 128 tokens (MMA N) x one K range of H;
 // the K ranges (splits) give the GPU enough CTAs at small T and are summed in
 // a fixed order by the gating kernel.  Warp roles as in the expert GEMMs: a
 // TMA producer warp, a single-thread MMA issuer, four epilogue warps; two
@@ -28,14 +30,14 @@ namespace moe {
 namespace {
 
 constexpr int kRThreads = 192;
-constexpr int kRBN = 64;                                   // tokens per tile
+constexpr int kRBN = 128;                                  // tokens per tile
 constexpr int kChunkKB = 8;                                // K blocks per TMEM accumulation
 constexpr uint32_t kRA = kBM * kBK * 2;                    // one 128 x 64 bf16 tile
 constexpr uint32_t kRB = kRBN * kBK * 2;
 constexpr uint32_t kRStage = 3 * kRA + kRB;                // hi, mid, lo + tokens
-constexpr int kRStages = 4;
-constexpr uint32_t kRAcc = 3 * kRBN;                       // hi, mid, lo accumulators
-constexpr uint32_t kRTmemCols = 512;                       // 2 buffers x 3 x 64 columns
+constexpr int kRStages = 3;
+constexpr uint32_t kRAcc = 2 * kRBN;                       // hi and (mid + lo) accumulators
+constexpr uint32_t kRTmemCols = 512;                       // 2 buffers x 2 x 128 columns
 constexpr size_t kRSmem = 1024 + (size_t)kRStages * kRStage + 256;
 
 __global__ void __launch_bounds__(256)
@@ -68,7 +70,8 @@ __global__ void __launch_bounds__(256)
 
 __global__ void __launch_bounds__(kRThreads, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tm_w,   // [3][E][H] bf16 (3D)
-                     const __grid_constant__ CUtensorMap tm_x,   // [T][H] bf16 (2D)
+                     const __grid_constant__ CUtensorMap tm_x,   // [T][H] bf16, 16-row box
+                     const __grid_constant__ CUtensorMap tm_x128,  // the same, 128-row box
                      int T, int E, int kb_per_split, int nkb, float *__restrict__ partial,
                      uint32_t *__restrict__ status) {
   extern __shared__ uint8_t smem_raw[];
@@ -111,6 +114,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
   if (warp == 4 && lane == 0) {
     tma_prefetch_desc(&tm_w);
     tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_x128);
   }
   pdl_wait();
   pdl_launch_dependents();
@@ -133,8 +137,12 @@ __global__ void __launch_bounds__(kRThreads, 1)
         uint8_t *a0 = sA + (size_t)st * 3 * kRA;
         for (int p = 0; p < 3; ++p) tma_load_3d(a0 + p * kRA, &tm_w, &full[st], kb * kBK, e0, p);
         uint8_t *b0 = sB + (size_t)st * kRB;
-        for (int q = 0; q < nb16; ++q)
-          tma_load_2d(b0 + q * 16 * kBK * 2, &tm_x, &full[st], kb * kBK, t0 + q * 16);
+        if (nrows == kRBN) {
+          tma_load_2d(b0, &tm_x128, &full[st], kb * kBK, t0);
+        } else {
+          for (int q = 0; q < nb16; ++q)
+            tma_load_2d(b0 + q * 16 * kBK * 2, &tm_x, &full[st], kb * kBK, t0 + q * 16);
+        }
       }
       const uint32_t first = it > (uint32_t)kRStages ? it - kRStages : 0u;
       for (uint32_t i = first; i < it; ++i) mbar_wait_drain(&full[i % kRStages], (i / kRStages) & 1u);
@@ -166,13 +174,14 @@ __global__ void __launch_bounds__(kRThreads, 1)
         const uint32_t a_addr = smem_u32(sA + (size_t)st * 3 * kRA);
         const uint64_t bdesc = sdesc_k_sw128(smem_u32(sB + (size_t)st * kRB));
         const uint32_t d0 = tmem_base + buf * kRAcc;
+        const uint64_t a_hi = sdesc_k_sw128(a_addr), a_mid = sdesc_k_sw128(a_addr + kRA),
+                       a_lo = sdesc_k_sw128(a_addr + 2 * kRA);
 #pragma unroll
         for (int ks = 0; ks < kBK / 16; ++ks) {
           const uint32_t acc = (!chunk_first || ks != 0) ? 1u : 0u;
-#pragma unroll
-          for (int p = 0; p < 3; ++p)
-            umma_bf16(d0 + p * kRBN, sdesc_k_sw128(a_addr + p * kRA) + 2 * ks, bdesc + 2 * ks,
-                      idesc, acc);
+          umma_bf16(d0, a_hi + 2 * ks, bdesc + 2 * ks, idesc, acc);
+          umma_bf16(d0 + kRBN, a_mid + 2 * ks, bdesc + 2 * ks, idesc, acc);
+          umma_bf16(d0 + kRBN, a_lo + 2 * ks, bdesc + 2 * ks, idesc, 1u);
         }
         umma_commit(&empty[st]);
         if (chunk_last) umma_commit(&tfull[buf]);
@@ -200,15 +209,12 @@ __global__ void __launch_bounds__(kRThreads, 1)
 #pragma unroll
       for (int n0 = 0; n0 < kRBN; n0 += 16) {
         if (n0 < N) {
-          uint32_t hi[16], mid[16], lo[16];
+          uint32_t hi[16], ml[16];
           tmem_ld16(tb + n0, hi);
-          tmem_ld16(tb + kRBN + n0, mid);
-          tmem_ld16(tb + 2 * kRBN + n0, lo);
+          tmem_ld16(tb + kRBN + n0, ml);
           tmem_ld_wait();
 #pragma unroll
-          for (int q = 0; q < 16; ++q)
-            acc[n0 + q] += (__uint_as_float(lo[q]) + __uint_as_float(mid[q])) +
-                           __uint_as_float(hi[q]);
+          for (int q = 0; q < 16; ++q) acc[n0 + q] += __uint_as_float(ml[q]) + __uint_as_float(hi[q]);
         }
       }
       tc_fence_before();
@@ -236,7 +242,7 @@ int route_splits(int T, int E, int H, int nsm) {
   const int nkb = H / kBK;
   // at most one CTA per SM (each holds all of TMEM): one wave
   int want = nsm / tiles;
-  int cap = nkb / 4;  // at least 4 K blocks per split
+  int cap = nkb / 2;  // at least 2 K blocks per split
   if (cap > kRouteMaxSplits) cap = kRouteMaxSplits;
   if (cap < 1) cap = 1;
   if (want > cap) want = cap;
@@ -262,11 +268,14 @@ cudaError_t launch_router_logits(const __nv_bfloat16 *x, const float *w_router, 
     const cuuint32_t box[3] = {(cuuint32_t)kBK, (cuuint32_t)kBM, 1};
     if (!encode_bf16_map(&mw, w_split, 3, dims, strides, box)) return cudaErrorInvalidValue;
   }
+  CUtensorMap mx128;
   {
     const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)T};
     const cuuint64_t strides[1] = {(cuuint64_t)H * 2};
     const cuuint32_t box[2] = {(cuuint32_t)kBK, 16};
     if (!encode_bf16_map(&mx, x, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    const cuuint32_t box128[2] = {(cuuint32_t)kBK, (cuuint32_t)kRBN};
+    if (!encode_bf16_map(&mx128, x, 2, dims, strides, box128)) return cudaErrorInvalidValue;
   }
   static bool configured[64] = {};
   int dev = 0;
@@ -281,7 +290,7 @@ cudaError_t launch_router_logits(const __nv_bfloat16 *x, const float *w_router, 
   const int nkb = H / kBK;
   const int per = (nkb + splits - 1) / splits;
   dim3 grid((E + kBM - 1) / kBM, (T + kRBN - 1) / kRBN, splits);
-  return launch_pdl(router_tc_kernel, grid, dim3(kRThreads), kRSmem, s, mw, mx, T, E, per, nkb,
+  return launch_pdl(router_tc_kernel, grid, dim3(kRThreads), kRSmem, s, mw, mx, mx128, T, E, per, nkb,
                     partial, status);
 }
 
