@@ -248,8 +248,8 @@ moe_status_t moe_build_dispatch(const moe_layer_desc_t *d, const int32_t *topk_i
   cudaError_t e = launch_dispatch(topk_ids, topk_w, d->T, d->k, d->E,
                                   at<int32_t>(workspace, L.blk_counts),
                                   at<int32_t>(workspace, L.blk_base), counts, offsets, perm_src,
-                                  inv_pos, w_perm, at<uint32_t>(workspace, L.status),
-                                  (cudaStream_t)stream);
+                                  inv_pos, w_perm, at<uint32_t>(workspace, L.status), nullptr,
+                                  d->H, d->I, d->has_shared_expert, (cudaStream_t)stream);
   return cuda_status(e);
 }
 
@@ -279,8 +279,8 @@ moe_status_t moe_grouped_swiglu_ffn(const moe_layer_desc_t *d, const void *x,
   cudaError_t e = launch_gather_plan(bf(x), perm_src, nullptr, offsets, d->T, d->k, d->E, d->H,
                                      d->I, d->has_shared_expert, x_perm, plan, status, s);
   if (e == cudaSuccess)
-    e = launch_expert_gateup(*d, w13, w13_shared, x_perm, plan, split_part, split_cnt, h, status,
-                             s);
+    e = launch_expert_gateup(*d, w13, w13_shared, x_perm, plan, 0, split_part, split_cnt, h,
+                             status, s);
   if (e == cudaSuccess)
     e = launch_expert_down(*d, w2, w2_shared, h, plan, w_perm, split_part,
                            split_cnt + kMaxSplitTiles, static_cast<__half *>(out_perm), status, s);
@@ -339,7 +339,8 @@ moe_status_t moe_layer_forward(const moe_layer_desc_t *d, const moe_layer_weight
   if (e == cudaSuccess)
     e = launch_dispatch(ids, tw, d->T, d->k, d->E, at<int32_t>(workspace, L.blk_counts),
                         at<int32_t>(workspace, L.blk_base), at<int32_t>(workspace, L.counts),
-                        offsets, perm_src, inv_pos, w_perm, status, s);
+                        offsets, perm_src, inv_pos, w_perm, status, plan, d->H, d->I,
+                        d->has_shared_expert, s);
   if (e == cudaSuccess) e = mark(2);
   if (e == cudaSuccess)
     // token-order gather (x read once) once x is too large to stay in L2
@@ -347,10 +348,10 @@ moe_status_t moe_layer_forward(const moe_layer_desc_t *d, const moe_layer_weight
     e = launch_gather_plan(bf(x), perm_src,
                            (int64_t)d->T * d->H * 2 > kGatherByTokenBytes ? inv_pos : nullptr,
                            offsets, d->T, d->k, d->E, d->H, d->I, d->has_shared_expert, x_perm,
-                           plan, status, s);
+                           nullptr, status, s);  // the dispatch wrote the plan
   if (e == cudaSuccess) e = mark(3);
   if (e == cudaSuccess)
-    e = launch_expert_gateup(*d, w->w13, w->w13_shared, x_perm, plan, split_part, split_cnt, h,
+    e = launch_expert_gateup(*d, w->w13, w->w13_shared, x_perm, plan, 1, split_part, split_cnt, h,
                              status, s);
   if (e == cudaSuccess) e = mark(4);
   if (e == cudaSuccess)

@@ -72,10 +72,14 @@ __device__ int block_exclusive_scan(int v, int *warp_tot, int *total) {
   return r;
 }
 
+__device__ void write_tile_plan(const int32_t *__restrict__ offsets, int T, int k, int E, int H,
+                                int I, int shared, int32_t *__restrict__ plan, int num_sms,
+                                uint32_t *__restrict__ status);
+
 __global__ void __launch_bounds__(kMaxE)
     dispatch_scan_kernel(const int32_t *__restrict__ blk_counts, int nblk, int E,
                          int32_t *__restrict__ blk_base, int32_t *__restrict__ counts,
-                         int32_t *__restrict__ offsets) {
+                         int32_t *__restrict__ offsets, PlanArgs pa) {
   pdl_wait();
   pdl_launch_dependents();
   __shared__ int warp_tot[32];
@@ -95,6 +99,10 @@ __global__ void __launch_bounds__(kMaxE)
     }
   }
   if (e == 0) offsets[E] = total;
+  if (pa.plan != nullptr) {
+    __syncthreads();
+    write_tile_plan(offsets, pa.T, pa.k, E, pa.H, pa.I, pa.shared, pa.plan, pa.num_sms, pa.status);
+  }
 }
 
 __global__ void __launch_bounds__(kDispatchThreads)
@@ -167,109 +175,121 @@ __device__ int choose_split(int total, int nkb, int num_sms, int max_m) {
   return (best_cost * 5 <= base * 4) ? best : nkb;
 }
 
+// The tile plan of the grouped GEMMs from the dispatch offsets (see the
+// workspace layout's `plan` field): segment row offsets, the gate/up and down
+// tile prefix sums, split-K pieces and pipeline layouts.  Called by every
+// thread of one block of 171..1024 threads (each thread owns up to three
+// consecutive segments; nseg <= 513).
+__device__ void write_tile_plan(const int32_t *__restrict__ offsets, int T, int k, int E, int H,
+                                int I, int shared, int32_t *__restrict__ plan, int num_sms,
+                                uint32_t *__restrict__ status) {
+  const int64_t Na = (int64_t)T * k;
+  const int64_t R = Na + (shared ? T : 0);
+  __shared__ int warp_tot[32];
+  __shared__ int tot_gu, tot_dn, bad, max_m, n_chunks, n_wide, st_narrow, st_wide;
+  const int nseg = E + (shared ? 1 : 0);
+  const int nj_dn = (H + kBM - 1) / kBM;
+  if (threadIdx.x == 0) {
+    bad = 0;
+    max_m = 0;
+    n_chunks = 0;
+    n_wide = 0;
+    st_narrow = 0;
+    st_wide = 0;
+  }
+  __syncthreads();
+  // validate the offsets (caller-provided in the standalone call)
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    if (offsets[e] < 0 || offsets[e + 1] < offsets[e] || offsets[e + 1] > Na) bad = 1;
+  if (threadIdx.x == 0 && offsets[0] != 0) bad = 1;
+  __syncthreads();
+  if (threadIdx.x == 0 && bad) atomicOr(status, kStatusBadOffsets);
+  int32_t *seg_row = plan, *pref_gu = plan + nseg + 1, *pref_dn = plan + 2 * (nseg + 1);
+  // each thread owns up to 3 consecutive segments (nseg <= 513 < 3*256)
+  constexpr int kPer = 3;
+  const int s0 = threadIdx.x * kPer;
+  int ms[kPer];
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const int s = s0 + q;
+    int m = 0;
+    if (!bad && s < nseg) m = (s < E) ? offsets[s + 1] - offsets[s] : T;
+    ms[q] = m;
+    if (m > 0) {
+      atomicMax(&max_m, m);
+      // 256-row token chunks; "wide" ones have more than 128 rows
+      atomicAdd(&n_chunks, (m + kTileRowsDown - 1) / kTileRowsDown);
+      atomicAdd(&n_wide, m / kTileRowsDown + (m % kTileRowsDown > 128 ? 1 : 0));
+      // gate/up pipeline stages per 128 weight rows and K step: narrow tiles
+      // (128 + 128 rows by <= 128 tokens) vs wide (64 + 64 rows by <= 256)
+      atomicAdd(&st_narrow, (m + kTileRowsGateUp - 1) / kTileRowsGateUp);
+      atomicAdd(&st_wide, 2 * ((m + kTileRowsDown - 1) / kTileRowsDown));
+    }
+    if (s < nseg) seg_row[s] = bad ? 0 : ((s < E) ? offsets[s] : (int)Na);
+  }
+  __syncthreads();
+  // Pipeline layouts.  Down: "wide" (stages of 256 token rows) when most
+  // 256-row chunks have more than 128 rows.  Gate/up: wide tiles (64 gate +
+  // 64 up rows by <= 256 token rows, one N <= 256 MMA per K16 step) when
+  // they need at most 9/8 the stages of narrow tiles (128 + 128 rows by
+  // <= 128 token rows, two MMAs per K16 step).  Measured: a wide stage costs
+  // about 0.9 of a narrow one (Mixtral T=4096, ratio 1.04: wide 7% faster;
+  // DeepSeek-V3 T=8192, ratio 1.29: wide 10% slower).
+  const bool wide_dn = n_wide > 0 && 2 * n_wide >= n_chunks;
+  const bool wide_gu = st_narrow > 0 && 8 * st_wide <= 9 * st_narrow;
+  const int tr_gu = wide_gu ? kTileRowsDown : kTileRowsGateUp;
+  const int nj_gu =
+      wide_gu ? (I + kGateUpColsWide - 1) / kGateUpColsWide : (I + kBM - 1) / kBM;
+  int gu[kPer], dn[kPer], sum_gu = 0, sum_dn = 0;
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    gu[q] = (ms[q] + tr_gu - 1) / tr_gu * nj_gu;
+    dn[q] = (ms[q] + kTileRowsDown - 1) / kTileRowsDown * nj_dn;
+    sum_gu += gu[q];
+    sum_dn += dn[q];
+  }
+  int run_gu = block_exclusive_scan(sum_gu, warp_tot, &tot_gu);
+  int run_dn = block_exclusive_scan(sum_dn, warp_tot, &tot_dn);
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const int s = s0 + q;
+    if (s < nseg) {
+      pref_gu[s] = run_gu;
+      pref_dn[s] = run_dn;
+    }
+    run_gu += gu[q];
+    run_dn += dn[q];
+  }
+  if (threadIdx.x == 0) {
+    seg_row[nseg] = bad ? 0 : (int)R;
+    pref_gu[nseg] = tot_gu;
+    pref_dn[nseg] = tot_dn;
+    plan[3 * (nseg + 1)] = choose_split(tot_gu, H / kBK, num_sms, max_m);
+    plan[3 * (nseg + 1) + 1] = choose_split(tot_dn, I / kBK, num_sms, max_m);
+    plan[3 * (nseg + 1) + 2] = wide_gu ? 1 : 0;
+    plan[3 * (nseg + 1) + 3] = wide_dn ? 1 : 0;
+  }
+}
+
 // Rows [0, Na): x_perm[p] = x[perm_src[p] / k]; rows [Na, Na+T) (shared
 // expert): x_perm[Na+t] = x[t].  16-byte vectors.  With inv_pos (the layer
 // forward) one warp per token reads its row of x once and writes it to the
 // token's k positions (and its shared-expert row), so x is read once even
 // when it does not fit in L2; without (the standalone FFN call) one warp per
 // x_perm row.  The last block instead writes the tile plan of the grouped
-// GEMMs.
+// GEMMs (with_plan: when no earlier kernel wrote it).
 __global__ void __launch_bounds__(256)
     gather_plan_kernel(const __nv_bfloat16 *__restrict__ x, const int32_t *__restrict__ perm_src,
                        const int32_t *__restrict__ inv_pos, const int32_t *__restrict__ offsets,
                        int T, int k, int E, int H, int I, int shared,
-                       __nv_bfloat16 *__restrict__ x_perm, int32_t *__restrict__ plan, int num_sms,
-                       uint32_t *__restrict__ status) {
+                       __nv_bfloat16 *__restrict__ x_perm, int32_t *__restrict__ plan,
+                       int with_plan, int num_sms, uint32_t *__restrict__ status) {
   pdl_wait();
   pdl_launch_dependents();
   const int64_t Na = (int64_t)T * k;
   const int64_t R = Na + (shared ? T : 0);
-  if (blockIdx.x == gridDim.x - 1) {
-    // ---- tile plan ----
-    __shared__ int warp_tot[32];
-    __shared__ int tot_gu, tot_dn, bad, max_m, n_chunks, n_wide, st_narrow, st_wide;
-    const int nseg = E + (shared ? 1 : 0);
-    const int nj_dn = (H + kBM - 1) / kBM;
-    if (threadIdx.x == 0) {
-      bad = 0;
-      max_m = 0;
-      n_chunks = 0;
-      n_wide = 0;
-      st_narrow = 0;
-      st_wide = 0;
-    }
-    __syncthreads();
-    // validate the offsets (caller-provided in the standalone call)
-    for (int e = threadIdx.x; e < E; e += blockDim.x)
-      if (offsets[e] < 0 || offsets[e + 1] < offsets[e] || offsets[e + 1] > Na) bad = 1;
-    if (threadIdx.x == 0 && offsets[0] != 0) bad = 1;
-    __syncthreads();
-    if (threadIdx.x == 0 && bad) atomicOr(status, kStatusBadOffsets);
-    int32_t *seg_row = plan, *pref_gu = plan + nseg + 1, *pref_dn = plan + 2 * (nseg + 1);
-    // each thread owns up to 3 consecutive segments (nseg <= 513 < 3*256)
-    constexpr int kPer = 3;
-    const int s0 = threadIdx.x * kPer;
-    int ms[kPer];
-#pragma unroll
-    for (int q = 0; q < kPer; ++q) {
-      const int s = s0 + q;
-      int m = 0;
-      if (!bad && s < nseg) m = (s < E) ? offsets[s + 1] - offsets[s] : T;
-      ms[q] = m;
-      if (m > 0) {
-        atomicMax(&max_m, m);
-        // 256-row token chunks; "wide" ones have more than 128 rows
-        atomicAdd(&n_chunks, (m + kTileRowsDown - 1) / kTileRowsDown);
-        atomicAdd(&n_wide, m / kTileRowsDown + (m % kTileRowsDown > 128 ? 1 : 0));
-        // gate/up pipeline stages per 128 weight rows and K step: narrow tiles
-        // (128 + 128 rows by <= 128 tokens) vs wide (64 + 64 rows by <= 256)
-        atomicAdd(&st_narrow, (m + kTileRowsGateUp - 1) / kTileRowsGateUp);
-        atomicAdd(&st_wide, 2 * ((m + kTileRowsDown - 1) / kTileRowsDown));
-      }
-      if (s < nseg) seg_row[s] = bad ? 0 : ((s < E) ? offsets[s] : (int)Na);
-    }
-    __syncthreads();
-    // Pipeline layouts.  Down: "wide" (stages of 256 token rows) when most
-    // 256-row chunks have more than 128 rows.  Gate/up: wide tiles (64 gate +
-    // 64 up rows by <= 256 token rows, one N <= 256 MMA per K16 step) when
-    // they need at most 9/8 the stages of narrow tiles (128 + 128 rows by
-    // <= 128 token rows, two MMAs per K16 step).  Measured: a wide stage costs
-    // about 0.9 of a narrow one (Mixtral T=4096, ratio 1.04: wide 7% faster;
-    // DeepSeek-V3 T=8192, ratio 1.29: wide 10% slower).
-    const bool wide_dn = n_wide > 0 && 2 * n_wide >= n_chunks;
-    const bool wide_gu = st_narrow > 0 && 8 * st_wide <= 9 * st_narrow;
-    const int tr_gu = wide_gu ? kTileRowsDown : kTileRowsGateUp;
-    const int nj_gu =
-        wide_gu ? (I + kGateUpColsWide - 1) / kGateUpColsWide : (I + kBM - 1) / kBM;
-    int gu[kPer], dn[kPer], sum_gu = 0, sum_dn = 0;
-#pragma unroll
-    for (int q = 0; q < kPer; ++q) {
-      gu[q] = (ms[q] + tr_gu - 1) / tr_gu * nj_gu;
-      dn[q] = (ms[q] + kTileRowsDown - 1) / kTileRowsDown * nj_dn;
-      sum_gu += gu[q];
-      sum_dn += dn[q];
-    }
-    int run_gu = block_exclusive_scan(sum_gu, warp_tot, &tot_gu);
-    int run_dn = block_exclusive_scan(sum_dn, warp_tot, &tot_dn);
-#pragma unroll
-    for (int q = 0; q < kPer; ++q) {
-      const int s = s0 + q;
-      if (s < nseg) {
-        pref_gu[s] = run_gu;
-        pref_dn[s] = run_dn;
-      }
-      run_gu += gu[q];
-      run_dn += dn[q];
-    }
-    if (threadIdx.x == 0) {
-      seg_row[nseg] = bad ? 0 : (int)R;
-      pref_gu[nseg] = tot_gu;
-      pref_dn[nseg] = tot_dn;
-      plan[3 * (nseg + 1)] = choose_split(tot_gu, H / kBK, num_sms, max_m);
-      plan[3 * (nseg + 1) + 1] = choose_split(tot_dn, I / kBK, num_sms, max_m);
-      plan[3 * (nseg + 1) + 2] = wide_gu ? 1 : 0;
-      plan[3 * (nseg + 1) + 3] = wide_dn ? 1 : 0;
-    }
+  if (with_plan && blockIdx.x == gridDim.x - 1) {
+    write_tile_plan(offsets, T, k, E, H, I, shared, plan, num_sms, status);
     return;
   }
   // ---- gather ----
@@ -350,7 +370,7 @@ __global__ void __launch_bounds__(kSmallThreads)
                           int64_t Na, int E, int32_t *__restrict__ counts,
                           int32_t *__restrict__ offsets, int32_t *__restrict__ perm_src,
                           int32_t *__restrict__ inv_pos, float *__restrict__ w_perm,
-                          uint32_t *__restrict__ status) {
+                          uint32_t *__restrict__ status, PlanArgs pa) {
   pdl_wait();
   pdl_launch_dependents();
   __shared__ int base[kMaxE];
@@ -402,6 +422,8 @@ __global__ void __launch_bounds__(kSmallThreads)
     if (e >= 0 && leader) atomicAdd(&base[e], __popc(peers));
     __syncthreads();
   }
+  if (pa.plan != nullptr) write_tile_plan(offsets, pa.T, pa.k, E, pa.H, pa.I, pa.shared, pa.plan,
+                                          pa.num_sms, pa.status);
 }
 
 }  // namespace
@@ -409,11 +431,21 @@ __global__ void __launch_bounds__(kSmallThreads)
 cudaError_t launch_dispatch(const int32_t *ids, const float *topk_w, int T, int k, int E,
                             int32_t *blk_counts, int32_t *blk_base, int32_t *counts,
                             int32_t *offsets, int32_t *perm_src, int32_t *inv_pos, float *w_perm,
-                            uint32_t *status, cudaStream_t s) {
+                            uint32_t *status, int32_t *plan, int H, int I, int shared,
+                            cudaStream_t s) {
   const int64_t Na = (int64_t)T * k;
+  PlanArgs pa;
+  pa.plan = plan;
+  pa.T = T;
+  pa.k = k;
+  pa.H = H;
+  pa.I = I;
+  pa.shared = shared;
+  pa.num_sms = plan != nullptr ? num_sms() : 1;
+  pa.status = status;
   if (Na <= kSmallDispatch) {
     return launch_pdl(dispatch_small_kernel, dim3(1), dim3(kSmallThreads), 0, s, ids, topk_w, Na, E,
-                      counts, offsets, perm_src, inv_pos, w_perm, status);
+                      counts, offsets, perm_src, inv_pos, w_perm, status, pa);
   }
   const int64_t chunk = dispatch_chunk(Na);
   const int nblk = (int)((Na + chunk - 1) / chunk);
@@ -421,7 +453,7 @@ cudaError_t launch_dispatch(const int32_t *ids, const float *topk_w, int T, int 
                              Na, chunk, E, blk_counts, status);
   if (e == cudaSuccess)
     e = launch_pdl(dispatch_scan_kernel, dim3(1), dim3(kMaxE), 0, s, blk_counts, nblk, E, blk_base,
-                   counts, offsets);
+                   counts, offsets, pa);
   if (e == cudaSuccess)
     e = launch_pdl(dispatch_scatter_kernel, dim3(nblk), dim3(kDispatchThreads), 0, s, ids, topk_w,
                    Na, chunk, E, blk_base, perm_src, inv_pos, w_perm);
@@ -432,11 +464,13 @@ cudaError_t launch_gather_plan(const __nv_bfloat16 *x, const int32_t *perm_src,
                                const int32_t *inv_pos, const int32_t *offsets, int T, int k, int E,
                                int H, int I, int shared, __nv_bfloat16 *x_perm, int32_t *plan,
                                uint32_t *status, cudaStream_t s) {
-  // eight warps per block: one per token (with inv_pos) or per x_perm row
+  // eight warps per block: one per token (with inv_pos) or per x_perm row;
+  // one more block writes the tile plan when `plan` is given
   const int64_t units = inv_pos != nullptr ? (int64_t)T : (int64_t)T * k + (shared ? T : 0);
-  const int blocks = (int)((units + 7) / 8) + 1;
+  const int with_plan = plan != nullptr ? 1 : 0;
+  const int blocks = (int)((units + 7) / 8) + with_plan;
   return launch_pdl(gather_plan_kernel, dim3(blocks), dim3(256), 0, s, x, perm_src, inv_pos,
-                    offsets, T, k, E, H, I, shared, x_perm, plan, num_sms(), status);
+                    offsets, T, k, E, H, I, shared, x_perm, plan, with_plan, num_sms(), status);
 }
 
 }  // namespace moe

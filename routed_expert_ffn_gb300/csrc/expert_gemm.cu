@@ -184,7 +184,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tm_aw,    // gate/up, wide: 64-row box
                        const __grid_constant__ CUtensorMap tm_aw_sh,
                        const __grid_constant__ TokenMaps tm_b,       // activations [R, K] (3D)
-                       const int32_t *__restrict__ plan, int nseg, int E, int K, int out_cols,
+                       const int32_t *__restrict__ plan, int plan_early, int nseg, int E, int K,
+                       int out_cols,
                        int64_t Na, const float *__restrict__ w_perm, void *__restrict__ out_,
                        float *__restrict__ split_part, uint32_t *__restrict__ split_cnt,
                        uint32_t *__restrict__ status) {
@@ -241,15 +242,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 16; ++i) tma_prefetch_desc(&tm_b.m[i]);
   }
-  // everything above is independent of earlier kernels' outputs
-  pdl_wait();
-  pdl_launch_dependents();
+  // Everything above is independent of earlier kernels' outputs.  With
+  // plan_early the tile plan was complete before the preceding kernel
+  // started (it comes from an earlier kernel of the chain), so it is read
+  // (through L2) before waiting on that kernel, and the producer requests its
+  // first stages' weights before the wait too; only the token rows, the
+  // preceding kernel's output, wait.
+  const bool early = plan_early != 0;
+  if (!early) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
   const int32_t *g_pref = plan + (kGateUp ? 1 : 2) * (nseg + 1);
   for (int i = threadIdx.x; i <= nseg; i += blockDim.x) {
-    seg_row[i] = plan[i];
-    pref[i] = g_pref[i];
+    seg_row[i] = __ldcg(plan + i);
+    pref[i] = __ldcg(g_pref + i);
   }
-  if (threadIdx.x == 0) *s_kbs = plan[3 * (nseg + 1) + (kGateUp ? 0 : 1)];
+  if (threadIdx.x == 0) *s_kbs = __ldcg(plan + 3 * (nseg + 1) + (kGateUp ? 0 : 1));
   // Stage layout of this launch (chosen by the tile plan).  Each stage holds
   // kStageKB K blocks of weights [K blocks][P][rows][64] and of token rows
   // [K blocks][rows][64]:
@@ -259,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   //    load hits L2);
   //  - wide: gate/up 64 gate + 64 up rows, down 128 rows, with <= 256 token
   //    rows in one stage and one MMA per K16 step.
-  const bool wide = plan[3 * (nseg + 1) + (kGateUp ? 2 : 3)] != 0;
+  const bool wide = __ldcg(plan + 3 * (nseg + 1) + (kGateUp ? 2 : 3)) != 0;
   const int tile_rows = (kGateUp && !wide) ? kTileRowsGateUp : kTileRowsDown;
   const int out_w = (kGateUp && wide) ? kGateUpColsWide : kBM;  // output columns per tile
   const uint32_t chunk_a = (kGateUp && !wide) ? 2 * kChunkBytes : kChunkBytes;  // per K block
@@ -271,6 +280,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (early && warp != 4) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
   const uint32_t tmem_base = *tmem_slot;
   const int total = pref[nseg];
   const int nkb = K / kBK;
@@ -288,6 +301,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t st = 0, ph = 0, issued = 0;  // stage, parity of its use, stages issued
       bool ok = true;
+      // before the wait on the preceding kernel (plan_early): the first nst
+      // stages' token-row copies are queued and issued after it
+      bool waiting = early;
+      int nq = 0;
+      uint32_t q_st[kMaxStages];
+      int q_row[kMaxStages], q_h[kMaxStages], q_kb[kMaxStages];
+      auto release_queue = [&]() {
+        pdl_wait();
+        pdl_launch_dependents();
+        for (int i = 0; i < nq; ++i)
+          tma_load_3d(ring + q_st[i] * stage_bytes + stage_a, &tm_b.m[(q_h[i] >> 4) - 1],
+                      &full[q_st[i]], 0, q_row[i], q_kb[i]);
+        nq = 0;
+        waiting = false;
+      };
       for (int pc = blockIdx.x; ok && pc < total_pieces; pc += gridDim.x) {
         const int tile = pc / S, z = pc - tile * S;
         const Tile t = decode_tile(tile, tile_rows, seg_row, pref, nseg);
@@ -300,6 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nu = (!wide && h1 > 0) ? 2 : 1;  // stages per K step
         for (int kb = kb0; ok && kb < kb1; kb += kStageKB) {
           for (int u = 0; u < nu; ++u) {
+            if (waiting && issued == nst) release_queue();  // before any stage is reused
             if (!mbar_wait(&empty[st], ph ^ 1u, abort_flag, status, kCode)) {
               ok = false;
               break;
@@ -312,7 +341,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             // [K blocks][P][rows][64]: gate/up P = 2 (gate rows, then the same
             // up rows), down P = 1
             tma_load_5d(dst, ma, &full[st], 0, t.j * out_w, 0, kb, ecoord);
-            tma_load_3d(dst + stage_a, &tm_b.m[(hb >> 4) - 1], &full[st], 0, t.row0 + u * 128, kb);
+            if (waiting) {
+              q_st[nq] = st;
+              q_row[nq] = t.row0 + u * 128;
+              q_h[nq] = hb;
+              q_kb[nq] = kb;
+              ++nq;
+            } else {
+              tma_load_3d(dst + stage_a, &tm_b.m[(hb >> 4) - 1], &full[st], 0, t.row0 + u * 128,
+                          kb);
+            }
             ++issued;
             if (++st == nst) {
               st = 0;
@@ -321,6 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      if (waiting) release_queue();
       // Drain: every issued copy must land before the CTA may exit.
       const uint32_t n = issued < nst ? issued : nst;
       for (uint32_t i = 0; i < n; ++i) {
@@ -604,7 +643,8 @@ bool act_map(CUtensorMap *m, const void *a, int K, int64_t R, int box_rows) {
 
 template <bool kGateUp>
 cudaError_t launch_gemm(const moe_layer_desc_t &d, const void *w, const void *w_sh,
-                        const __nv_bfloat16 *act, const int32_t *plan, const float *w_perm,
+                        const __nv_bfloat16 *act, const int32_t *plan, int plan_early,
+                        const float *w_perm,
                         void *out, float *split_part, uint32_t *split_cnt, uint32_t *status,
                         cudaStream_t s) {
   using C = Cfg<kGateUp>;
@@ -654,26 +694,28 @@ cudaError_t launch_gemm(const moe_layer_desc_t &d, const void *w, const void *w_
   // one CTA per SM: the device-side plan decides the tiles (and split-K
   // pieces); CTAs without work leave at once
   const int grid = num_sms();
-  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, ma, msh, maw, mawsh, mb, plan, nseg,
-                    d.E, K, rows, Na, w_perm, out, split_part, split_cnt, status);
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, ma, msh, maw, mawsh, mb, plan,
+                    plan_early, nseg, d.E, K, rows, Na, w_perm, out, split_part, split_cnt, status);
 }
 
 }  // namespace
 
 cudaError_t launch_expert_gateup(const moe_layer_desc_t &d, const void *w13, const void *w13_shared,
-                                 const __nv_bfloat16 *x_perm, const int32_t *plan,
+                                 const __nv_bfloat16 *x_perm, const int32_t *plan, int plan_early,
                                  float *split_part, uint32_t *split_cnt, __nv_bfloat16 *h,
                                  uint32_t *status, cudaStream_t s) {
-  return launch_gemm<true>(d, w13, w13_shared, x_perm, plan, nullptr, h, split_part, split_cnt,
-                          status, s);
+  return launch_gemm<true>(d, w13, w13_shared, x_perm, plan, plan_early, nullptr, h, split_part,
+                           split_cnt, status, s);
 }
 
 cudaError_t launch_expert_down(const moe_layer_desc_t &d, const void *w2, const void *w2_shared,
                                const __nv_bfloat16 *h, const int32_t *plan, const float *w_perm,
                                float *split_part, uint32_t *split_cnt, __half *out_perm,
                                uint32_t *status, cudaStream_t s) {
-  return launch_gemm<false>(d, w2, w2_shared, h, plan, w_perm, out_perm, split_part, split_cnt,
-                           status, s);
+  // the plan comes from the dispatch or the gather kernel: at least two
+  // launches before the down GEMM
+  return launch_gemm<false>(d, w2, w2_shared, h, plan, 1, w_perm, out_perm, split_part, split_cnt,
+                            status, s);
 }
 
 }  // namespace moe

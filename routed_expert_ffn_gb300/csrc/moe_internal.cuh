@@ -126,12 +126,22 @@ cudaError_t launch_route_small(const __nv_bfloat16 *x, const float *w_router,
 cudaError_t launch_topk_gating(const float *partial, int splits, const float *sel_bias, int T,
                                int E, int k, int gating, float *logits, int32_t *ids, float *w,
                                float *gap, cudaStream_t s);
+// Where a dispatch kernel also writes the GEMMs' tile plan (plan != null).
+struct PlanArgs {
+  int32_t *plan;
+  int T, k, H, I, shared, num_sms;
+  uint32_t *status;
+};
+// plan may be null; otherwise the dispatch also writes the tile plan, so the
+// expert GEMMs can read it before waiting on the gather kernel.
 cudaError_t launch_dispatch(const int32_t *ids, const float *topk_w, int T, int k, int E,
                             int32_t *blk_counts, int32_t *blk_base, int32_t *counts,
                             int32_t *offsets, int32_t *perm_src, int32_t *inv_pos, float *w_perm,
-                            uint32_t *status, cudaStream_t s);
+                            uint32_t *status, int32_t *plan, int H, int I, int shared,
+                            cudaStream_t s);
 // inv_pos may be null: then one warp per x_perm row (the standalone FFN call,
-// and layer forwards whose x is at most kGatherByTokenBytes).
+// and layer forwards whose x is at most kGatherByTokenBytes).  plan may be
+// null (the dispatch wrote it); otherwise one more block writes it.
 constexpr int64_t kGatherByTokenBytes = 8ll << 20;
 cudaError_t launch_gather_plan(const __nv_bfloat16 *x, const int32_t *perm_src,
                                const int32_t *inv_pos, const int32_t *offsets, int T, int k, int E,
@@ -139,8 +149,10 @@ cudaError_t launch_gather_plan(const __nv_bfloat16 *x, const int32_t *perm_src,
                                uint32_t *status, cudaStream_t s);
 // split_part: kMaxSplitTiles x 2 x kBM x kSplitMaxRows fp32; split_cnt: the
 // GEMM's kMaxSplitTiles arrival counters (in the workspace status block).
+// plan_early: the plan was written before the kernel preceding the GEMM
+// (by the dispatch), so the GEMM may read it before waiting on that kernel.
 cudaError_t launch_expert_gateup(const moe_layer_desc_t &d, const void *w13, const void *w13_shared,
-                                 const __nv_bfloat16 *x_perm, const int32_t *plan,
+                                 const __nv_bfloat16 *x_perm, const int32_t *plan, int plan_early,
                                  float *split_part, uint32_t *split_cnt, __nv_bfloat16 *h,
                                  uint32_t *status, cudaStream_t s);
 cudaError_t launch_expert_down(const moe_layer_desc_t &d, const void *w2, const void *w2_shared,

@@ -102,7 +102,8 @@ extern "C" moe_status_t moe_build_dispatch_noalloc(const moe_layer_desc_t *d,
   cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s);
   if (e == cudaSuccess)
     e = launch_dispatch(topk_ids, topk_w, d->T, d->k, d->E, blk_counts, blk_base, counts, offsets,
-                        perm_src, inv_pos, w_perm, status, s);
+                        perm_src, inv_pos, w_perm, status, nullptr, d->H, d->I,
+                        d->has_shared_expert, s);
   if (e == cudaSuccess && device_status != nullptr)
     e = cudaMemcpyAsync(device_status, status, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
