@@ -13,7 +13,7 @@
 //               running per-expert base orders the block's sub-chunks.
 // The result is bit-exact: expert e owns positions [offsets[e], offsets[e+1])
 // in ascending assignment (hence token) order.
-#include "moe_internal.cuh"
+#include "dispatch_block.cuh"
 
 namespace moe {
 
@@ -43,38 +43,6 @@ __global__ void __launch_bounds__(kDispatchThreads)
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) blk_counts[(size_t)blockIdx.x * E + e] = cnt[e];
 }
-
-// Exclusive scan of one value per thread over a block of up to 1024 threads.
-__device__ int block_exclusive_scan(int v, int *warp_tot, int *total) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
-  int incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int u = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += u;
-  }
-  if (lane == 31) warp_tot[w] = incl;
-  __syncthreads();
-  if (w == 0) {
-    int t = (lane < nw) ? warp_tot[lane] : 0;
-    int ti = t;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int u = __shfl_up_sync(0xffffffffu, ti, o);
-      if (lane >= o) ti += u;
-    }
-    if (lane < nw) warp_tot[lane] = ti - t;  // exclusive prefix of warp totals
-    if (lane == nw - 1) *total = ti;
-  }
-  __syncthreads();
-  const int r = warp_tot[w] + incl - v;
-  __syncthreads();
-  return r;
-}
-
-__device__ void write_tile_plan(const int32_t *__restrict__ offsets, int T, int k, int E, int H,
-                                int I, int shared, int32_t *__restrict__ plan, int num_sms,
-                                uint32_t *__restrict__ status);
 
 __global__ void __launch_bounds__(kMaxE)
     dispatch_scan_kernel(const int32_t *__restrict__ blk_counts, int nblk, int E,
@@ -144,131 +112,6 @@ __global__ void __launch_bounds__(kDispatchThreads)
     __syncthreads();
   }
   (void)lane;
-}
-
-// Split-K of one GEMM, as the number of K blocks per piece: nkb (no split)
-// or an even number below nkb (the GEMM streams K in steps of two blocks).
-// With `total` tiles on `num_sms` SMs it minimises the K blocks the busiest
-// SM streams.  Only small batches split (every tile has at most
-// kSplitMaxRows token rows).  Cost model, in K blocks streamed by the busiest
-// SM: each piece also pays a fixed epilogue cost (partial store, fence,
-// arrival, barriers) worth kSplitPieceCost K blocks, and the last piece reads
-// the partials.  A split is taken only if it saves at least a fifth.
-__device__ int choose_split(int total, int nkb, int num_sms, int max_m) {
-  // 32-bit arithmetic throughout: total*pieces <= kMaxSplitTiles is checked
-  // before any product that could grow, nkb <= 512
-  constexpr int kSplitPieceCost = 8;  // measured: 2 and 4 split too eagerly
-  if (total <= 0 || max_m > kSplitMaxRows || total > kMaxSplitTiles / 2) return nkb;
-  const int base = (total + num_sms - 1) / num_sms * nkb;
-  int best = nkb, best_cost = base;
-  for (int S = 2; S <= kMaxSplit; ++S) {
-    const int kbs = 2 * ((nkb + 2 * S - 1) / (2 * S));  // even, >= 2
-    if (kbs >= nkb) continue;
-    const int pieces = (nkb + kbs - 1) / kbs;  // no empty piece
-    if (total * pieces > kMaxSplitTiles) break;
-    const int cost = (total * pieces + num_sms - 1) / num_sms * (kbs + kSplitPieceCost) + pieces;
-    if (cost < best_cost) {
-      best = kbs;
-      best_cost = cost;
-    }
-  }
-  return (best_cost * 5 <= base * 4) ? best : nkb;
-}
-
-// The tile plan of the grouped GEMMs from the dispatch offsets (see the
-// workspace layout's `plan` field): segment row offsets, the gate/up and down
-// tile prefix sums, split-K pieces and pipeline layouts.  Called by every
-// thread of one block of 171..1024 threads (each thread owns up to three
-// consecutive segments; nseg <= 513).
-__device__ void write_tile_plan(const int32_t *__restrict__ offsets, int T, int k, int E, int H,
-                                int I, int shared, int32_t *__restrict__ plan, int num_sms,
-                                uint32_t *__restrict__ status) {
-  const int64_t Na = (int64_t)T * k;
-  const int64_t R = Na + (shared ? T : 0);
-  __shared__ int warp_tot[32];
-  __shared__ int tot_gu, tot_dn, bad, max_m, n_chunks, n_wide, st_narrow, st_wide;
-  const int nseg = E + (shared ? 1 : 0);
-  const int nj_dn = (H + kBM - 1) / kBM;
-  if (threadIdx.x == 0) {
-    bad = 0;
-    max_m = 0;
-    n_chunks = 0;
-    n_wide = 0;
-    st_narrow = 0;
-    st_wide = 0;
-  }
-  __syncthreads();
-  // validate the offsets (caller-provided in the standalone call)
-  for (int e = threadIdx.x; e < E; e += blockDim.x)
-    if (offsets[e] < 0 || offsets[e + 1] < offsets[e] || offsets[e + 1] > Na) bad = 1;
-  if (threadIdx.x == 0 && offsets[0] != 0) bad = 1;
-  __syncthreads();
-  if (threadIdx.x == 0 && bad) atomicOr(status, kStatusBadOffsets);
-  int32_t *seg_row = plan, *pref_gu = plan + nseg + 1, *pref_dn = plan + 2 * (nseg + 1);
-  // each thread owns up to 3 consecutive segments (nseg <= 513 < 3*256)
-  constexpr int kPer = 3;
-  const int s0 = threadIdx.x * kPer;
-  int ms[kPer];
-#pragma unroll
-  for (int q = 0; q < kPer; ++q) {
-    const int s = s0 + q;
-    int m = 0;
-    if (!bad && s < nseg) m = (s < E) ? offsets[s + 1] - offsets[s] : T;
-    ms[q] = m;
-    if (m > 0) {
-      atomicMax(&max_m, m);
-      // 256-row token chunks; "wide" ones have more than 128 rows
-      atomicAdd(&n_chunks, (m + kTileRowsDown - 1) / kTileRowsDown);
-      atomicAdd(&n_wide, m / kTileRowsDown + (m % kTileRowsDown > 128 ? 1 : 0));
-      // gate/up pipeline stages per 128 weight rows and K step: narrow tiles
-      // (128 + 128 rows by <= 128 tokens) vs wide (64 + 64 rows by <= 256)
-      atomicAdd(&st_narrow, (m + kTileRowsGateUp - 1) / kTileRowsGateUp);
-      atomicAdd(&st_wide, 2 * ((m + kTileRowsDown - 1) / kTileRowsDown));
-    }
-    if (s < nseg) seg_row[s] = bad ? 0 : ((s < E) ? offsets[s] : (int)Na);
-  }
-  __syncthreads();
-  // Pipeline layouts.  Down: "wide" (stages of 256 token rows) when most
-  // 256-row chunks have more than 128 rows.  Gate/up: wide tiles (64 gate +
-  // 64 up rows by <= 256 token rows, one N <= 256 MMA per K16 step) when
-  // they need at most 9/8 the stages of narrow tiles (128 + 128 rows by
-  // <= 128 token rows, two MMAs per K16 step).  Measured: a wide stage costs
-  // about 0.9 of a narrow one (Mixtral T=4096, ratio 1.04: wide 7% faster;
-  // DeepSeek-V3 T=8192, ratio 1.29: wide 10% slower).
-  const bool wide_dn = n_wide > 0 && 2 * n_wide >= n_chunks;
-  const bool wide_gu = st_narrow > 0 && 8 * st_wide <= 9 * st_narrow;
-  const int tr_gu = wide_gu ? kTileRowsDown : kTileRowsGateUp;
-  const int nj_gu =
-      wide_gu ? (I + kGateUpColsWide - 1) / kGateUpColsWide : (I + kBM - 1) / kBM;
-  int gu[kPer], dn[kPer], sum_gu = 0, sum_dn = 0;
-#pragma unroll
-  for (int q = 0; q < kPer; ++q) {
-    gu[q] = (ms[q] + tr_gu - 1) / tr_gu * nj_gu;
-    dn[q] = (ms[q] + kTileRowsDown - 1) / kTileRowsDown * nj_dn;
-    sum_gu += gu[q];
-    sum_dn += dn[q];
-  }
-  int run_gu = block_exclusive_scan(sum_gu, warp_tot, &tot_gu);
-  int run_dn = block_exclusive_scan(sum_dn, warp_tot, &tot_dn);
-#pragma unroll
-  for (int q = 0; q < kPer; ++q) {
-    const int s = s0 + q;
-    if (s < nseg) {
-      pref_gu[s] = run_gu;
-      pref_dn[s] = run_dn;
-    }
-    run_gu += gu[q];
-    run_dn += dn[q];
-  }
-  if (threadIdx.x == 0) {
-    seg_row[nseg] = bad ? 0 : (int)R;
-    pref_gu[nseg] = tot_gu;
-    pref_dn[nseg] = tot_dn;
-    plan[3 * (nseg + 1)] = choose_split(tot_gu, H / kBK, num_sms, max_m);
-    plan[3 * (nseg + 1) + 1] = choose_split(tot_dn, I / kBK, num_sms, max_m);
-    plan[3 * (nseg + 1) + 2] = wide_gu ? 1 : 0;
-    plan[3 * (nseg + 1) + 3] = wide_dn ? 1 : 0;
-  }
 }
 
 // Rows [0, Na): x_perm[p] = x[perm_src[p] / k]; rows [Na, Na+T) (shared
@@ -358,12 +201,9 @@ __global__ void __launch_bounds__(256)
 }
 
 // Small batches (N_a <= kSmallDispatch): histogram, scan and stable scatter
-// in one block, so the dispatch is one launch.  The ranking is the same as
-// the multi-block path's: chunks of the block size in order, warps in order
-// inside a chunk (per-warp counts), lanes in order inside a warp
-// (__match_any_sync).
+// in one block (dispatch_block), so the dispatch is one launch; the block
+// then writes the tile plan.
 constexpr int kSmallThreads = 512;
-constexpr int kSmallWarps = kSmallThreads / 32;
 
 __global__ void __launch_bounds__(kSmallThreads)
     dispatch_small_kernel(const int32_t *__restrict__ ids, const float *__restrict__ topk_w,
@@ -373,55 +213,8 @@ __global__ void __launch_bounds__(kSmallThreads)
                           uint32_t *__restrict__ status, PlanArgs pa) {
   pdl_wait();
   pdl_launch_dependents();
-  __shared__ int base[kMaxE];
-  __shared__ int wcnt[kSmallWarps][kMaxE];
-  __shared__ int warp_tot[32];
-  __shared__ int total;
-  const int w = threadIdx.x >> 5;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) base[e] = 0;
-  __syncthreads();
-  bool bad = false;
-  for (int64_t a = threadIdx.x; a < Na; a += blockDim.x) {
-    const int e = ids[a];
-    if (e >= 0 && e < E)
-      atomicAdd(&base[e], 1);
-    else
-      bad = true;
-  }
-  if (bad) atomicOr(status, kStatusBadExpertId);
-  __syncthreads();
-  const int cnt = (threadIdx.x < E) ? base[threadIdx.x] : 0;
-  const int excl = block_exclusive_scan(cnt, warp_tot, &total);
-  if (threadIdx.x < E) {
-    counts[threadIdx.x] = cnt;
-    offsets[threadIdx.x] = excl;
-    base[threadIdx.x] = excl;
-  }
-  if (threadIdx.x == 0) offsets[E] = total;
-  __syncthreads();
-  for (int64_t sub = 0; sub < Na; sub += kSmallThreads) {
-    for (int i = threadIdx.x; i < kSmallWarps * E; i += blockDim.x) wcnt[i / E][i % E] = 0;
-    __syncthreads();
-    const int64_t a = sub + threadIdx.x;
-    int e = (a < Na) ? ids[a] : -1;
-    if (e < 0 || e >= E) e = -1;
-    const uint32_t peers = __match_any_sync(0xffffffffu, e);
-    const uint32_t below = peers & lanemask_lt();
-    const bool leader = (below == 0);
-    if (e >= 0 && leader) wcnt[w][e] = __popc(peers);
-    __syncthreads();
-    if (e >= 0) {
-      int before = 0;
-      for (int ww = 0; ww < w; ++ww) before += wcnt[ww][e];
-      const int pos = base[e] + before + __popc(below);
-      perm_src[pos] = (int32_t)a;
-      inv_pos[a] = pos;
-      if (w_perm != nullptr) w_perm[pos] = topk_w[a];
-    }
-    __syncthreads();
-    if (e >= 0 && leader) atomicAdd(&base[e], __popc(peers));
-    __syncthreads();
-  }
+  dispatch_block<kSmallThreads>(ids, topk_w, Na, E, counts, offsets, perm_src, inv_pos, w_perm,
+                                status);
   if (pa.plan != nullptr) write_tile_plan(offsets, pa.T, pa.k, E, pa.H, pa.I, pa.shared, pa.plan,
                                           pa.num_sms, pa.status);
 }
