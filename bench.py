@@ -340,22 +340,48 @@ def run_gpu(args):
     stage_us = {n: 1e3 * v / args.steps for n, v in stage_ms.items()}
 
     # ---- end to end: pinned host x in, host y out, through the same call ----
+    # Every step copies its x from pinned host memory, runs moe_layer_forward
+    # and copies its y back to pinned host memory.  The copies run on their
+    # own streams with two device buffers each, so a step's copies overlap the
+    # neighbouring steps' forwards (the forwards themselves share the
+    # workspace and run in order on the compute stream).
     x_host = inp.x.cpu().pin_memory()
-    y_host = torch.empty((T, cfg.H), dtype=torch.bfloat16).pin_memory()
-    x_dev = torch.empty_like(inp.x)
+    y_host = [torch.empty((T, cfg.H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    x_dev = [torch.empty_like(inp.x) for _ in range(2)]
+    y_dev = [torch.empty_like(y) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    h2d_done, fwd_done, d2h_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
     e_steps = max(3, min(args.steps, 50))
-    for _ in range(2):
-        x_dev.copy_(x_host, non_blocking=True)
-        moe.moe_layer_forward(d, wts, x_dev, y, ws)
-        y_host.copy_(y, non_blocking=True)
+
+    def e2e_steps(n, start_event=None):
+        for i in range(n):
+            b = i & 1
+            if start_event is not None and i == 0:
+                s_in.wait_event(start_event)
+            if i >= 2:
+                s_in.wait_event(fwd_done[b])      # forward i-2 has read x_dev[b]
+            with torch.cuda.stream(s_in):
+                x_dev[b].copy_(x_host, non_blocking=True)
+                h2d_done[b].record(s_in)
+            stream.wait_event(h2d_done[b])
+            if i >= 2:
+                stream.wait_event(d2h_done[b])    # y_dev[b] of step i-2 is on the host
+            moe.moe_layer_forward(d, wts, x_dev[b], y_dev[b], ws, stream=stream)
+            fwd_done[b].record(stream)
+            s_out.wait_event(fwd_done[b])
+            with torch.cuda.stream(s_out):
+                y_host[b].copy_(y_dev[b], non_blocking=True)
+                d2h_done[b].record(s_out)
+        for b in range(min(n, 2)):
+            stream.wait_event(d2h_done[b])
+
+    e2e_steps(4)
     torch.cuda.synchronize()
     barrier(pg)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e_steps):
-        x_dev.copy_(x_host, non_blocking=True)
-        moe.moe_layer_forward(d, wts, x_dev, y, ws)
-        y_host.copy_(y, non_blocking=True)
+    e2e_steps(e_steps, start_event=e0)
     e1.record(stream)
     torch.cuda.synchronize()
     e_ms = max_over_ranks(e0.elapsed_time(e1), pg)
