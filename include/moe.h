@@ -136,7 +136,9 @@ typedef struct {
                         * 3(nseg+1) + 0 / 1    K blocks (of 64) per split-K
                         *                      piece, gate/up / down
                         * 3(nseg+1) + 2 / 3    pipeline layout, gate/up /
-                        *                      down: 1 = wide, 0 = narrow */
+                        *                      down: 0 = narrow, 1 = wide,
+                        *                      2 = thin (every segment has
+                        *                      at most 16 rows) */
   size_t total;        /* == moe_workspace_size(desc)                     */
 } moe_workspace_layout_t;
 

@@ -155,8 +155,12 @@ static __device__ void write_tile_plan(const int32_t *__restrict__ offsets, int 
     pref_dn[nseg] = tot_dn;
     plan[3 * (nseg + 1)] = choose_split(tot_gu, H / kBK, num_sms, max_m);
     plan[3 * (nseg + 1) + 1] = choose_split(tot_dn, I / kBK, num_sms, max_m);
-    plan[3 * (nseg + 1) + 2] = wide_gu ? 1 : 0;
-    plan[3 * (nseg + 1) + 3] = wide_dn ? 1 : 0;
+    // layouts: 2 = thin (every tile <= kThinRows token rows: stages of
+    // weights + kThinRows token rows, more of them in flight), 1 = wide, 0 =
+    // narrow
+    const bool thin = max_m <= kThinRows;
+    plan[3 * (nseg + 1) + 2] = thin ? 2 : (wide_gu ? 1 : 0);
+    plan[3 * (nseg + 1) + 3] = thin ? 2 : (wide_dn ? 1 : 0);
   }
 }
 

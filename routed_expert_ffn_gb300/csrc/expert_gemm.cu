@@ -97,11 +97,15 @@ constexpr uint32_t kChunkBytes = kBM * kBK * 2;  // 16 KB: 128 rows x 64 bf16
 constexpr uint32_t kTmemCols = 512;              // two accumulators of 256 columns
 constexpr uint32_t kAccCols = kTmemCols / 2;
 // stage sizes (in units of kStageKB * 16 KB): gate/up 3, down 2 (narrow) or 3
-constexpr int kMaxStages = kRingBytes / (2 * kStageKB * kChunkBytes);
-static_assert(kStageKB == 1 || kStageKB == 2, "one or two K blocks per stage");
-static_assert(kRingBytes % (2 * kStageKB * kChunkBytes) == 0 &&
-                  kRingBytes % (3 * kStageKB * kChunkBytes) == 0,
-              "the ring holds whole stages of every layout");
+// token rows of a thin stage (kStageKB K blocks x kThinRows rows)
+constexpr uint32_t kThinB = kStageKB * kThinRows * kBK * 2;
+// the most stages: thin down stages of 32 KB weights + kThinB
+constexpr int kMaxStages = kRingBytes / (kStageKB * kChunkBytes + kThinB);
+static_assert(kStageKB == 2, "stages are pairs of K blocks");
+static_assert(kMaxStages == 5 && kRingBytes == 3 * (2 * kStageKB * kChunkBytes + kThinB),
+              "ring: 3 thin gate/up stages, 5 thin down stages");
+static_assert(kRingBytes >= 2 * 3 * kStageKB * kChunkBytes + 16 * 64 * 4 * 2,
+              "wide gate/up: 2 stages of 96 KB and the up-value exchange buffer");
 
 // Token-row tensor maps with box heights 16, 32, ..., 256 rows (x kStageKB K
 // blocks).
@@ -114,11 +118,10 @@ struct Cfg {
   static constexpr uint32_t STAGE_UNIT = kStageKB * kChunkBytes;  // 128 rows of a stage
   static constexpr uint32_t SOUT_BYTES = 16 * kBM * 2;            // one 16-token slice
   // gate/up, wide layout: up-row values handed to the gate rows' threads
-  static constexpr uint32_t SUP_BYTES = kGateUp ? 16 * kGateUpColsWide * 4 : 0;
   static constexpr uint32_t BAR_BYTES = (2 * kMaxStages + 5) * 8 + 16;
   static constexpr size_t smem_bytes(int nseg) {
-    return 1024 + (size_t)kRingBytes + 2 * SOUT_BYTES + 2 * SUP_BYTES +
-           (size_t)kTileRowsDown * 4 + BAR_BYTES + (size_t)2 * (nseg + 1) * 4;
+    return 1024 + (size_t)kRingBytes + 2 * SOUT_BYTES + (size_t)kTileRowsDown * 4 +
+           BAR_BYTES + (size_t)2 * (nseg + 1) * 4;
   }
   static_assert(smem_bytes(kMaxE + 1) <= 232448, "shared memory per CTA");
 };
@@ -201,8 +204,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                               ~static_cast<uintptr_t>(1023));
   uint8_t *ring = smem;  // [stages][weights | token rows]
   uint16_t *sOut = reinterpret_cast<uint16_t *>(ring + kRingBytes);  // [2][16][kBM]
-  float *sUp = reinterpret_cast<float *>(sOut + 2 * 16 * kBM);        // [2][16][64] (gate/up)
-  float *sW = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(sUp) + 2 * C::SUP_BYTES);
+  // wide gate/up: the up values handed to the gate rows' threads, [2][16][64],
+  // in the ring's last 12 KB (two 96 KB stages leave them free)
+  float *sUp = reinterpret_cast<float *>(ring + 2 * 3 * kStageKB * kChunkBytes);
+  float *sW = reinterpret_cast<float *>(sOut + 2 * 16 * kBM);         // [kTileRowsDown] (down)
   uint64_t *full = reinterpret_cast<uint64_t *>(sW + kTileRowsDown);  // [kMaxStages]
   uint64_t *empty = full + kMaxStages;
   uint64_t *tfull = empty + kMaxStages;
@@ -267,13 +272,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   //    stage per 128-row half (its weights loaded once per half; the second
   //    load hits L2);
   //  - wide: gate/up 64 gate + 64 up rows, down 128 rows, with <= 256 token
-  //    rows in one stage and one MMA per K16 step.
-  const bool wide = __ldcg(plan + 3 * (nseg + 1) + (kGateUp ? 2 : 3)) != 0;
+  //    rows in one stage and one MMA per K16 step;
+  //  - thin (every tile <= kThinRows token rows, the decode regime): narrow
+  //    tiles with a token-row region of kThinRows rows, so 3 gate/up or 5
+  //    down stages of weights are in flight instead of 2 or 3.
+  const int layout = __ldcg(plan + 3 * (nseg + 1) + (kGateUp ? 2 : 3));
+  const bool wide = layout == 1;
+  const bool thin = layout == 2;  // every tile <= kThinRows token rows
   const int tile_rows = (kGateUp && !wide) ? kTileRowsGateUp : kTileRowsDown;
   const int out_w = (kGateUp && wide) ? kGateUpColsWide : kBM;  // output columns per tile
   const uint32_t chunk_a = (kGateUp && !wide) ? 2 * kChunkBytes : kChunkBytes;  // per K block
   const uint32_t stage_a = kStageKB * chunk_a;
-  const uint32_t stage_bytes = stage_a + (wide ? 2 : 1) * C::STAGE_UNIT;
+  const uint32_t stage_bytes = stage_a + (thin ? kThinB : (wide ? 2 : 1) * C::STAGE_UNIT);
   const uint32_t nst = kRingBytes / stage_bytes;
   const CUtensorMap *ma_r = (kGateUp && wide) ? &tm_aw : &tm_a;
   const CUtensorMap *ma_s = (kGateUp && wide) ? &tm_aw_sh : &tm_a_sh;

@@ -62,7 +62,8 @@ constexpr int kGateUpColsWide = 64;
 #define MOE_STAGE_KB 2
 #endif
 constexpr int kStageKB = MOE_STAGE_KB;
-constexpr int kRingBytes = 3 * 65536;  // = 2 * 98304
+constexpr int kThinRows = 16;           // the thin layout: tiles of <= 16 token rows
+constexpr int kRingBytes = 204 * 1024;  // 3 thin gate/up stages of 68 KB
 
 // Status word bits (latched with atomicOr).
 constexpr uint32_t kStatusBadExpertId = 1u << 0;

@@ -178,9 +178,14 @@ def test_tile_plan(name, T):
     nsm = torch.cuda.get_device_properties(0).multi_processor_count
     want = (seg_row + pref(gu) + pref(dn) +
             [_split_kbs(sum(gu), cfg.H // 64, nsm, max(ms)),
-             _split_kbs(sum(dn), cfg.I // 64, nsm, max(ms)), int(wide_gu), int(wide_dn)])
+             _split_kbs(sum(dn), cfg.I // 64, nsm, max(ms))])
+    # pipeline layouts: 2 = thin (every segment <= 16 rows), 1 = wide, 0 = narrow
+    thin = max(ms) <= 16
+    want += [2 if thin else int(wide_gu), 2 if thin else int(wide_dn)]
     assert plan == want
     if name == "mixtral":
         assert wide_gu and wide_dn   # uniform prefill: both GEMMs run wide
     if (name, T) == ("qwen3", 1024):
         assert not wide_gu and not wide_dn
+    if (name, T) in (("qwen3", 1), ("qwen3_tp8", 8)):
+        assert thin
