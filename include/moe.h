@@ -138,7 +138,8 @@ typedef struct {
                         * 3(nseg+1) + 2 / 3    pipeline layout, gate/up /
                         *                      down: 0 = narrow, 1 = wide,
                         *                      2 = thin (every segment has
-                        *                      at most 16 rows) */
+                        *                      at most 16 rows), 3 = medium
+                        *                      (down only: at most 64) */
   size_t total;        /* == moe_workspace_size(desc)                     */
 } moe_workspace_layout_t;
 

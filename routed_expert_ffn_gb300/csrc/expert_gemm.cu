@@ -275,15 +275,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   //    rows in one stage and one MMA per K16 step;
   //  - thin (every tile <= kThinRows token rows, the decode regime): narrow
   //    tiles with a token-row region of kThinRows rows, so 3 gate/up or 5
-  //    down stages of weights are in flight instead of 2 or 3.
+  //    down stages of weights are in flight instead of 2 or 3;
+  //  - medium (down only, every tile <= kMediumRows token rows): 4 stages of
+  //    128 rows + 64 token rows.
   const int layout = __ldcg(plan + 3 * (nseg + 1) + (kGateUp ? 2 : 3));
   const bool wide = layout == 1;
-  const bool thin = layout == 2;  // every tile <= kThinRows token rows
+  const bool thin = layout == 2;    // every tile <= kThinRows token rows
+  const bool medium = layout == 3;  // down: stages of 64 token rows
+  // token rows per stage: a down tile runs one stage per unit of this many
+  // rows (gate/up tiles always fit one stage)
+  const int unit_rows =
+      kGateUp ? 256 : (wide ? 256 : (medium ? kMediumRows : (thin ? kThinRows : 128)));
   const int tile_rows = (kGateUp && !wide) ? kTileRowsGateUp : kTileRowsDown;
   const int out_w = (kGateUp && wide) ? kGateUpColsWide : kBM;  // output columns per tile
   const uint32_t chunk_a = (kGateUp && !wide) ? 2 * kChunkBytes : kChunkBytes;  // per K block
   const uint32_t stage_a = kStageKB * chunk_a;
-  const uint32_t stage_bytes = stage_a + (thin ? kThinB : (wide ? 2 : 1) * C::STAGE_UNIT);
+  const uint32_t stage_bytes =
+      stage_a + (thin ? kThinB : medium ? C::STAGE_UNIT / 2 : (wide ? 2 : 1) * C::STAGE_UNIT);
   const uint32_t nst = kRingBytes / stage_bytes;
   const CUtensorMap *ma_r = (kGateUp && wide) ? &tm_aw : &tm_a;
   const CUtensorMap *ma_s = (kGateUp && wide) ? &tm_aw_sh : &tm_a_sh;
@@ -333,9 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool sh = (t.seg >= E);
         const CUtensorMap *ma = sh ? ma_s : ma_r;
         const int ecoord = sh ? 0 : t.seg;
-        const int h0 = min(128, (t.nrows + 15) & ~15);        // rows of half 0, padded
-        const int h1 = max(0, ((t.nrows + 15) & ~15) - 128);  // rows of half 1, padded
-        const int nu = (!wide && h1 > 0) ? 2 : 1;  // stages per K step
+        const int n16 = (t.nrows + 15) & ~15;       // token rows, padded to 16
+        const int nu = (n16 + unit_rows - 1) / unit_rows;  // stages per K step
         for (int kb = kb0; ok && kb < kb1; kb += kStageKB) {
           for (int u = 0; u < nu; ++u) {
             if (waiting && issued == nst) release_queue();  // before any stage is reused
@@ -344,22 +351,21 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             uint8_t *dst = ring + st * stage_bytes;
-            // token rows of this stage: one 128-row unit, or (nu == 1) the
-            // whole tile, up to 256 rows in the wide layout
-            const int hb = (nu == 2) ? (u == 0 ? h0 : h1) : h0 + h1;
+            // token rows of this stage: unit u of the tile
+            const int hb = min(unit_rows, n16 - u * unit_rows);
             mbar_arrive_expect_tx(&full[st], stage_a + (uint32_t)hb * (kStageKB * kBK * 2));
             // [K blocks][P][rows][64]: gate/up P = 2 (gate rows, then the same
             // up rows), down P = 1
             tma_load_5d(dst, ma, &full[st], 0, t.j * out_w, 0, kb, ecoord);
             if (waiting) {
               q_st[nq] = st;
-              q_row[nq] = t.row0 + u * 128;
+              q_row[nq] = t.row0 + u * unit_rows;
               q_h[nq] = hb;
               q_kb[nq] = kb;
               ++nq;
             } else {
-              tma_load_3d(dst + stage_a, &tm_b.m[(hb >> 4) - 1], &full[st], 0, t.row0 + u * 128,
-                          kb);
+              tma_load_3d(dst + stage_a, &tm_b.m[(hb >> 4) - 1], &full[st], 0,
+                          t.row0 + u * unit_rows, kb);
             }
             ++issued;
             if (++st == nst) {
@@ -392,15 +398,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tile = pc / S, z = pc - tile * S;
         const Tile t = decode_tile(tile, tile_rows, seg_row, pref, nseg);
         const int kb0 = z * kbs, kb1 = min(nkb, kb0 + kbs);
-        const int h0 = min(128, (t.nrows + 15) & ~15);
-        const int h1 = max(0, ((t.nrows + 15) & ~15) - 128);
-        const int nu = (!wide && h1 > 0) ? 2 : 1;
+        const int n16 = (t.nrows + 15) & ~15;
+        const int nu = (n16 + unit_rows - 1) / unit_rows;
         // token column n -> accumulator column n (a wide down tile in the
         // narrow layout as two 128-row units); gate/up, narrow: gate rows ->
         // columns [0, 128), up rows -> [128, 256) of the same token; gate/up,
         // wide: one accumulator, gate rows in lanes [0, 64), up in [64, 128)
-        const uint32_t idesc0 = idesc_bf16_f32(kBM, nu == 2 ? h0 : h0 + h1);
-        const uint32_t idesc1 = idesc_bf16_f32(kBM, h1 > 0 ? h1 : 16);
+
         const uint32_t buf = tl & 1u, use = tl >> 1;
         if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, status, kCode)) break;
         tc_fence_after();
@@ -415,17 +419,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint64_t adesc = desc0 + st * dstage;
             const uint64_t bdesc = adesc + (stage_a >> 4);
-            const int hb = (nu == 2) ? (u == 0 ? h0 : h1) : h0 + h1;
+            const int hb = min(unit_rows, n16 - u * unit_rows);
+            const uint32_t id = idesc_bf16_f32(kBM, hb);
             for (int c = 0; c < nc; ++c) {
               const uint32_t acc = (kb != kb0 || c != 0) ? 1u : 0u;
               const uint64_t ac = adesc + c * (chunk_a >> 4);
               const uint64_t bc = bdesc + c * ((uint32_t)hb * (kBK * 2) >> 4);
               if (kGateUp && !wide) {
-                umma_kblock(d0, ac, bc, idesc0, acc);                              // gate
-                umma_kblock(d0 + 128, ac + (kChunkBytes >> 4), bc, idesc0, acc);  // up
+                umma_kblock(d0, ac, bc, id, acc);                              // gate
+                umma_kblock(d0 + 128, ac + (kChunkBytes >> 4), bc, id, acc);  // up
               } else {
                 // one MMA over all of the stage's token rows (N <= 256)
-                umma_kblock(d0 + (uint32_t)u * 128, ac, bc, u == 0 ? idesc0 : idesc1, acc);
+                umma_kblock(d0 + (uint32_t)(u * unit_rows), ac, bc, id, acc);
               }
             }
             umma_commit(&empty[st]);  // the stage is free once these MMAs have read it

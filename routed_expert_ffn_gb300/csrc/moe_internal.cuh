@@ -63,6 +63,7 @@ constexpr int kGateUpColsWide = 64;
 #endif
 constexpr int kStageKB = MOE_STAGE_KB;
 constexpr int kThinRows = 16;           // the thin layout: tiles of <= 16 token rows
+constexpr int kMediumRows = 64;         // the down GEMM's medium layout: <= 64 rows
 constexpr int kRingBytes = 204 * 1024;  // 3 thin gate/up stages of 68 KB
 
 // Status word bits (latched with atomicOr).

@@ -144,8 +144,8 @@ def _split_kbs(total, nkb, num_sms, max_m):
     return best if best_cost * 5 <= base * 4 else nkb
 
 
-@pytest.mark.parametrize("name,T", [("qwen3", 1), ("qwen3", 1024), ("mixtral", 4096),
-                                    ("qwen3_tp8", 8)])
+@pytest.mark.parametrize("name,T", [("qwen3", 1), ("qwen3", 256), ("qwen3", 1024),
+                                    ("mixtral", 4096), ("qwen3_tp8", 8)])
 def test_tile_plan(name, T):
     """The device-side tile plan (segments, tile prefixes, split-K pieces, layouts)
     is an integer function of the dispatch counts: recomputed here from the rules
@@ -181,7 +181,9 @@ def test_tile_plan(name, T):
              _split_kbs(sum(dn), cfg.I // 64, nsm, max(ms))])
     # pipeline layouts: 2 = thin (every segment <= 16 rows), 1 = wide, 0 = narrow
     thin = max(ms) <= 16
-    want += [2 if thin else int(wide_gu), 2 if thin else int(wide_dn)]
+    medium = max(ms) <= 64
+    want += [2 if thin else int(wide_gu),
+             2 if thin else (3 if medium else int(wide_dn))]
     assert plan == want
     if name == "mixtral":
         assert wide_gu and wide_dn   # uniform prefill: both GEMMs run wide
@@ -189,3 +191,5 @@ def test_tile_plan(name, T):
         assert not wide_gu and not wide_dn
     if (name, T) in (("qwen3", 1), ("qwen3_tp8", 8)):
         assert thin
+    if (name, T) == ("qwen3", 256):
+        assert medium and not thin
