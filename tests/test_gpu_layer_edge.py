@@ -92,3 +92,32 @@ def test_stage_calls_match_layer_forward(T):
     assert np.array_equal(w.cpu().numpy(), meta["w"])
     assert np.array_equal(perm.cpu().numpy(), meta["perm_src"])
     assert torch.equal(y, y_fused)
+
+
+@pytest.mark.parametrize("name,T", [("qwen3", 1), ("qwen3", 300)])
+def test_layer_forward_replays_from_a_cuda_graph(name, T):
+    """The forward makes no host synchronisation or host-side decision on
+    device data, so it can be captured in a CUDA graph; replays give exactly
+    the eager result (and leave the split-K and router counters at zero)."""
+    cfg = synth.CONFIGS[name]
+    inp = synth.make_layer(cfg, T, 0, device="cuda")
+    run = LayerRun(inp)
+    y_eager = run.forward().clone()
+    y = torch.empty_like(y_eager)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        moe.moe_layer_forward(run.d, run.w, inp.x, y, run.ws, stream=s)   # warm-up on s
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        moe.moe_layer_forward(run.d, run.w, inp.x, y, run.ws, stream=s)
+    for _ in range(3):
+        y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y, y_eager)
+    st, raw = moe.moe_get_device_status(run.ws)
+    assert st == moe.MOE_OK, raw
+    del g
