@@ -126,13 +126,16 @@ static __device__ void write_tile_plan(const int32_t *__restrict__ offsets, int 
   // DeepSeek-V3 T=8192, ratio 1.29: wide 10% slower).
   const bool wide_dn = n_wide > 0 && 2 * n_wide >= n_chunks;
   const bool wide_gu = st_narrow > 0 && 8 * st_wide <= 9 * st_narrow;
-  const int tr_gu = wide_gu ? kTileRowsDown : kTileRowsGateUp;
-  const int nj_gu =
-      wide_gu ? (I + kGateUpColsWide - 1) / kGateUpColsWide : (I + kBM - 1) / kBM;
+  const bool thin_all = max_m <= kThinRows;
+  // gate/up segments above this many rows take wide tiles
+  const int wide_above = wide_gu ? 0 : (thin_all ? (1 << 30) : kGateUpWideAbove);
   int gu[kPer], dn[kPer], sum_gu = 0, sum_dn = 0;
 #pragma unroll
   for (int q = 0; q < kPer; ++q) {
-    gu[q] = (ms[q] + tr_gu - 1) / tr_gu * nj_gu;
+    gu[q] = ms[q] > wide_above
+                ? (ms[q] + kTileRowsDown - 1) / kTileRowsDown *
+                      ((I + kGateUpColsWide - 1) / kGateUpColsWide)
+                : (ms[q] + kTileRowsGateUp - 1) / kTileRowsGateUp * ((I + kBM - 1) / kBM);
     dn[q] = (ms[q] + kTileRowsDown - 1) / kTileRowsDown * nj_dn;
     sum_gu += gu[q];
     sum_dn += dn[q];

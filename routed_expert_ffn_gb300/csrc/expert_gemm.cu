@@ -128,6 +128,7 @@ struct Cfg {
 
 struct Tile {
   int seg, j, row0, nrows;
+  bool wide;  // gate/up: 64 + 64 rows of W13 by up to 256 token rows
 };
 
 // Named barrier 1 over the 128 epilogue threads (warps 0-3).
@@ -148,7 +149,11 @@ __device__ __forceinline__ bool epi_all(bool p) {
   return r != 0;
 }
 
-__device__ __forceinline__ Tile decode_tile(int tile, int kTileRows, const int32_t *seg_row,
+// Gate/up tiles are wide (64 + 64 rows of W13 by <= 256 token rows) in
+// segments of more than `wide_above` rows, else 128 + 128 rows by <= 128
+// token rows; down tiles are 128 rows of W2 by <= 256 token rows.
+template <bool kGateUp>
+__device__ __forceinline__ Tile decode_tile(int tile, int wide_above, const int32_t *seg_row,
                                             const int32_t *pref, int nseg) {
   int lo = 0, hi = nseg;  // pref[lo] <= tile < pref[hi]
   while (hi - lo > 1) {
@@ -162,11 +167,13 @@ __device__ __forceinline__ Tile decode_tile(int tile, int kTileRows, const int32
   t.seg = lo;
   const int local = tile - pref[lo];
   const int m = seg_row[lo + 1] - seg_row[lo];
-  const int chunks = (m + kTileRows - 1) / kTileRows;
+  t.wide = kGateUp && m > wide_above;
+  const int rows = (kGateUp && !t.wide) ? kTileRowsGateUp : kTileRowsDown;
+  const int chunks = (m + rows - 1) / rows;
   t.j = local / chunks;
   const int c = local - t.j * chunks;
-  t.row0 = seg_row[lo] + c * kTileRows;
-  t.nrows = min(kTileRows, m - c * kTileRows);
+  t.row0 = seg_row[lo] + c * rows;
+  t.nrows = min(rows, m - c * rows);
   return t;
 }
 
@@ -286,15 +293,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   // rows (gate/up tiles always fit one stage)
   const int unit_rows =
       kGateUp ? 256 : (wide ? 256 : (medium ? kMediumRows : (thin ? kThinRows : 128)));
-  const int tile_rows = (kGateUp && !wide) ? kTileRowsGateUp : kTileRowsDown;
-  const int out_w = (kGateUp && wide) ? kGateUpColsWide : kBM;  // output columns per tile
-  const uint32_t chunk_a = (kGateUp && !wide) ? 2 * kChunkBytes : kChunkBytes;  // per K block
-  const uint32_t stage_a = kStageKB * chunk_a;
+  // gate/up: segments above this many rows get wide tiles (all of them in
+  // the wide layout, the largest in the narrow one, none in the thin one)
+  const int wide_above = wide ? 0 : (thin ? 1 << 30 : kGateUpWideAbove);
+  // gate/up stages: 96 KB for either tile shape (64 KB weights + 32 KB token
+  // rows, or 32 + 64 KB), thin 64 + 4 KB; down stages: 32 KB weights + the
+  // layout's token rows
+  const uint32_t U = C::STAGE_UNIT;
   const uint32_t stage_bytes =
-      stage_a + (thin ? kThinB : medium ? C::STAGE_UNIT / 2 : (wide ? 2 : 1) * C::STAGE_UNIT);
+      kGateUp ? (thin ? 2 * U + kThinB : 3 * U)
+              : U + (thin ? kThinB : medium ? U / 2 : (wide ? 2 : 1) * U);
   const uint32_t nst = kRingBytes / stage_bytes;
-  const CUtensorMap *ma_r = (kGateUp && wide) ? &tm_aw : &tm_a;
-  const CUtensorMap *ma_s = (kGateUp && wide) ? &tm_aw_sh : &tm_a_sh;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -324,23 +333,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool waiting = early;
       int nq = 0;
       uint32_t q_st[kMaxStages];
-      int q_row[kMaxStages], q_h[kMaxStages], q_kb[kMaxStages];
+      int q_row[kMaxStages], q_h[kMaxStages], q_kb[kMaxStages], q_off[kMaxStages];
       auto release_queue = [&]() {
         pdl_wait();
         pdl_launch_dependents();
         for (int i = 0; i < nq; ++i)
-          tma_load_3d(ring + q_st[i] * stage_bytes + stage_a, &tm_b.m[(q_h[i] >> 4) - 1],
+          tma_load_3d(ring + q_st[i] * stage_bytes + q_off[i], &tm_b.m[(q_h[i] >> 4) - 1],
                       &full[q_st[i]], 0, q_row[i], q_kb[i]);
         nq = 0;
         waiting = false;
       };
       for (int pc = blockIdx.x; ok && pc < total_pieces; pc += gridDim.x) {
         const int tile = pc / S, z = pc - tile * S;
-        const Tile t = decode_tile(tile, tile_rows, seg_row, pref, nseg);
+        const Tile t = decode_tile<kGateUp>(tile, wide_above, seg_row, pref, nseg);
         const int kb0 = z * kbs, kb1 = min(nkb, kb0 + kbs);
         const bool sh = (t.seg >= E);
-        const CUtensorMap *ma = sh ? ma_s : ma_r;
+        const CUtensorMap *ma = t.wide ? (sh ? &tm_aw_sh : &tm_aw) : (sh ? &tm_a_sh : &tm_a);
         const int ecoord = sh ? 0 : t.seg;
+        // this tile's weight bytes per stage (and offset of its token rows)
+        const uint32_t stage_a = (kGateUp && !t.wide) ? 2 * U : U;
+        const int arow = t.j * (t.wide ? kGateUpColsWide : kBM);
         const int n16 = (t.nrows + 15) & ~15;       // token rows, padded to 16
         const int nu = (n16 + unit_rows - 1) / unit_rows;  // stages per K step
         for (int kb = kb0; ok && kb < kb1; kb += kStageKB) {
@@ -356,12 +368,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(&full[st], stage_a + (uint32_t)hb * (kStageKB * kBK * 2));
             // [K blocks][P][rows][64]: gate/up P = 2 (gate rows, then the same
             // up rows), down P = 1
-            tma_load_5d(dst, ma, &full[st], 0, t.j * out_w, 0, kb, ecoord);
+            tma_load_5d(dst, ma, &full[st], 0, arow, 0, kb, ecoord);
             if (waiting) {
               q_st[nq] = st;
               q_row[nq] = t.row0 + u * unit_rows;
               q_h[nq] = hb;
               q_kb[nq] = kb;
+              q_off[nq] = (int)stage_a;
               ++nq;
             } else {
               tma_load_3d(dst + stage_a, &tm_b.m[(hb >> 4) - 1], &full[st], 0,
@@ -396,10 +409,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int pc = blockIdx.x; ok && pc < total_pieces; pc += gridDim.x, ++tl) {
         const int tile = pc / S, z = pc - tile * S;
-        const Tile t = decode_tile(tile, tile_rows, seg_row, pref, nseg);
+        const Tile t = decode_tile<kGateUp>(tile, wide_above, seg_row, pref, nseg);
         const int kb0 = z * kbs, kb1 = min(nkb, kb0 + kbs);
         const int n16 = (t.nrows + 15) & ~15;
         const int nu = (n16 + unit_rows - 1) / unit_rows;
+        const uint32_t stage_a = (kGateUp && !t.wide) ? 2 * U : U;  // this tile's weights
+        const uint32_t chunk_a = stage_a / kStageKB;                   // per K block
         // token column n -> accumulator column n (a wide down tile in the
         // narrow layout as two 128-row units); gate/up, narrow: gate rows ->
         // columns [0, 128), up rows -> [128, 256) of the same token; gate/up,
@@ -425,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t acc = (kb != kb0 || c != 0) ? 1u : 0u;
               const uint64_t ac = adesc + c * (chunk_a >> 4);
               const uint64_t bc = bdesc + c * ((uint32_t)hb * (kBK * 2) >> 4);
-              if (kGateUp && !wide) {
+              if (kGateUp && !t.wide) {
                 umma_kblock(d0, ac, bc, id, acc);                              // gate
                 umma_kblock(d0 + 128, ac + (kChunkBytes >> 4), bc, id, acc);  // up
               } else {
@@ -516,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kSlot = (kGateUp ? 2 : 1) * kBM * kSplitMaxRows;
     for (int pc = blockIdx.x; pc < total_pieces; pc += gridDim.x, ++tl) {
       const int tile = pc / S, z = pc - tile * S;
-      const Tile t = decode_tile(tile, tile_rows, seg_row, pref, nseg);
+      const Tile t = decode_tile<kGateUp>(tile, wide_above, seg_row, pref, nseg);
       const uint32_t buf = tl & 1u, use = tl >> 1;
       const bool waited = mbar_wait(&tfull[buf], use & 1u, abort_flag, status, kCode);
       // one decision for all 128 epilogue threads: they share named barriers
@@ -531,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint32_t tb = tmem_base + ((uint32_t)(warp * 32) << 16) + buf * kAccCols;
       const int N = (t.nrows + 15) & ~15;
-      if (kGateUp && wide) {
+      if (kGateUp && t.wide) {
         for (int n0 = 0; n0 < N; n0 += 16) {
           uint32_t v0[16];
           tmem_ld16(tb + n0, v0);

@@ -58,6 +58,12 @@ constexpr int kBK = 64;
 constexpr int kTileRowsGateUp = 128;
 constexpr int kTileRowsDown = 256;
 constexpr int kGateUpColsWide = 64;
+// In the narrow gate/up layout, segments of more than this many rows still take
+// wide tiles (their stages are the same size).
+#ifndef MOE_GU_WIDE_ABOVE
+#define MOE_GU_WIDE_ABOVE 1024
+#endif
+constexpr int kGateUpWideAbove = MOE_GU_WIDE_ABOVE;
 #ifndef MOE_STAGE_KB
 #define MOE_STAGE_KB 2
 #endif

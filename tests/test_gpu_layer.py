@@ -145,7 +145,7 @@ def _split_kbs(total, nkb, num_sms, max_m):
 
 
 @pytest.mark.parametrize("name,T", [("qwen3", 1), ("qwen3", 256), ("qwen3", 1024),
-                                    ("mixtral", 4096), ("qwen3_tp8", 8)])
+                                    ("mixtral", 4096), ("qwen3_tp8", 8), ("dsv3", 8192)])
 def test_tile_plan(name, T):
     """The device-side tile plan (segments, tile prefixes, split-K pieces, layouts)
     is an integer function of the dispatch counts: recomputed here from the rules
@@ -171,8 +171,11 @@ def test_tile_plan(name, T):
     st_wide = sum(2 * cdiv(m, 256) for m in live)
     wide_dn = n_wide > 0 and 2 * n_wide >= n_chunks
     wide_gu = st_narrow > 0 and 8 * st_wide <= 9 * st_narrow
-    tr_gu, nj_gu = (256, cdiv(cfg.I, 64)) if wide_gu else (128, cdiv(cfg.I, 128))
-    gu = [cdiv(m, tr_gu) * nj_gu for m in ms]
+    # gate/up tiles per segment: wide (64+64 rows by <= 256 tokens) above
+    # wide_above rows, else 128+128 rows by <= 128 tokens
+    wide_above = 0 if wide_gu else (1 << 30 if max(ms) <= 16 else 1024)
+    gu = [cdiv(m, 256) * cdiv(cfg.I, 64) if m > wide_above else cdiv(m, 128) * cdiv(cfg.I, 128)
+          for m in ms]
     dn = [cdiv(m, 256) * cdiv(cfg.H, 128) for m in ms]
     pref = lambda v: np.concatenate([[0], np.cumsum(v)]).astype(int).tolist()
     nsm = torch.cuda.get_device_properties(0).multi_processor_count
