@@ -43,6 +43,10 @@ def parse():
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-tokens", type=int, default=48)
+    p.add_argument("--op", default="layer", choices=["layer", "reshard"],
+                   help="layer: the MoE layer forward (default); reshard: the EP<->TP "
+                        "expert-weight permute of one rank's experts")
+    p.add_argument("--tp", type=int, default=8, help="--op reshard: ranks P of the switch")
     return p.parse_args()
 
 
@@ -333,6 +337,18 @@ def run_gpu(args):
     if st != moe.MOE_OK:
         raise RuntimeError(f"device status {st} raw={raw:#x}")
 
+    # ---- the same K steps once more with an event between consecutive
+    # forwards only: the spread of single-step times (p10 / p50 / p90) ----
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    step_ev[0].record(stream)
+    for i in range(args.steps):
+        moe.moe_layer_forward(d, wts, inp.x, y, ws)
+        step_ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    step_us = sorted(1e3 * step_ev[i].elapsed_time(step_ev[i + 1]) for i in range(args.steps))
+    pct = lambda q: step_us[min(len(step_us) - 1, int(q * (len(step_us) - 1) + 0.5))]
+    step_spread = {"p10": pct(0.1), "p50": pct(0.5), "p90": pct(0.9)}
+
     stage_ms = {n: 0.0 for n in moe.STAGE_NAMES}
     for ev in stage_ev:
         for j, n in enumerate(moe.STAGE_NAMES):
@@ -427,6 +443,7 @@ def run_gpu(args):
                            "hbm_peak_gbs": pk["hbm_gbs"],
                            "tc_peak_tflops": pk["bf16_tflops_sustained"]},
         "stages_us": stage_us,
+        "step_us_spread": step_spread,
         "routing": {"imbalance_ratio": num / den, "touched_experts": alg["touched"]},
         "e2e": {"value": world * T * e_steps / (e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": T * cfg.H * 2, "d2h_bytes_per_step": T * cfg.H * 2},
@@ -461,8 +478,90 @@ def kernel_sources_sha():
     return h.hexdigest()[:16]
 
 
+def run_reshard(args):
+    """EP <-> TP expert-weight reshard permute of one rank's E/P experts of the
+    configuration (Moebius, section 3.1 "Weights Resharding"): pack (EP ->
+    per-peer chunks) then unpack (chunks -> EP), each step both directions;
+    HBM-bound, every byte read once and written once per direction."""
+    import torch
+    import synth
+    import routed_expert_ffn_gb300 as moe
+    from routed_expert_ffn_gb300 import build
+    build.build()
+    cfg = synth.CONFIGS[args.config]
+    P = args.tp
+    E_l = max(1, (args.E or cfg.E) // P)
+    H, I = cfg.H, cfg.I
+    g = torch.Generator(device="cuda").manual_seed(args.seed)
+    w13 = torch.randint(-32768, 32767, (E_l, 2 * I, H), dtype=torch.int16, device="cuda",
+                        generator=g)
+    w2 = torch.randint(-32768, 32767, (E_l, H, I), dtype=torch.int16, device="cuda", generator=g)
+    c13 = torch.empty((P, E_l, 2 * I // P, H), dtype=torch.int16, device="cuda")
+    c2 = torch.empty((P, E_l, H, I // P), dtype=torch.int16, device="cuda")
+    b13, b2 = torch.empty_like(w13), torch.empty_like(w2)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        moe.moe_reshard_ep_to_tp_pack(E_l, H, I, P, w13, w2, c13, c2)
+        moe.moe_reshard_tp_to_ep_unpack(E_l, H, I, P, c13, c2, b13, b2)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if not (torch.equal(b13, w13) and torch.equal(b2, w2)):
+        raise RuntimeError("reshard round trip changed the weights")
+    uuid = "GPU-" + str(torch.cuda.get_device_properties(0).uuid)
+    sampler = ClockSampler(uuid)
+    time.sleep(0.5)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    sampler.stop()
+    ms = a.elapsed_time(b) / args.steps
+    weight_bytes = (w13.numel() + w2.numel()) * 2
+    moved = 2 * 2 * weight_bytes  # two directions, each reads and writes every byte
+    gbs = moved / (ms * 1e-3) / 1e9
+    pk = peaks()
+    # the oracle's permutation (numpy) on the host, same shapes, one direction each
+    import oracle
+    h13, h2 = w13.cpu().numpy(), w2.cpu().numpy()
+    c0 = time.time()
+    p13, p2 = oracle.reshard_pack(h13, h2, P)
+    oracle.reshard_unpack(p13, p2, P)
+    cpu_s = time.time() - c0
+    line = {"metric": "EP<->TP expert-weight reshard permute, GB/s moved (read + write)",
+            "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (bit copies)",
+            "data": "synthetic (random 16-bit patterns)",
+            "config": {"workload": f"{cfg.name} EP->TP->EP reshard of one rank, P={P}",
+                       "E_local": E_l, "H": H, "I": I, "P": P,
+                       "weight_bytes": weight_bytes,
+                       "l2": "inputs larger than L2" if weight_bytes > (129 << 20)
+                             else "inputs smaller than L2"},
+            "roofline": {"bound": "hbm", "kernel": "reshard_kernel (pack + unpack)",
+                         "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / pk["hbm_gbs"], "traffic": None,
+                         "peak_source": pk["source"]},
+            "cpu_baseline": {"value": moved / cpu_s / 1e9, "unit": "GB/s", "cores": 1,
+                             "kind": "oracle",
+                             "sample": "one pack and one unpack of the same tensors (numpy)"},
+            "gpu_launches": 2 * args.steps,
+            "clocks": sampler.summary(t0, t1)}
+    print(json.dumps(line))
+
+
 def main():
     args = parse()
+    if args.op == "reshard":
+        run_reshard(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -312,6 +312,45 @@ moe_status_t moe_build_dispatch_noalloc(const moe_layer_desc_t *d, const int32_t
                                         int32_t *perm_src, int32_t *inv_pos, float *w_perm,
                                         int32_t *device_status, moe_stream_t stream);
 
+/*
+ * moe_reshard_ep_to_tp_pack -- the local permute of an expert-weight switch
+ * from expert parallelism to tensor parallelism (Moebius, section 3.1 "Weights
+ * Resharding" and Figure 4: EP -> TP packs each rank's complete experts into
+ * one contiguous chunk per peer, so that one all-to-all delivers every peer
+ * its shard of every expert already in the TP layout).  Under EP a rank owns
+ * E_local complete experts; under TP each of the P ranks owns an I/P slice of
+ * the intermediate dimension of every expert.
+ *   w13        [E_local, 2I, H] bf16 in (rows [0,I) gate, [I,2I) up)
+ *   w2         [E_local, H, I] bf16 in
+ *   w13_chunks [P, E_local, 2I/P, H] bf16 out: chunk p of expert e holds gate
+ *              rows [p*I/P, (p+1)*I/P), then up rows [I + p*I/P,
+ *              I + (p+1)*I/P): a W13 of intermediate size I/P, gate first
+ *   w2_chunks  [P, E_local, H, I/P] bf16 out: columns [p*I/P, (p+1)*I/P)
+ *              of every row of W2
+ * Either tensor may be skipped by passing NULL for both its input and its
+ * output.  Every element is copied once (a pure permutation: bit-exact).
+ * Limits: 1 <= P <= I, I % P == 0, (I/P) % 8 == 0, H % 8 == 0, E_local >= 1,
+ * and each tensor below 2^35 bytes; otherwise MOE_ERR_UNSUPPORTED_SHAPE.
+ * Pointers 16-byte aligned and the outputs not overlapping the inputs
+ * (MOE_ERR_INVALID_ARG otherwise).  Asynchronous on `stream`; the caller
+ * owns every buffer.
+ */
+moe_status_t moe_reshard_ep_to_tp_pack(int32_t E_local, int32_t H, int32_t I, int32_t P,
+                                       const void *w13, const void *w2, void *w13_chunks,
+                                       void *w2_chunks, moe_stream_t stream);
+
+/*
+ * moe_reshard_tp_to_ep_unpack -- the inverse local permute (TP -> EP:
+ * Moebius, same section -- the all-to-all first delivers, from every peer q,
+ * q's shard of this rank's E_local experts; the local permute then
+ * interleaves the shards into complete experts).  Inputs in the chunk layout
+ * of moe_reshard_ep_to_tp_pack (chunk index = the peer the shard came from),
+ * outputs in the EP layout; the same limits.  unpack(pack(W)) == W exactly.
+ */
+moe_status_t moe_reshard_tp_to_ep_unpack(int32_t E_local, int32_t H, int32_t I, int32_t P,
+                                         const void *w13_chunks, const void *w2_chunks,
+                                         void *w13, void *w2, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

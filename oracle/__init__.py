@@ -202,3 +202,50 @@ def layer(inputs, tokens: Optional[Sequence[int]] = None, nthreads: int = 0):
     y = layer_tokens(inputs.x, r["ids"], r["w"], inputs.w13, inputs.w2, list(tokens),
                      inputs.w13_shared, inputs.w2_shared, nthreads)
     return y, r
+
+
+# ------------------------------------------------- EP <-> TP weight reshard --
+# Moebius, section 3.1 "Weights Resharding" and Figure 4.  Under expert
+# parallelism a rank holds E_l complete experts, W13 [E_l, 2I, H] (gate rows
+# [0,I), up rows [I,2I)) and W2 [E_l, H, I]; under tensor parallelism each of P
+# ranks holds slice p of the intermediate dimension of every expert.  The
+# EP -> TP local permute packs one chunk per peer: chunk p of expert e is
+# W13 rows (gate slice p, then up slice p) and W2 columns slice p.  Written as
+# the index permutation itself (reshape + transpose; no arithmetic), on any
+# element type.
+
+def reshard_pack(w13, w2, P: int):
+    """EP -> TP: (w13 [E_l,2I,H], w2 [E_l,H,I]) -> (w13_chunks [P,E_l,2I/P,H],
+    w2_chunks [P,E_l,H,I/P]); either may be None."""
+    c13 = c2 = None
+    if w13 is not None:
+        a = np.asarray(w13)
+        E_l, two_i, H = a.shape
+        Ip = two_i // 2 // P
+        # [e][g][p][r][h] -> [p][e][g][r][h]
+        c13 = np.ascontiguousarray(
+            a.reshape(E_l, 2, P, Ip, H).transpose(2, 0, 1, 3, 4).reshape(P, E_l, 2 * Ip, H))
+    if w2 is not None:
+        a = np.asarray(w2)
+        E_l, H, I = a.shape
+        # [e][h][p][c] -> [p][e][h][c]
+        c2 = np.ascontiguousarray(a.reshape(E_l, H, P, I // P).transpose(2, 0, 1, 3))
+    return c13, c2
+
+
+def reshard_unpack(w13_chunks, w2_chunks, P: int):
+    """TP -> EP: the inverse of reshard_pack (chunk index = source peer)."""
+    w13 = w2 = None
+    if w13_chunks is not None:
+        a = np.asarray(w13_chunks)
+        _, E_l, two_ip, H = a.shape
+        Ip = two_ip // 2
+        # [p][e][g][r][h] -> [e][g][p][r][h]
+        w13 = np.ascontiguousarray(
+            a.reshape(P, E_l, 2, Ip, H).transpose(1, 2, 0, 3, 4).reshape(E_l, 2 * P * Ip, H))
+    if w2_chunks is not None:
+        a = np.asarray(w2_chunks)
+        _, E_l, H, Ip = a.shape
+        # [p][e][h][c] -> [e][h][p][c]
+        w2 = np.ascontiguousarray(a.transpose(1, 2, 0, 3).reshape(E_l, H, P * Ip))
+    return w13, w2

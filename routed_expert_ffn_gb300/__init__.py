@@ -89,6 +89,8 @@ def library() -> ctypes.CDLL:
         "moe_grouped_swiglu_ffn": ([D, P, P, P, P, P, P, P, P, P, P, S, P], I32),
         "moe_combine": ([D, P, P, P, P, P], I32),
         "moe_layer_forward": ([D, ctypes.POINTER(LayerWeights), P, P, P, S, P, P], I32),
+        "moe_reshard_ep_to_tp_pack": ([I32, I32, I32, I32, P, P, P, P, P], I32),
+        "moe_reshard_tp_to_ep_unpack": ([I32, I32, I32, I32, P, P, P, P, P], I32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -199,6 +201,23 @@ def moe_grouped_swiglu_ffn(d: LayerDesc, x, perm_src, offsets, w_perm, w13, w2, 
 def moe_combine(d: LayerDesc, out_perm, inv_pos, topk_w, y, stream=None):
     _check("moe_combine", library().moe_combine(
         ctypes.byref(d), _ptr(out_perm), _ptr(inv_pos), _ptr(topk_w), _ptr(y), _stream(stream)))
+
+
+def moe_reshard_ep_to_tp_pack(E_local: int, H: int, I: int, P: int, w13, w2, w13_chunks,
+                              w2_chunks, stream=None):
+    """EP -> TP local permute: [E_l,2I,H] / [E_l,H,I] -> per-peer chunks
+    [P,E_l,2I/P,H] / [P,E_l,H,I/P] (either pair may be None)."""
+    _check("moe_reshard_ep_to_tp_pack", library().moe_reshard_ep_to_tp_pack(
+        E_local, H, I, P, _ptr(w13), _ptr(w2), _ptr(w13_chunks), _ptr(w2_chunks),
+        _stream(stream)))
+
+
+def moe_reshard_tp_to_ep_unpack(E_local: int, H: int, I: int, P: int, w13_chunks, w2_chunks, w13,
+                                w2, stream=None):
+    """TP -> EP local permute, the inverse of moe_reshard_ep_to_tp_pack."""
+    _check("moe_reshard_tp_to_ep_unpack", library().moe_reshard_tp_to_ep_unpack(
+        E_local, H, I, P, _ptr(w13_chunks), _ptr(w2_chunks), _ptr(w13), _ptr(w2),
+        _stream(stream)))
 
 
 def layer_weights(w_router, w13, w2, sel_bias=None, w13_shared=None, w2_shared=None) -> LayerWeights:

@@ -364,4 +364,49 @@ moe_status_t moe_layer_forward(const moe_layer_desc_t *d, const moe_layer_weight
   return cuda_status(e);
 }
 
+// Shared checks of the two reshard calls (the two directions take the same
+// shapes; src/dst are the inputs/outputs of the call).
+static moe_status_t reshard_checks(int32_t E_local, int32_t H, int32_t I, int32_t P,
+                                   const void *src13, const void *src2, const void *dst13,
+                                   const void *dst2) {
+  if ((src13 == nullptr) != (dst13 == nullptr) || (src2 == nullptr) != (dst2 == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (src13 == nullptr && src2 == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!ok_opt(src13) || !ok_opt(src2) || !ok_opt(dst13) || !ok_opt(dst2))
+    return MOE_ERR_INVALID_ARG;
+  if (E_local < 1 || H < 8 || I < 8 || P < 1 || H % 8 != 0 || I % P != 0 || (I / P) % 8 != 0)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  const int64_t bytes = (int64_t)E_local * 2 * I * H * 2;  // W13; W2 is half of it
+  if (bytes >= (int64_t)1 << 35) return MOE_ERR_UNSUPPORTED_SHAPE;
+  auto overlap = [](const void *a, int64_t na, const void *b, int64_t nb) {
+    if (a == nullptr || b == nullptr) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + (uintptr_t)nb && y < x + (uintptr_t)na;
+  };
+  const int64_t b13 = bytes, b2 = bytes / 2;
+  if (overlap(src13, b13, dst13, b13) || overlap(src13, b13, dst2, b2) ||
+      overlap(src2, b2, dst13, b13) || overlap(src2, b2, dst2, b2) ||
+      overlap(dst13, b13, dst2, b2))
+    return MOE_ERR_INVALID_ARG;
+  return check_device();
+}
+
+moe_status_t moe_reshard_ep_to_tp_pack(int32_t E_local, int32_t H, int32_t I, int32_t P,
+                                       const void *w13, const void *w2, void *w13_chunks,
+                                       void *w2_chunks, moe_stream_t stream) {
+  moe_status_t st = reshard_checks(E_local, H, I, P, w13, w2, w13_chunks, w2_chunks);
+  if (st != MOE_OK) return st;
+  return cuda_status(launch_reshard(E_local, H, I, P, w13, w13_chunks, w2, w2_chunks, 0,
+                                   (cudaStream_t)stream));
+}
+
+moe_status_t moe_reshard_tp_to_ep_unpack(int32_t E_local, int32_t H, int32_t I, int32_t P,
+                                         const void *w13_chunks, const void *w2_chunks,
+                                         void *w13, void *w2, moe_stream_t stream) {
+  moe_status_t st = reshard_checks(E_local, H, I, P, w13_chunks, w2_chunks, w13, w2);
+  if (st != MOE_OK) return st;
+  return cuda_status(launch_reshard(E_local, H, I, P, w13_chunks, w13, w2_chunks, w2, 1,
+                                   (cudaStream_t)stream));
+}
+
 }  // extern "C"

@@ -38,7 +38,12 @@ constexpr int kSplitCounterWord = 64;  // first split-K counter
 // list (a multiple of the block size, chosen so there are at most
 // kDispatchMaxBlocks blocks).
 constexpr int kDispatchThreads = 256;
-constexpr int64_t kSmallDispatch = 2048;  // N_a up to this: one-block dispatch
+// (measured: raising it to 8192 made the dispatch 23 us slower at
+// T*k = 8192, where three launches overlap through PDL)
+#ifndef MOE_SMALL_DISPATCH
+#define MOE_SMALL_DISPATCH 2048
+#endif
+constexpr int64_t kSmallDispatch = MOE_SMALL_DISPATCH;  // N_a up to this: one-block dispatch
 constexpr int kDispatchMaxBlocks = 1024;
 inline int64_t dispatch_chunk(int64_t Na) {
   int64_t c = (Na + kDispatchMaxBlocks - 1) / kDispatchMaxBlocks;
@@ -150,7 +155,11 @@ cudaError_t launch_dispatch(const int32_t *ids, const float *topk_w, int T, int 
 // inv_pos may be null: then one warp per x_perm row (the standalone FFN call,
 // and layer forwards whose x is at most kGatherByTokenBytes).  plan may be
 // null (the dispatch wrote it); otherwise one more block writes it.
-constexpr int64_t kGatherByTokenBytes = 8ll << 20;
+// (measured: a 4 MB threshold made the Qwen3 T=1024 forward 5 us slower)
+#ifndef MOE_GATHER_TOKEN_KB
+#define MOE_GATHER_TOKEN_KB 8192
+#endif
+constexpr int64_t kGatherByTokenBytes = (int64_t)MOE_GATHER_TOKEN_KB << 10;
 cudaError_t launch_gather_plan(const __nv_bfloat16 *x, const int32_t *perm_src,
                                const int32_t *inv_pos, const int32_t *offsets, int T, int k, int E,
                                int H, int I, int shared, __nv_bfloat16 *x_perm, int32_t *plan,
@@ -170,6 +179,10 @@ cudaError_t launch_expert_down(const moe_layer_desc_t &d, const void *w2, const 
 cudaError_t launch_combine(const __half *out_perm, const int32_t *inv_pos,
                            const float *topk_w, int T, int k, int H, int shared, __nv_bfloat16 *y,
                            cudaStream_t s);
+// EP <-> TP expert-weight reshard permute (reshard.cu); a null source skips
+// that tensor.  unpack = 0: EP layout -> per-peer chunks; 1: the inverse.
+cudaError_t launch_reshard(int E_local, int H, int I, int P, const void *w13_src, void *w13_dst,
+                           const void *w2_src, void *w2_dst, int unpack, cudaStream_t st);
 
 int num_sms();  // of the current device (cached)
 
