@@ -18,6 +18,13 @@ namespace moe {
 
 namespace {
 
+// Router K-split partials loaded per batch by the gating kernel (measured:
+// 8 takes 2-5 us off the route at T = 1024..2048 against 4).
+#ifndef MOE_TOPK_BATCH
+#define MOE_TOPK_BATCH 8
+#endif
+constexpr int kTopkSplitBatch = MOE_TOPK_BATCH;
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -125,19 +132,20 @@ __global__ void __launch_bounds__(256) topk_gating_kernel(
   float s[NV];
 #pragma unroll
   for (int i = 0; i < NV; ++i) s[i] = 0.f;
-  // sum the router's K-split partials in split order; four splits' loads are
-  // issued together
-  for (int z0 = 0; z0 < splits; z0 += 4) {
-    float p[NV][4];
+  // sum the router's K-split partials in split order; kTopkSplitBatch
+  // splits' loads are issued together
+  constexpr int kB = kTopkSplitBatch;
+  for (int z0 = 0; z0 < splits; z0 += kB) {
+    float p[NV][kB];
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
+    for (int u = 0; u < kB; ++u)
 #pragma unroll
       for (int i = 0; i < NV; ++i) {
         const int e = lane + 32 * i;
         p[i][u] = (e < E && z0 + u < splits) ? partial[((size_t)(z0 + u) * T + t) * E + e] : 0.f;
       }
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
+    for (int u = 0; u < kB; ++u)
 #pragma unroll
       for (int i = 0; i < NV; ++i) s[i] += p[i][u];
   }
