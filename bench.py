@@ -528,6 +528,15 @@ def run_reshard(args):
     moved = 2 * 2 * weight_bytes  # two directions, each reads and writes every byte
     gbs = moved / (ms * 1e-3) / 1e9
     pk = peaks()
+    # DRAM bytes of one step (pack + unpack) from an ncu capture of the same
+    # kernel sources, if one is recorded
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        with open(prof) as f:
+            tr = json.load(f).get(f"reshard_{cfg.name}_P{P}")
+        if tr and tr.get("kernel_sources_sha") == kernel_sources_sha():
+            traffic = tr["step_dram_bytes"]
     # the oracle's permutation (numpy) on the host, same shapes, one direction each
     import oracle
     h13, h2 = w13.cpu().numpy(), w2.cpu().numpy()
@@ -547,7 +556,7 @@ def run_reshard(args):
                              else "inputs smaller than L2"},
             "roofline": {"bound": "hbm", "kernel": "reshard_kernel (pack + unpack)",
                          "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": gbs / pk["hbm_gbs"], "traffic": None,
+                         "frac": gbs / pk["hbm_gbs"], "traffic": traffic,
                          "peak_source": pk["source"]},
             "cpu_baseline": {"value": moved / cpu_s / 1e9, "unit": "GB/s", "cores": 1,
                              "kind": "oracle",
