@@ -139,7 +139,9 @@ typedef struct {
                         *                      down: 0 = narrow, 1 = wide,
                         *                      2 = thin (every segment has
                         *                      at most 16 rows), 3 = medium
-                        *                      (down only: at most 64) */
+                        *                      (down only: at most 64), 4 =
+                        *                      pair (down only: 256 W2 rows
+                        *                      by <= 128 token rows) */
   size_t total;        /* == moe_workspace_size(desc)                     */
 } moe_workspace_layout_t;
 

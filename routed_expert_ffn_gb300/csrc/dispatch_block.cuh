@@ -127,6 +127,10 @@ static __device__ void write_tile_plan(const int32_t *__restrict__ offsets, int 
   const bool wide_dn = n_wide > 0 && 2 * n_wide >= n_chunks;
   const bool wide_gu = st_narrow > 0 && 8 * st_wide <= 9 * st_narrow;
   const bool thin_all = max_m <= kThinRows;
+  const bool medium_all = max_m <= kMediumRows;
+  // down, where it would otherwise be narrow: "pair" tiles of 256 W2 rows by
+  // <= 128 token rows (H >= 256)
+  const bool pair_dn = kDownPair && !thin_all && !medium_all && !wide_dn && H >= 2 * kBM;
   // gate/up segments above this many rows take wide tiles
   const int wide_above = wide_gu ? 0 : (thin_all ? (1 << 30) : kGateUpWideAbove);
   int gu[kPer], dn[kPer], sum_gu = 0, sum_dn = 0;
@@ -136,7 +140,8 @@ static __device__ void write_tile_plan(const int32_t *__restrict__ offsets, int 
                 ? (ms[q] + kTileRowsDown - 1) / kTileRowsDown *
                       ((I + kGateUpColsWide - 1) / kGateUpColsWide)
                 : (ms[q] + kTileRowsGateUp - 1) / kTileRowsGateUp * ((I + kBM - 1) / kBM);
-    dn[q] = (ms[q] + kTileRowsDown - 1) / kTileRowsDown * nj_dn;
+    dn[q] = pair_dn ? (ms[q] + kBM - 1) / kBM * ((H + 2 * kBM - 1) / (2 * kBM))
+                    : (ms[q] + kTileRowsDown - 1) / kTileRowsDown * nj_dn;
     sum_gu += gu[q];
     sum_dn += dn[q];
   }
@@ -165,8 +170,9 @@ static __device__ void write_tile_plan(const int32_t *__restrict__ offsets, int 
     plan[3 * (nseg + 1) + 2] = thin ? 2 : (wide_gu ? 1 : 0);
     // down only: 3 = medium (every tile <= 64 token rows: stages of 64 rows,
     // four in flight; measured 2% faster than narrow there, and far slower
-    // once hot experts reload their weights per 64-row unit)
-    plan[3 * (nseg + 1) + 3] = thin ? 2 : (max_m <= kMediumRows ? 3 : (wide_dn ? 1 : 0));
+    // once hot experts reload their weights per 64-row unit); 4 = pair
+    plan[3 * (nseg + 1) + 3] =
+        thin ? 2 : (medium_all ? 3 : (wide_dn ? 1 : (pair_dn ? 4 : 0)));
   }
 }
 

@@ -151,10 +151,12 @@ __device__ __forceinline__ bool epi_all(bool p) {
 
 // Gate/up tiles are wide (64 + 64 rows of W13 by <= 256 token rows) in
 // segments of more than `wide_above` rows, else 128 + 128 rows by <= 128
-// token rows; down tiles are 128 rows of W2 by <= 256 token rows.
+// token rows; down tiles are 128 rows of W2 by <= 256 token rows, or in the
+// pair layout 256 rows by <= 128 (dn_rows = token rows per down tile).
 template <bool kGateUp>
-__device__ __forceinline__ Tile decode_tile(int tile, int wide_above, const int32_t *seg_row,
-                                            const int32_t *pref, int nseg) {
+__device__ __forceinline__ Tile decode_tile(int tile, int wide_above, int dn_rows,
+                                            const int32_t *seg_row, const int32_t *pref,
+                                            int nseg) {
   int lo = 0, hi = nseg;  // pref[lo] <= tile < pref[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -168,7 +170,7 @@ __device__ __forceinline__ Tile decode_tile(int tile, int wide_above, const int3
   const int local = tile - pref[lo];
   const int m = seg_row[lo + 1] - seg_row[lo];
   t.wide = kGateUp && m > wide_above;
-  const int rows = (kGateUp && !t.wide) ? kTileRowsGateUp : kTileRowsDown;
+  const int rows = kGateUp ? (t.wide ? kTileRowsDown : kTileRowsGateUp) : dn_rows;
   const int chunks = (m + rows - 1) / rows;
   t.j = local / chunks;
   const int c = local - t.j * chunks;
@@ -248,10 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 4 && lane == 0) {
     tma_prefetch_desc(&tm_a);
     tma_prefetch_desc(&tm_a_sh);
-    if (kGateUp) {
-      tma_prefetch_desc(&tm_aw);
-      tma_prefetch_desc(&tm_aw_sh);
-    }
+    tma_prefetch_desc(&tm_aw);
+    tma_prefetch_desc(&tm_aw_sh);
     for (int i = 0; i < 16; ++i) tma_prefetch_desc(&tm_b.m[i]);
   }
   // Everything above is independent of earlier kernels' outputs.  With
@@ -289,6 +289,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool wide = layout == 1;
   const bool thin = layout == 2;    // every tile <= kThinRows token rows
   const bool medium = layout == 3;  // down: stages of 64 token rows
+  // down, pair: 256 W2 rows (two 128-row halves) by <= 128 token rows
+  const bool pair = !kGateUp && layout == 4;
+  const int dn_rows = pair ? kBM : kTileRowsDown;  // token rows per down tile
   // token rows per stage: a down tile runs one stage per unit of this many
   // rows (gate/up tiles always fit one stage)
   const int unit_rows =
@@ -302,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t U = C::STAGE_UNIT;
   const uint32_t stage_bytes =
       kGateUp ? (thin ? 2 * U + kThinB : 3 * U)
-              : U + (thin ? kThinB : medium ? U / 2 : (wide ? 2 : 1) * U);
+              : (pair ? 3 * U : U + (thin ? kThinB : medium ? U / 2 : (wide ? 2 : 1) * U));
   const uint32_t nst = kRingBytes / stage_bytes;
   tc_fence_before();
   __syncthreads();
@@ -345,14 +348,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       for (int pc = blockIdx.x; ok && pc < total_pieces; pc += gridDim.x) {
         const int tile = pc / S, z = pc - tile * S;
-        const Tile t = decode_tile<kGateUp>(tile, wide_above, seg_row, pref, nseg);
+        const Tile t = decode_tile<kGateUp>(tile, wide_above, dn_rows, seg_row, pref, nseg);
         const int kb0 = z * kbs, kb1 = min(nkb, kb0 + kbs);
         const bool sh = (t.seg >= E);
-        const CUtensorMap *ma = t.wide ? (sh ? &tm_aw_sh : &tm_aw) : (sh ? &tm_a_sh : &tm_a);
+        // gate/up wide tiles and down pair tiles take the second pair of maps
+        // (64-row and 256-row boxes)
+        const CUtensorMap *ma =
+            (t.wide || pair) ? (sh ? &tm_aw_sh : &tm_aw) : (sh ? &tm_a_sh : &tm_a);
         const int ecoord = sh ? 0 : t.seg;
         // this tile's weight bytes per stage (and offset of its token rows)
-        const uint32_t stage_a = (kGateUp && !t.wide) ? 2 * U : U;
-        const int arow = t.j * (t.wide ? kGateUpColsWide : kBM);
+        const bool two = (kGateUp && !t.wide) || pair;  // two 128-row A halves
+        const uint32_t stage_a = two ? 2 * U : U;
+        const int arow = t.j * (t.wide ? kGateUpColsWide : (pair ? 2 * kBM : kBM));
         const int n16 = (t.nrows + 15) & ~15;       // token rows, padded to 16
         const int nu = (n16 + unit_rows - 1) / unit_rows;  // stages per K step
         for (int kb = kb0; ok && kb < kb1; kb += kStageKB) {
@@ -409,11 +416,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int pc = blockIdx.x; ok && pc < total_pieces; pc += gridDim.x, ++tl) {
         const int tile = pc / S, z = pc - tile * S;
-        const Tile t = decode_tile<kGateUp>(tile, wide_above, seg_row, pref, nseg);
+        const Tile t = decode_tile<kGateUp>(tile, wide_above, dn_rows, seg_row, pref, nseg);
         const int kb0 = z * kbs, kb1 = min(nkb, kb0 + kbs);
         const int n16 = (t.nrows + 15) & ~15;
         const int nu = (n16 + unit_rows - 1) / unit_rows;
-        const uint32_t stage_a = (kGateUp && !t.wide) ? 2 * U : U;  // this tile's weights
+        const bool two = (kGateUp && !t.wide) || pair;  // two 128-row A halves
+        const uint32_t stage_a = two ? 2 * U : U;          // this tile's weights
         const uint32_t chunk_a = stage_a / kStageKB;                   // per K block
         // token column n -> accumulator column n (a wide down tile in the
         // narrow layout as two 128-row units); gate/up, narrow: gate rows ->
@@ -440,9 +448,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t acc = (kb != kb0 || c != 0) ? 1u : 0u;
               const uint64_t ac = adesc + c * (chunk_a >> 4);
               const uint64_t bc = bdesc + c * ((uint32_t)hb * (kBK * 2) >> 4);
-              if (kGateUp && !t.wide) {
-                umma_kblock(d0, ac, bc, id, acc);                              // gate
-                umma_kblock(d0 + 128, ac + (kChunkBytes >> 4), bc, id, acc);  // up
+              if (two) {
+                // gate/up: gate rows, up rows; down pair: W2 rows [0,128), [128,256)
+                umma_kblock(d0, ac, bc, id, acc);
+                umma_kblock(d0 + 128, ac + (kChunkBytes >> 4), bc, id, acc);
               } else {
                 // one MMA over all of the stage's token rows (N <= 256)
                 umma_kblock(d0 + (uint32_t)(u * unit_rows), ac, bc, id, acc);
@@ -473,7 +482,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = warp * 32 + lane;  // TMEM lane = weight row of the tile
     uint32_t tl = 0, slice = 0;
     bool range_bad = false;
-    auto emit16 = [&](const Tile &t, int n0, const float(&g)[16], const float(&u)[16]) {
+    auto emit16 = [&](const Tile &t, int n0, int col0, const float(&g)[16],
+                      const float(&u)[16]) {
       uint16_t *so = sOut + (slice & 1u) * (16 * kBM);
 #pragma unroll
       for (int q = 0; q < 16; ++q) {
@@ -489,7 +499,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       epi_sync();
       // 16 token rows x 128 columns x 2 bytes = 256 chunks of 16 bytes
-      const int col0 = t.j * kBM;
       for (int c = r; c < 16 * (kBM / 8); c += 128) {
         const int q = c / (kBM / 8), ch = c % (kBM / 8);
         const int n = n0 + q, col = col0 + ch * 8;
@@ -531,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kSlot = (kGateUp ? 2 : 1) * kBM * kSplitMaxRows;
     for (int pc = blockIdx.x; pc < total_pieces; pc += gridDim.x, ++tl) {
       const int tile = pc / S, z = pc - tile * S;
-      const Tile t = decode_tile<kGateUp>(tile, wide_above, seg_row, pref, nseg);
+      const Tile t = decode_tile<kGateUp>(tile, wide_above, dn_rows, seg_row, pref, nseg);
       const uint32_t buf = tl & 1u, use = tl >> 1;
       const bool waited = mbar_wait(&tfull[buf], use & 1u, abort_flag, status, kCode);
       // one decision for all 128 epilogue threads: they share named barriers
@@ -562,18 +571,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       if (S == 1) {
-        for (int n0 = 0; n0 < N; n0 += 16) {
-          uint32_t v0[16], v1[16];
-          tmem_ld16(tb + n0, v0);
-          if (kGateUp) tmem_ld16(tb + 128 + n0, v1);
-          tmem_ld_wait();
-          float g[16], u[16];
+        // down pair: the second 128-row half's columns follow at +128
+        for (int h = 0; h < (pair ? 2 : 1); ++h) {
+          const int col0 = pair ? t.j * 2 * kBM + h * kBM : t.j * kBM;
+          for (int n0 = 0; n0 < N; n0 += 16) {
+            uint32_t v0[16], v1[16];
+            tmem_ld16(tb + h * 128 + n0, v0);
+            if (kGateUp) tmem_ld16(tb + 128 + n0, v1);
+            tmem_ld_wait();
+            float g[16], u[16];
 #pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            g[q] = __uint_as_float(v0[q]);
-            u[q] = kGateUp ? __uint_as_float(v1[q]) : 0.f;
+            for (int q = 0; q < 16; ++q) {
+              g[q] = __uint_as_float(v0[q]);
+              u[q] = kGateUp ? __uint_as_float(v1[q]) : 0.f;
+            }
+            emit16(t, n0, col0, g, u);
           }
-          emit16(t, n0, g, u);
         }
         tc_fence_before();
         __syncwarp();
@@ -634,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        emit16(t, n0, g, u);
+        emit16(t, n0, t.j * kBM, g, u);
       }
     }
     if (range_bad) atomicOr(status, kStatusRange);
@@ -699,6 +712,14 @@ cudaError_t launch_gemm(const moe_layer_desc_t &d, const void *w, const void *w_
     if (!weight_map(&maw, w, K, rows, P, d.E, kGateUpColsWide)) return cudaErrorInvalidValue;
     if (shared) {
       if (!weight_map(&mawsh, w_sh, K, rows, P, 1, kGateUpColsWide)) return cudaErrorInvalidValue;
+    } else {
+      mawsh = maw;
+    }
+  } else if (d.H >= 2 * kBM) {
+    // down, pair layout: 256-row boxes
+    if (!weight_map(&maw, w, K, rows, P, d.E, 2 * kBM)) return cudaErrorInvalidValue;
+    if (shared) {
+      if (!weight_map(&mawsh, w_sh, K, rows, P, 1, 2 * kBM)) return cudaErrorInvalidValue;
     } else {
       mawsh = maw;
     }

@@ -73,6 +73,13 @@ constexpr int kGateUpWideAbove = MOE_GU_WIDE_ABOVE;
 #define MOE_STAGE_KB 2
 #endif
 constexpr int kStageKB = MOE_STAGE_KB;
+// The down GEMM's "pair" layout: where it would otherwise run narrow, tiles
+// of 256 W2 rows (two 128-row halves, two MMAs sharing the token operand) by
+// <= 128 token rows: 64 KB of weights per 96 KB stage instead of 32 of 64.
+#ifndef MOE_DOWN_PAIR
+#define MOE_DOWN_PAIR 1
+#endif
+constexpr bool kDownPair = MOE_DOWN_PAIR != 0;
 constexpr int kThinRows = 16;           // the thin layout: tiles of <= 16 token rows
 constexpr int kMediumRows = 64;         // the down GEMM's medium layout: <= 64 rows
 constexpr int kRingBytes = 204 * 1024;  // 3 thin gate/up stages of 68 KB
