@@ -141,7 +141,8 @@ typedef struct {
                         *                      at most 16 rows), 3 = medium
                         *                      (down only: at most 64), 4 =
                         *                      pair (down only: 256 W2 rows
-                        *                      by <= 128 token rows) */
+                        *                      by <= 128 token rows), 5 = thin
+                        *                      pair (down only) */
   size_t total;        /* == moe_workspace_size(desc)                     */
 } moe_workspace_layout_t;
 

@@ -130,7 +130,12 @@ static __device__ void write_tile_plan(const int32_t *__restrict__ offsets, int 
   const bool medium_all = max_m <= kMediumRows;
   // down, where it would otherwise be narrow: "pair" tiles of 256 W2 rows by
   // <= 128 token rows (H >= 256)
+  // (measured in place of wide as well: Mixtral T=4096 down 744 -> 827 us)
   const bool pair_dn = kDownPair && !thin_all && !medium_all && !wide_dn && H >= 2 * kBM;
+  // thin (decode) pairing only for a short down K (I <= 4096); measured:
+  // Qwen3 TP-8 slice (I = 192) down 3.6-10.6 us faster at T = 2..16, Qwen3
+  // (I = 1536) 1.5 us at T = 1, Mixtral (I = 14336) 3.5 us slower at T = 1
+  const bool thin_pair_dn = kDownThinPair && thin_all && H >= 2 * kBM && I <= 4096;
   // gate/up segments above this many rows take wide tiles
   const int wide_above = wide_gu ? 0 : (thin_all ? (1 << 30) : kGateUpWideAbove);
   int gu[kPer], dn[kPer], sum_gu = 0, sum_dn = 0;
@@ -140,7 +145,7 @@ static __device__ void write_tile_plan(const int32_t *__restrict__ offsets, int 
                 ? (ms[q] + kTileRowsDown - 1) / kTileRowsDown *
                       ((I + kGateUpColsWide - 1) / kGateUpColsWide)
                 : (ms[q] + kTileRowsGateUp - 1) / kTileRowsGateUp * ((I + kBM - 1) / kBM);
-    dn[q] = pair_dn ? (ms[q] + kBM - 1) / kBM * ((H + 2 * kBM - 1) / (2 * kBM))
+    dn[q] = (pair_dn || thin_pair_dn) ? (ms[q] + kBM - 1) / kBM * ((H + 2 * kBM - 1) / (2 * kBM))
                     : (ms[q] + kTileRowsDown - 1) / kTileRowsDown * nj_dn;
     sum_gu += gu[q];
     sum_dn += dn[q];
@@ -170,9 +175,10 @@ static __device__ void write_tile_plan(const int32_t *__restrict__ offsets, int 
     plan[3 * (nseg + 1) + 2] = thin ? 2 : (wide_gu ? 1 : 0);
     // down only: 3 = medium (every tile <= 64 token rows: stages of 64 rows,
     // four in flight; measured 2% faster than narrow there, and far slower
-    // once hot experts reload their weights per 64-row unit); 4 = pair
+    // once hot experts reload their weights per 64-row unit); 4 = pair;
+    // 5 = thin pair
     plan[3 * (nseg + 1) + 3] =
-        thin ? 2 : (medium_all ? 3 : (wide_dn ? 1 : (pair_dn ? 4 : 0)));
+        thin ? (thin_pair_dn ? 5 : 2) : (medium_all ? 3 : (pair_dn ? 4 : (wide_dn ? 1 : 0)));
   }
 }
 

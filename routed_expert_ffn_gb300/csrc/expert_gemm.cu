@@ -287,10 +287,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   //    128 rows + 64 token rows.
   const int layout = __ldcg(plan + 3 * (nseg + 1) + (kGateUp ? 2 : 3));
   const bool wide = layout == 1;
-  const bool thin = layout == 2;    // every tile <= kThinRows token rows
+  // every tile <= kThinRows token rows (down: 5 = thin pair)
+  const bool thin = layout == 2 || (!kGateUp && layout == 5);
   const bool medium = layout == 3;  // down: stages of 64 token rows
   // down, pair: 256 W2 rows (two 128-row halves) by <= 128 token rows
-  const bool pair = !kGateUp && layout == 4;
+  const bool pair = !kGateUp && (layout == 4 || layout == 5);
   const int dn_rows = pair ? kBM : kTileRowsDown;  // token rows per down tile
   // token rows per stage: a down tile runs one stage per unit of this many
   // rows (gate/up tiles always fit one stage)
@@ -305,7 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t U = C::STAGE_UNIT;
   const uint32_t stage_bytes =
       kGateUp ? (thin ? 2 * U + kThinB : 3 * U)
-              : (pair ? 3 * U : U + (thin ? kThinB : medium ? U / 2 : (wide ? 2 : 1) * U));
+              : (pair ? (thin ? 2 * U + kThinB : 3 * U)
+                      : U + (thin ? kThinB : medium ? U / 2 : (wide ? 2 : 1) * U));
   const uint32_t nst = kRingBytes / stage_bytes;
   tc_fence_before();
   __syncthreads();
@@ -536,8 +538,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++slice;
     };
     // floats of one split-K piece's partial (a split launch is never wide:
-    // the plan splits only when every tile has <= kSplitMaxRows rows)
-    constexpr int kSlot = (kGateUp ? 2 : 1) * kBM * kSplitMaxRows;
+    // the plan splits only when every tile has <= kSplitMaxRows rows); two
+    // accumulators for gate/up and for the down pair layouts
+    const bool two_acc = kGateUp || pair;
+    const int slot = (two_acc ? 2 : 1) * kBM * kSplitMaxRows;
     for (int pc = blockIdx.x; pc < total_pieces; pc += gridDim.x, ++tl) {
       const int tile = pc / S, z = pc - tile * S;
       const Tile t = decode_tile<kGateUp>(tile, wide_above, dn_rows, seg_row, pref, nseg);
@@ -594,18 +598,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       // ---- split-K piece (N <= kSplitMaxRows): fp32 partial to global ----
-      float *part = split_part + (size_t)(tile * S + z) * kSlot + (size_t)r * kSplitMaxRows;
+      float *part = split_part + (size_t)(tile * S + z) * slot + (size_t)r * kSplitMaxRows;
       for (int n0 = 0; n0 < N; n0 += 16) {
         uint32_t v0[16], v1[16];
         tmem_ld16(tb + n0, v0);
-        if (kGateUp) tmem_ld16(tb + 128 + n0, v1);
+        if (two_acc) tmem_ld16(tb + 128 + n0, v1);
         tmem_ld_wait();
 #pragma unroll
         for (int q = 0; q < 16; q += 4) {
           *reinterpret_cast<float4 *>(part + n0 + q) =
               make_float4(__uint_as_float(v0[q]), __uint_as_float(v0[q + 1]),
                           __uint_as_float(v0[q + 2]), __uint_as_float(v0[q + 3]));
-          if (kGateUp)
+          if (two_acc)
             *reinterpret_cast<float4 *>(part + kBM * kSplitMaxRows + n0 + q) =
                 make_float4(__uint_as_float(v1[q]), __uint_as_float(v1[q + 1]),
                             __uint_as_float(v1[q + 2]), __uint_as_float(v1[q + 3]));
@@ -630,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < 16; ++q) g[q] = u[q] = 0.f;
         for (int zz = 0; zz < S; ++zz) {
           const float *p =
-              split_part + (size_t)(tile * S + zz) * kSlot + (size_t)r * kSplitMaxRows + n0;
+              split_part + (size_t)(tile * S + zz) * slot + (size_t)r * kSplitMaxRows + n0;
 #pragma unroll
           for (int q = 0; q < 16; q += 4) {
             const float4 a = __ldcg(reinterpret_cast<const float4 *>(p + q));
@@ -638,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             g[q + 1] += a.y;
             g[q + 2] += a.z;
             g[q + 3] += a.w;
-            if (kGateUp) {
+            if (two_acc) {
               const float4 b = __ldcg(reinterpret_cast<const float4 *>(p + kBM * kSplitMaxRows + q));
               u[q] += b.x;
               u[q + 1] += b.y;
@@ -647,7 +651,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        emit16(t, n0, t.j * kBM, g, u);
+        if (pair) {
+          // the two 128-row halves of the W2 block, each its own columns
+          emit16(t, n0, t.j * 2 * kBM, g, u);
+          emit16(t, n0, t.j * 2 * kBM + kBM, u, g);
+        } else {
+          emit16(t, n0, t.j * kBM, g, u);
+        }
       }
     }
     if (range_bad) atomicOr(status, kStatusRange);

@@ -80,6 +80,12 @@ constexpr int kStageKB = MOE_STAGE_KB;
 #define MOE_DOWN_PAIR 1
 #endif
 constexpr bool kDownPair = MOE_DOWN_PAIR != 0;
+// The same pairing in the thin (decode) layout: stages of 64 KB of weights
+// + 16 token rows, three in flight (192 KB of weights instead of 160).
+#ifndef MOE_DOWN_THIN_PAIR
+#define MOE_DOWN_THIN_PAIR 1
+#endif
+constexpr bool kDownThinPair = MOE_DOWN_THIN_PAIR != 0;
 constexpr int kThinRows = 16;           // the thin layout: tiles of <= 16 token rows
 constexpr int kMediumRows = 64;         // the down GEMM's medium layout: <= 64 rows
 constexpr int kRingBytes = 204 * 1024;  // 3 thin gate/up stages of 68 KB

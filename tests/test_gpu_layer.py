@@ -179,19 +179,22 @@ def test_tile_plan(name, T):
     # down: "pair" tiles (256 W2 rows by <= 128 token rows) where the launch
     # would otherwise be narrow
     pair = max(ms) > 64 and not wide_dn and cfg.H >= 256
-    dn = [cdiv(m, 128) * cdiv(cfg.H, 256) if pair else cdiv(m, 256) * cdiv(cfg.H, 128)
-          for m in ms]
+    # the same tiles in the thin layout when the down K is short
+    thin_pair = max(ms) <= 16 and cfg.H >= 256 and cfg.I <= 4096
+    dn = [cdiv(m, 128) * cdiv(cfg.H, 256) if pair or thin_pair
+          else cdiv(m, 256) * cdiv(cfg.H, 128) for m in ms]
     pref = lambda v: np.concatenate([[0], np.cumsum(v)]).astype(int).tolist()
     nsm = torch.cuda.get_device_properties(0).multi_processor_count
     want = (seg_row + pref(gu) + pref(dn) +
             [_split_kbs(sum(gu), cfg.H // 64, nsm, max(ms)),
              _split_kbs(sum(dn), cfg.I // 64, nsm, max(ms))])
     # pipeline layouts: 2 = thin (every segment <= 16 rows), 3 = medium (down, <= 64),
-    # 1 = wide, 4 = pair (down), 0 = narrow
+    # 1 = wide, 4 = pair (down), 5 = thin pair (down), 0 = narrow
     thin = max(ms) <= 16
     medium = max(ms) <= 64
     want += [2 if thin else int(wide_gu),
-             2 if thin else (3 if medium else (1 if wide_dn else (4 if pair else 0)))]
+             (5 if thin_pair else 2) if thin else
+             (3 if medium else (1 if wide_dn else (4 if pair else 0)))]
     assert plan == want
     if name == "mixtral":
         assert wide_gu and wide_dn   # uniform prefill: both GEMMs run wide
