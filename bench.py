@@ -47,6 +47,9 @@ def parse():
                    help="layer: the MoE layer forward (default); reshard: the EP<->TP "
                         "expert-weight permute of one rank's experts")
     p.add_argument("--tp", type=int, default=8, help="--op reshard: ranks P of the switch")
+    p.add_argument("--l2-flush", action="store_true",
+                   help="write a 256 MB buffer before every timed step (each step then "
+                        "timed alone); for layers whose working set fits in L2")
     return p.parse_args()
 
 
@@ -72,14 +75,23 @@ def layer_config(args):
     return cfg
 
 
-def workload_config(cfg, T):
+L2_BYTES = 129 << 20
+
+
+def workload_config(cfg, T, l2_flush=False):
+    weights = (cfg.E + (1 if cfg.shared else 0)) * 3 * cfg.H * cfg.I * 2
+    if l2_flush:
+        l2 = "L2 flushed before every step (256 MB write), each step timed alone"
+    elif weights > L2_BYTES:
+        l2 = ("inputs larger than L2 (the step streams the touched experts' weights, "
+              f"{weights / 1e9:.2f} GB for all experts)")
+    else:
+        l2 = f"inputs smaller than L2 ({weights / 1e6:.1f} MB of weights), warm, no flush"
     return {"workload": f"{cfg.name} layer, T={T} tokens/step", "layer": cfg.name,
             "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I, "T": T,
             "gating": ["topk_softmax", "softmax_topk", "softmax_topk_renorm",
                        "sigmoid_bias_renorm"][cfg.gating],
-            "shared_expert": cfg.shared, "routing_skew": str(cfg.skew),
-            "l2": "inputs larger than L2 (the step streams the touched experts' weights, "
-                  f"{cfg.E * 3 * cfg.H * cfg.I * 2 / 1e9:.2f} GB for all experts)"}
+            "shared_expert": cfg.shared, "routing_skew": str(cfg.skew), "l2": l2}
 
 
 # ------------------------------------------------------------- clocks --
@@ -318,14 +330,28 @@ def run_gpu(args):
     barrier(pg)
     torch.cuda.synchronize()
     t_wall0 = time.time()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for i in range(args.steps):
-        moe.moe_layer_forward(d, wts, inp.x, y, ws)
-    end.record(stream)
-    torch.cuda.synchronize()
-    barrier(pg)
-    ms = start.elapsed_time(end)
+    if args.l2_flush:
+        # each step alone, after a write larger than L2
+        scratch = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for i in range(args.steps):
+            scratch.fill_(i & 0xff)
+            ev_a[i].record(stream)
+            moe.moe_layer_forward(d, wts, inp.x, y, ws)
+            ev_b[i].record(stream)
+        torch.cuda.synchronize()
+        barrier(pg)
+        ms = sum(ev_a[i].elapsed_time(ev_b[i]) for i in range(args.steps))
+    else:
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(args.steps):
+            moe.moe_layer_forward(d, wts, inp.x, y, ws)
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier(pg)
+        ms = start.elapsed_time(end)
     ms_max = max_over_ranks(ms, pg)
     # ---- the same K steps again with CUDA events at every stage boundary, on
     # the launching stream: per-kernel durations for the roofline ----
@@ -430,7 +456,7 @@ def run_gpu(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded counter-based generator; random-init weights of the layer shape)",
-        "config": workload_config(cfg, T),
+        "config": workload_config(cfg, T, args.l2_flush),
         "roofline": {"bound": "hbm", "kernel": "expert gate/up GEMM + SwiGLU (tcgen05)",
                      "achieved": gu_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": gu_gbs / pk["hbm_gbs"], "traffic": traffic,
