@@ -317,6 +317,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_launch_dependents();
   }
   const uint32_t tmem_base = *tmem_slot;
+  // the stage ring must hold one to kMaxStages stages of this layout (the
+  // barrier arrays have kMaxStages entries); otherwise report and stop
+  if (nst < 1 || nst > (uint32_t)kMaxStages) {
+    if (threadIdx.x == 0) atomicOr(status, kCode);
+    if (warp == 5) tmem_dealloc(tmem_base, kTmemCols);
+    return;
+  }
   const int total = pref[nseg];
   const int nkb = K / kBK;
   // work unit = one K piece of a tile: kbs K blocks (the whole tile, or an
