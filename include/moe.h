@@ -177,6 +177,15 @@ moe_status_t moe_get_device_status(void *workspace, size_t ws_bytes, moe_stream_
 /* Static text for a status code. */
 const char *moe_status_string(moe_status_t s);
 
+/* Check of the failure reporting the pipelined kernels rely on: launches one
+ * thread that waits, with the same bounded wait as the GEMM and router
+ * pipelines, on a barrier that nothing completes.  After about one second the
+ * wait gives up and latches bit 6 in the workspace status word (the kernel
+ * then returns; the context stays usable), so a following
+ * moe_get_device_status returns MOE_ERR_TIMEOUT.  Asynchronous on `stream`;
+ * MOE_ERR_INVALID_ARG for a NULL, unaligned or too small workspace. */
+moe_status_t moe_check_bounded_wait(void *workspace, size_t ws_bytes, moe_stream_t stream);
+
 /* ------------------------------------------------------------ compute -- */
 
 /*

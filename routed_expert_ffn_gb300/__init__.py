@@ -89,6 +89,7 @@ def library() -> ctypes.CDLL:
         "moe_grouped_swiglu_ffn": ([D, P, P, P, P, P, P, P, P, P, P, S, P], I32),
         "moe_combine": ([D, P, P, P, P, P], I32),
         "moe_layer_forward": ([D, ctypes.POINTER(LayerWeights), P, P, P, S, P, P], I32),
+        "moe_check_bounded_wait": ([P, S, P], I32),
         "moe_reshard_ep_to_tp_pack": ([I32, I32, I32, I32, P, P, P, P, P], I32),
         "moe_reshard_tp_to_ep_unpack": ([I32, I32, I32, I32, P, P, P, P, P], I32),
     }
@@ -173,6 +174,13 @@ def moe_get_device_status(ws, clear: bool = True, stream=None):
     st = library().moe_get_device_status(_ptr(ws), _nbytes(ws), _stream(stream), 1 if clear else 0,
                                          ctypes.byref(raw))
     return int(st), int(raw.value)
+
+
+def moe_check_bounded_wait(ws, stream=None):
+    """Launch the bounded-wait check (about one second on the GPU); read the
+    result with moe_get_device_status (MOE_ERR_TIMEOUT, bit 6)."""
+    _check("moe_check_bounded_wait",
+           library().moe_check_bounded_wait(_ptr(ws), _nbytes(ws), _stream(stream)))
 
 
 # ------------------------------------------------------------- compute API --

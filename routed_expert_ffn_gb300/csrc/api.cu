@@ -193,10 +193,21 @@ moe_status_t moe_get_device_status(void *workspace, size_t ws_bytes, moe_stream_
     if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (raw != nullptr) *raw = (int32_t)word;
-  if (word & (kStatusTimeoutGateUp | kStatusTimeoutDown | kStatusTimeoutRouter))
+  if (word & (kStatusTimeoutGateUp | kStatusTimeoutDown | kStatusTimeoutRouter |
+              kStatusTimeoutCheck))
     return MOE_ERR_TIMEOUT;
   if (word & (kStatusBadExpertId | kStatusBadOffsets | kStatusRange)) return MOE_ERR_DEVICE_CHECK;
   return MOE_OK;
+}
+
+moe_status_t moe_check_bounded_wait(void *workspace, size_t ws_bytes, moe_stream_t stream) {
+  if (workspace == nullptr || ws_bytes < kStatusBlockBytes ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return MOE_ERR_INVALID_ARG;
+  moe_status_t st = check_device();
+  if (st != MOE_OK) return st;
+  return cuda_status(
+      launch_bounded_wait_check(static_cast<uint32_t *>(workspace), (cudaStream_t)stream));
 }
 
 const char *moe_status_string(moe_status_t s) {

@@ -97,6 +97,7 @@ constexpr uint32_t kStatusTimeoutDown = 1u << 2;
 constexpr uint32_t kStatusBadOffsets = 1u << 3;
 constexpr uint32_t kStatusTimeoutRouter = 1u << 4;
 constexpr uint32_t kStatusRange = 1u << 5;  // a gate-weighted expert output beyond fp16 range
+constexpr uint32_t kStatusTimeoutCheck = 1u << 6;  // the bounded-wait check ran out (expected)
 
 // A bounded pipeline wait gives up after this long (the longest legitimate
 // wait is one tile's mainloop, well under a millisecond).
@@ -192,6 +193,8 @@ cudaError_t launch_expert_down(const moe_layer_desc_t &d, const void *w2, const 
 cudaError_t launch_combine(const __half *out_perm, const int32_t *inv_pos,
                            const float *topk_w, int T, int k, int H, int shared, __nv_bfloat16 *y,
                            cudaStream_t s);
+// One thread waits on an mbarrier nothing arrives on (waitcheck.cu).
+cudaError_t launch_bounded_wait_check(uint32_t *status, cudaStream_t s);
 // EP <-> TP expert-weight reshard permute (reshard.cu); a null source skips
 // that tensor.  unpack = 0: EP layout -> per-peer chunks; 1: the inverse.
 cudaError_t launch_reshard(int E_local, int H, int I, int P, const void *w13_src, void *w13_dst,

@@ -149,3 +149,11 @@ def test_binding_passes_pointer_width_arguments(lib):
                 assert a is ctypes.c_size_t, (name, decl)
             else:
                 assert a is ctypes.c_int32, (name, decl)
+
+
+def test_bounded_wait_check_validates_before_launch(lib):
+    # NULL, unaligned or too small workspaces are rejected on the host
+    assert lib.moe_check_bounded_wait(None, 1 << 20, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_check_bounded_wait(0x10010, 1 << 20, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_check_bounded_wait(0x10000, 16, None) == moe.MOE_ERR_INVALID_ARG
+

@@ -1,0 +1,28 @@
+"""Failure reporting without a GPU fault (needs a GB300 for the GPU test).
+
+The pipelined kernels bound every wait and report a wait that ran out in the
+workspace status word instead of hanging.  moe_check_bounded_wait makes one
+such wait run out -- a barrier that nothing completes -- and the test checks
+that the host reads MOE_ERR_TIMEOUT with the check's bit, that clearing the
+word works, and that the same context then still computes a correct layer."""
+
+import pytest
+import torch
+
+import routed_expert_ffn_gb300 as moe
+from test_gpu_layer import check_layer, layer_inputs
+
+
+@pytest.mark.gpu
+def test_bounded_wait_reports_and_context_survives():
+    from routed_expert_ffn_gb300 import build
+    build.build()
+    d = moe.desc(64, 256, 8, 2, 512, moe.MOE_GATE_TOPK_SOFTMAX)
+    ws = moe.alloc_workspace(d)
+    moe.moe_check_bounded_wait(ws)
+    st, raw = moe.moe_get_device_status(ws, clear=True)
+    assert st == moe.MOE_ERR_TIMEOUT and raw & (1 << 6), (st, raw)
+    st, raw = moe.moe_get_device_status(ws)
+    assert st == moe.MOE_OK and raw == 0
+    torch.cuda.synchronize()
+    check_layer(layer_inputs("tiny", 64), n_sample=16)
