@@ -47,6 +47,13 @@ def parse():
                    help="layer: the MoE layer forward (default); reshard: the EP<->TP "
                         "expert-weight permute of one rank's experts")
     p.add_argument("--tp", type=int, default=8, help="--op reshard: ranks P of the switch")
+    p.add_argument("--sweep", action="store_true",
+                   help="time every layer configuration at each of its batch sizes, one JSON "
+                        "line each (appended to --sweep-out)")
+    p.add_argument("--sweep-out", default="",
+                   help="--sweep: file the lines are appended to")
+    p.add_argument("--sweep-configs", default="",
+                   help="--sweep: comma-separated layer names to keep (default: all)")
     p.add_argument("--l2-flush", action="store_true",
                    help="write a 256 MB buffer before every timed step (each step then "
                         "timed alone); for layers whose working set fits in L2")
@@ -146,11 +153,48 @@ class ClockSampler:
 
 # ------------------------------------------------------ roofline model --
 
+def expert_params(H, I):
+    """Parameters of one SwiGLU expert: W_gate and W_up [I,H] and W_down [H,I]
+    (Moebius reading notes eq. (2))."""
+    return 3 * H * I
+
+
+def expert_bytes(H, I, bytes_per_param=2):
+    """Bytes one touched expert streams from HBM per forward (bf16: 2 B)."""
+    return expert_params(H, I) * bytes_per_param
+
+
+def expected_touched(E, k, n):
+    """Expected number of experts a batch of n tokens touches when each token
+    picks a uniform random k-subset of E: E * (1 - (1 - k/E)^n) (CS349D
+    lecture 8 notes, section 2.1 "一批 token 会碰到几个专家")."""
+    return E * (1.0 - (1.0 - k / E) ** n)
+
+
+def tokens_per_expert(n, k, E):
+    """Average rows per expert, n*k/E (CS349D lecture 8 notes, section 2.1)."""
+    return n * k / E
+
+
+def ridge_rows(peak_flops, hbm_bytes_per_s):
+    """Rows per expert at which an expert GEMM turns compute-bound: its
+    arithmetic intensity is about m_e flops per weight byte (2 flops per
+    multiply-add over 2-byte weights), so the ridge is F/B (CS349D lecture 8
+    notes, section 2.1, exercise 2)."""
+    return peak_flops / hbm_bytes_per_s
+
+
+def expert_gemm_utilisation(m_rows, peak_flops, hbm_bytes_per_s):
+    """Fraction of the tensor peak an HBM-bound expert GEMM with m rows per
+    expert can reach: min(1, m / ridge)."""
+    return min(1.0, m_rows / ridge_rows(peak_flops, hbm_bytes_per_s))
+
+
 def algorithmic(cfg, T, counts):
     """Algorithmic bytes and flops of one step and of the gate/up GEMM."""
     touched = int(sum(1 for c in counts if c > 0))
     H, I, E, k = cfg.H, cfg.I, cfg.E, cfg.k
-    per_expert = 3 * H * I * 2
+    per_expert = expert_bytes(H, I)
     nsh = 1 if cfg.shared else 0
     layer_bytes = (touched + nsh) * per_expert + E * H * 4 + 2 * T * H * 2
     layer_flops = 2 * T * k * 3 * H * I + nsh * 2 * T * 3 * H * I + 2 * T * H * E
@@ -281,6 +325,156 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+def new_events(stream, n):
+    import torch
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for e in evs:
+        e.record(stream)  # materialise the handles
+    return evs
+
+
+def time_layer(moe, d, wts, x, y, ws, lay, cfg, T, steps, warmup, pg, stream, l2_flush=False):
+    """Warm-up, then the timed region (K forwards between two events, barrier +
+    synchronize on both sides), then the same K forwards with stage events and
+    with per-step events.  Returns the timings, the host time per call and the
+    routing counts the workspace holds afterwards."""
+    import torch
+    for _ in range(warmup):
+        moe.moe_layer_forward(d, wts, x, y, ws)
+    torch.cuda.synchronize()
+    st, raw = moe.moe_get_device_status(ws)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device status {st} raw={raw:#x}")
+    stage_ev = [new_events(stream, moe.MOE_STAGE_EVENTS) for _ in range(steps)]
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, only start/end events (an event between two
+    # kernels would serialise their programmatic-dependent launch) ----
+    barrier(pg)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    if l2_flush:
+        # each step alone, after a write larger than L2
+        scratch = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        for i in range(steps):
+            scratch.fill_(i & 0xff)
+            ev_a[i].record(stream)
+            moe.moe_layer_forward(d, wts, x, y, ws)
+            ev_b[i].record(stream)
+        torch.cuda.synchronize()
+        barrier(pg)
+        ms = sum(ev_a[i].elapsed_time(ev_b[i]) for i in range(steps))
+    else:
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(steps):
+            moe.moe_layer_forward(d, wts, x, y, ws)
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier(pg)
+        ms = start.elapsed_time(end)
+    ms_max = max_over_ranks(ms, pg)
+    # ---- the same K steps again with CUDA events at every stage boundary, on
+    # the launching stream: per-kernel durations for the roofline ----
+    for i in range(steps):
+        moe.moe_layer_forward(d, wts, x, y, ws, stage_events=stage_ev[i])
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    st, raw = moe.moe_get_device_status(ws)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device status {st} raw={raw:#x}")
+
+    # ---- the same K steps once more with an event between consecutive
+    # forwards only: the spread of single-step times (p10 / p50 / p90) ----
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    step_ev[0].record(stream)
+    for i in range(steps):
+        moe.moe_layer_forward(d, wts, x, y, ws)
+        step_ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    step_us = sorted(1e3 * step_ev[i].elapsed_time(step_ev[i + 1]) for i in range(steps))
+    pct = lambda q: step_us[min(len(step_us) - 1, int(q * (len(step_us) - 1) + 0.5))]
+    step_spread = {"p10": pct(0.1), "p50": pct(0.5), "p90": pct(0.9)}
+
+    # ---- host time of one call (argument checks, cached tensor maps, launches;
+    # the Python binding's marshalling included), the GPU kept busy ahead ----
+    n_host = max(10, min(steps, 100))
+    torch.cuda.synchronize()
+    h0 = time.perf_counter()
+    for _ in range(n_host):
+        moe.moe_layer_forward(d, wts, x, y, ws)
+    host_us = 1e6 * (time.perf_counter() - h0) / n_host
+    torch.cuda.synchronize()
+
+    stage_ms = {n: 0.0 for n in moe.STAGE_NAMES}
+    for ev in stage_ev:
+        for j, n in enumerate(moe.STAGE_NAMES):
+            stage_ms[n] += ev[j].elapsed_time(ev[j + 1])
+    stage_us = {n: 1e3 * v / steps for n, v in stage_ms.items()}
+    counts = moe.workspace_view(ws, lay, "counts", torch.int32, (cfg.E,)).cpu().tolist()
+    gap = moe.workspace_view(ws, lay, "gap", torch.float32, (T,)).cpu()
+    near_ties = int((gap < NEAR_TIE).sum().item()) if cfg.k < cfg.E else 0
+    return {"ms_max": ms_max, "stage_us": stage_us, "step_spread": step_spread,
+            "host_us": host_us, "counts": counts, "near_ties": near_ties,
+            "t_wall": (t_wall0, t_wall1)}
+
+
+# top-k boundary gaps below this are near-ties (the configuration statement)
+NEAR_TIE = 1e-5
+
+
+def layer_line(cfg, T, args, world, tm, pk, sampler):
+    """The JSON line of one layer measurement (without e2e / cpu_baseline)."""
+    counts = tm["counts"]
+    alg = algorithmic(cfg, T, counts)
+    step_s = tm["ms_max"] / 1e3 / args.steps
+    value = world * T / step_s
+    stage_us = tm["stage_us"]
+    gu_s = stage_us["gateup"] / 1e6
+    gu_gbs = alg["gateup_bytes"] / gu_s / 1e9
+    layer_t_hbm = alg["layer_bytes"] / (pk["hbm_gbs"] * 1e9)
+    layer_t_tc = alg["layer_flops"] / (pk["bf16_tflops_sustained"] * 1e12)
+    layer_roof = max(layer_t_hbm, layer_t_tc)
+    num = max(counts) * cfg.E
+    den = T * cfg.k
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        with open(prof) as f:
+            tr = json.load(f).get(f"{cfg.name}_T{T}")
+        if tr and tr.get("kernel_sources_sha") == kernel_sources_sha():
+            traffic = tr["gateup_dram_bytes"]
+    return {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tm["ms_max"] / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded counter-based generator; random-init weights of the layer shape)",
+        "config": workload_config(cfg, T, args.l2_flush),
+        "roofline": {"bound": "hbm", "kernel": "expert gate/up GEMM + SwiGLU (tcgen05)",
+                     "achieved": gu_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": gu_gbs / pk["hbm_gbs"], "traffic": traffic,
+                     "algorithmic_bytes": alg["gateup_bytes"], "launch_us": stage_us["gateup"],
+                     "peak_source": pk["source"]},
+        "layer_roofline": {"bound": "hbm" if layer_t_hbm >= layer_t_tc else "tensor",
+                           "roof_us": layer_roof * 1e6, "step_us": step_s * 1e6,
+                           "frac": layer_roof / step_s, "bytes": alg["layer_bytes"],
+                           "flops": alg["layer_flops"], "touched_experts": alg["touched"],
+                           "hbm_peak_gbs": pk["hbm_gbs"],
+                           "tc_peak_tflops": pk["bf16_tflops_sustained"],
+                           "tc_frac_of_burst": alg["layer_flops"] / step_s
+                                               / (pk["bf16_tflops"] * 1e12)},
+        "stages_us": stage_us,
+        "step_us_spread": tm["step_spread"],
+        "host_us_per_call": tm["host_us"],
+        "routing": {"imbalance_ratio": num / den, "touched_experts": alg["touched"],
+                    "near_ties": tm["near_ties"], "near_tie_gap": NEAR_TIE},
+        "gpu_launches": launches_per_step(cfg, T) * args.steps,
+        "clocks": sampler.summary(*tm["t_wall"]) if sampler else None,
+    }
+
+
 def run_gpu(args):
     import torch
 
@@ -305,81 +499,11 @@ def run_gpu(args):
     y = torch.empty((T, cfg.H), dtype=torch.bfloat16, device="cuda")
     stream = torch.cuda.current_stream()
 
-    def new_events(n):
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-        for e in evs:
-            e.record(stream)  # materialise the handles
-        return evs
-
-    # warm-up
-    for _ in range(args.warmup):
-        moe.moe_layer_forward(d, wts, inp.x, y, ws)
-    torch.cuda.synchronize()
-    st, raw = moe.moe_get_device_status(ws)
-    if st != moe.MOE_OK:
-        raise RuntimeError(f"device status {st} raw={raw:#x}")
-
-    stage_ev = [new_events(moe.MOE_STAGE_EVENTS) for _ in range(args.steps)]
-    torch.cuda.synchronize()
     uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
     sampler = ClockSampler(uuid) if rank == 0 else None
     time.sleep(0.5 if sampler else 0)
-
-    # ---- timed region: K steps, only start/end events (an event between two
-    # kernels would serialise their programmatic-dependent launch) ----
-    barrier(pg)
-    torch.cuda.synchronize()
-    t_wall0 = time.time()
-    if args.l2_flush:
-        # each step alone, after a write larger than L2
-        scratch = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
-        ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        for i in range(args.steps):
-            scratch.fill_(i & 0xff)
-            ev_a[i].record(stream)
-            moe.moe_layer_forward(d, wts, inp.x, y, ws)
-            ev_b[i].record(stream)
-        torch.cuda.synchronize()
-        barrier(pg)
-        ms = sum(ev_a[i].elapsed_time(ev_b[i]) for i in range(args.steps))
-    else:
-        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        start.record(stream)
-        for i in range(args.steps):
-            moe.moe_layer_forward(d, wts, inp.x, y, ws)
-        end.record(stream)
-        torch.cuda.synchronize()
-        barrier(pg)
-        ms = start.elapsed_time(end)
-    ms_max = max_over_ranks(ms, pg)
-    # ---- the same K steps again with CUDA events at every stage boundary, on
-    # the launching stream: per-kernel durations for the roofline ----
-    for i in range(args.steps):
-        moe.moe_layer_forward(d, wts, inp.x, y, ws, stage_events=stage_ev[i])
-    torch.cuda.synchronize()
-    t_wall1 = time.time()
-    st, raw = moe.moe_get_device_status(ws)
-    if st != moe.MOE_OK:
-        raise RuntimeError(f"device status {st} raw={raw:#x}")
-
-    # ---- the same K steps once more with an event between consecutive
-    # forwards only: the spread of single-step times (p10 / p50 / p90) ----
-    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-    step_ev[0].record(stream)
-    for i in range(args.steps):
-        moe.moe_layer_forward(d, wts, inp.x, y, ws)
-        step_ev[i + 1].record(stream)
-    torch.cuda.synchronize()
-    step_us = sorted(1e3 * step_ev[i].elapsed_time(step_ev[i + 1]) for i in range(args.steps))
-    pct = lambda q: step_us[min(len(step_us) - 1, int(q * (len(step_us) - 1) + 0.5))]
-    step_spread = {"p10": pct(0.1), "p50": pct(0.5), "p90": pct(0.9)}
-
-    stage_ms = {n: 0.0 for n in moe.STAGE_NAMES}
-    for ev in stage_ev:
-        for j, n in enumerate(moe.STAGE_NAMES):
-            stage_ms[n] += ev[j].elapsed_time(ev[j + 1])
-    stage_us = {n: 1e3 * v / args.steps for n, v in stage_ms.items()}
+    tm = time_layer(moe, d, wts, inp.x, y, ws, lay, cfg, T, args.steps, args.warmup, pg, stream,
+                    args.l2_flush)
 
     # ---- end to end: pinned host x in, host y out, through the same call ----
     # Every step copies its x from pinned host memory, runs moe_layer_forward
@@ -429,61 +553,121 @@ def run_gpu(args):
     e_ms = max_over_ranks(e0.elapsed_time(e1), pg)
     if sampler:
         sampler.stop()
-
-    counts = moe.workspace_view(ws, lay, "counts", torch.int32, (cfg.E,)).cpu().tolist()
     if rank != 0:
         return
     pk = peaks()
-    alg = algorithmic(cfg, T, counts)
-    step_s = ms_max / 1e3 / args.steps
-    value = world * T / step_s
-    gu_s = stage_us["gateup"] / 1e6
-    gu_gbs = alg["gateup_bytes"] / gu_s / 1e9
-    layer_t_hbm = alg["layer_bytes"] / (pk["hbm_gbs"] * 1e9)
-    layer_t_tc = alg["layer_flops"] / (pk["bf16_tflops_sustained"] * 1e12)
-    layer_roof = max(layer_t_hbm, layer_t_tc)
-    num = max(counts) * cfg.E
-    den = T * cfg.k
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(prof):
-        with open(prof) as f:
-            tr = json.load(f).get(f"{cfg.name}_T{T}")
-        if tr and tr.get("kernel_sources_sha") == kernel_sources_sha():
-            traffic = tr["gateup_dram_bytes"]
-    line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded counter-based generator; random-init weights of the layer shape)",
-        "config": workload_config(cfg, T, args.l2_flush),
-        "roofline": {"bound": "hbm", "kernel": "expert gate/up GEMM + SwiGLU (tcgen05)",
-                     "achieved": gu_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": gu_gbs / pk["hbm_gbs"], "traffic": traffic,
-                     "algorithmic_bytes": alg["gateup_bytes"], "launch_us": stage_us["gateup"],
-                     "peak_source": pk["source"]},
-        "layer_roofline": {"bound": "hbm" if layer_t_hbm >= layer_t_tc else "tensor",
-                           "roof_us": layer_roof * 1e6, "step_us": step_s * 1e6,
-                           "frac": layer_roof / step_s, "bytes": alg["layer_bytes"],
-                           "flops": alg["layer_flops"], "touched_experts": alg["touched"],
-                           "hbm_peak_gbs": pk["hbm_gbs"],
-                           "tc_peak_tflops": pk["bf16_tflops_sustained"]},
-        "stages_us": stage_us,
-        "step_us_spread": step_spread,
-        "routing": {"imbalance_ratio": num / den, "touched_experts": alg["touched"]},
-        "e2e": {"value": world * T * e_steps / (e_ms / 1e3), "unit": "tokens/s",
-                "h2d_bytes_per_step": T * cfg.H * 2, "d2h_bytes_per_step": T * cfg.H * 2},
-        "gpu_launches": launches_per_step(cfg, T) * args.steps,
-        "clocks": sampler.summary(t_wall0, t_wall1) if sampler else None,
-    }
+    line = layer_line(cfg, T, args, world, tm, pk, sampler)
+    line["e2e"] = {"value": world * T * e_steps / (e_ms / 1e3), "unit": "tokens/s",
+                   "h2d_bytes_per_step": T * cfg.H * 2, "d2h_bytes_per_step": T * cfg.H * 2}
     if not args.no_cpu_baseline:
         hin = host_inputs(cfg, T, args.seed, experts_from_gpu=inp)
         n, dt, threads = cpu_oracle_sample(hin, args.cpu_tokens)
         line["cpu_baseline"] = {"value": n / dt, "unit": "tokens/s", "cores": threads,
-                                "kind": "oracle",
+                                "kind": "oracle", "cpu_model": cpu_model(),
                                 "sample": f"{n} seeded tokens of the T={T} batch (routing + "
-                                          "expert FFNs + combine, fp64)"}
+                                          "expert FFNs + combine, fp64)",
+                                "tiny_layer_single_thread": tiny_single_thread()}
     print(json.dumps(line))
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        vendor = model = ""
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+            elif line.startswith("Vendor ID:"):
+                vendor = line.split(":", 1)[1].strip()
+        if model:
+            return f"{vendor} {model}".strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
+def tiny_single_thread():
+    """The oracle on one thread over the whole tiny layer (T=64: router, top-k
+    gating, expert FFNs, combine), median of 3 runs, in tokens/s."""
+    import oracle
+    import synth
+    cfg = synth.CONFIGS["tiny"]
+    T = 64
+    inp = synth.make_layer(cfg, T, 0, device="cpu")
+    times = []
+    for _ in range(3):
+        t0 = time.perf_counter()
+        oracle.layer(inp, nthreads=1)
+        times.append(time.perf_counter() - t0)
+    dt = statistics.median(times)
+    return {"value": T / dt, "unit": "tokens/s", "cores": 1, "workload": "tiny layer, T=64",
+            "seconds": dt}
+
+
+# (config, T) pairs of the sweep: every layer configuration at its batch sizes
+SWEEP = [("qwen3", T) for T in (1, 16, 128, 256, 1024)] + \
+        [("qwen3_tp8", T) for T in (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 2048)] + \
+        [("mixtral", T) for T in (1, 8, 64, 512, 4096)] + \
+        [("dsv3", T) for T in (2048, 8192)] + [("tiny", 64)]
+
+
+def run_sweep(args):
+    """One JSON line per (layer, T) of SWEEP, each with its own clock record and
+    stage times, appended to --sweep-out (and printed)."""
+    import torch
+
+    import routed_expert_ffn_gb300 as moe
+    import synth
+    from routed_expert_ffn_gb300 import build as moe_build
+    torch.cuda.set_device(0)
+    moe_build.build()
+    pk = peaks()
+    uuid = "GPU-" + str(torch.cuda.get_device_properties(0).uuid)
+    only = set(args.sweep_configs.split(",")) if args.sweep_configs else None
+    stream = torch.cuda.current_stream()
+    layers = {}
+    out_path = args.sweep_out
+    for name, T in SWEEP:
+        if only is not None and name not in only:
+            continue
+        cfg = synth.CONFIGS[name]
+        if name not in layers:
+            layers.clear()
+            torch.cuda.empty_cache()
+            layers[name] = synth.make_layer(cfg, 1, args.seed, device="cuda")
+        full = layers[name]
+        x = synth.make_tokens(cfg, T, args.seed, device="cuda")
+        w_r, b = synth.make_router(cfg, args.seed, device="cuda")
+        d = moe.desc(T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.gating, cfg.shared)
+        ws = moe.alloc_workspace(d)
+        lay = moe.moe_workspace_layout(d)
+        wts = moe.layer_weights(w_r, full.w13, full.w2, b, full.w13_shared, full.w2_shared)
+        y = torch.empty((T, cfg.H), dtype=torch.bfloat16, device="cuda")
+        steps = args.steps if T < 4096 else max(3, args.steps // 10)
+        a = argparse.Namespace(**vars(args))
+        a.steps = steps
+        a.l2_flush = name == "tiny"
+        sampler = ClockSampler(uuid)
+        time.sleep(0.3)
+        tm = time_layer(moe, d, wts, x, y, ws, lay, cfg, T, steps, args.warmup, None, stream,
+                        a.l2_flush)
+        sampler.stop()
+        line = layer_line(cfg, T, a, 1, tm, pk, sampler)
+        line["sweep"] = True
+        print(json.dumps(line), flush=True)
+        if out_path:
+            with open(out_path, "a") as f:
+                f.write(json.dumps(line) + "\n")
+        del ws, y, x
 
 
 def launches_per_step(cfg, T):
@@ -599,6 +783,8 @@ def main():
         return
     if args.impl == "reference":
         run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
     else:
         run_gpu(args)
 

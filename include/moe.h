@@ -26,6 +26,11 @@
  *   range, a pipeline wait that ran out of time) are latched in a status word
  *   at the start of the workspace and read with moe_get_device_status(); the
  *   kernels never trap.
+ * - Deliberate departures from the first sketch of this interface: the
+ *   dispatch call writes no permuted copy of x (moe_grouped_swiglu_ffn
+ *   gathers the rows it needs into its workspace), moe_combine takes no
+ *   separate shared-expert output (those rows ride in out_perm[T*k:]), and
+ *   out_perm is fp16 rather than bf16 (11 significant bits for the k-row sum).
  * - Workspace: one caller-allocated device buffer of moe_workspace_size(desc)
  *   bytes (256-byte aligned) serves every call made with that descriptor;
  *   initialise its status word once with moe_workspace_init().  Calls that
@@ -311,7 +316,11 @@ moe_status_t moe_layer_forward(const moe_layer_desc_t *d, const moe_layer_weight
  *   E = 512: T*k <= 65536.)
  * Set-up: the first call on each device looks up the array's device address
  *   (with that device current); make that first call before any stream
- *   capture.
+ *   capture.  Under CUDA's lazy module loading that first lookup can load
+ *   this library's device code and reserve the array's device memory (the
+ *   runtime's doing, once per device); from then on no call reserves
+ *   memory.  The address is cached per device, so after cudaDeviceReset the
+ *   library must be reloaded before this entry point is used again.
  * Sharing: every call uses the same array and it keeps the last call's
  *   contents (the call clears what must start at zero).  Calls whose work
  *   overlaps on the GPU -- e.g. on two streams with no ordering between

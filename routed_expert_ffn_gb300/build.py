@@ -33,7 +33,10 @@ def sources():
 def _stale(obj: str, src: str) -> bool:
     if not os.path.exists(obj):
         return True
-    deps = [src, os.path.join(CSRC, "moe_internal.cuh"), os.path.join(ROOT, "include", "moe.h")]
+    # every header the sources include (csrc/*.cuh, include/*.h)
+    inc = os.path.join(ROOT, "include")
+    deps = [src] + [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
+    deps += [os.path.join(inc, f) for f in os.listdir(inc) if f.endswith(".h")]
     t = os.path.getmtime(obj)
     return any(os.path.getmtime(d) > t for d in deps)
 

@@ -63,12 +63,6 @@ Layout make_layout(const moe_layer_desc_t &d) {
   return L;
 }
 
-}  // namespace moe
-
-using namespace moe;
-
-namespace {
-
 moe_status_t validate_desc(const moe_layer_desc_t *d) {
   if (d == nullptr) return MOE_ERR_INVALID_ARG;
   if (d->gating < MOE_GATE_TOPK_SOFTMAX || d->gating > MOE_GATE_SIGMOID_BIAS_RENORM)
@@ -99,6 +93,12 @@ moe_status_t check_device() {
   }
   return state[dev] == 1 ? MOE_OK : MOE_ERR_UNSUPPORTED_DEVICE;
 }
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
 
 // Common prologue of the compute calls: descriptor and workspace (host only;
 // the device check comes after every argument has been validated).

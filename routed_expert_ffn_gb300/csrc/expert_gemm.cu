@@ -49,6 +49,9 @@
 // Every wait is bounded; on expiry the CTA records MOE_ERR_TIMEOUT's status
 // bit, drains its copies and MMAs in flight, frees TMEM and returns.
 #include <stdio.h>
+#include <string.h>
+
+#include <mutex>
 
 #include "moe_internal.cuh"
 
@@ -701,6 +704,79 @@ bool act_map(CUtensorMap *m, const void *a, int K, int64_t R, int box_rows) {
   return encode_bf16_map(m, a, 3, dims, strides, box);
 }
 
+// The tensor maps of one GEMM launch.  Encoding them takes host time on every
+// call (about 20 cuTensorMapEncodeTiled calls per GEMM), so the sets of recent
+// calls are kept, keyed by everything the maps depend on: the device, the
+// weight and activation pointers and the shapes.
+struct GemmMaps {
+  CUtensorMap ma, msh, maw, mawsh;
+  TokenMaps mb;
+};
+struct GemmMapKey {
+  int dev, E, K, rows, P, shared, pair_maps;
+  int64_t R;
+  const void *w, *w_sh, *act;
+  bool operator==(const GemmMapKey &o) const {
+    return dev == o.dev && E == o.E && K == o.K && rows == o.rows && P == o.P &&
+           shared == o.shared && pair_maps == o.pair_maps && R == o.R && w == o.w &&
+           w_sh == o.w_sh && act == o.act;
+  }
+};
+
+template <bool kGateUp>
+bool encode_gemm_maps(const GemmMapKey &k, GemmMaps *g) {
+  // rows of each half of W13 / of W2 per tile; gate/up in the wide layout
+  // takes kGateUpColsWide rows of each half
+  if (!weight_map(&g->ma, k.w, k.K, k.rows, k.P, k.E, kBM)) return false;
+  if (k.shared) {
+    if (!weight_map(&g->msh, k.w_sh, k.K, k.rows, k.P, 1, kBM)) return false;
+  } else {
+    g->msh = g->ma;
+  }
+  if (kGateUp || k.pair_maps) {
+    // gate/up: 64-row boxes (wide layout); down, pair layouts: 256-row boxes
+    const int box = kGateUp ? kGateUpColsWide : 2 * kBM;
+    if (!weight_map(&g->maw, k.w, k.K, k.rows, k.P, k.E, box)) return false;
+    if (k.shared) {
+      if (!weight_map(&g->mawsh, k.w_sh, k.K, k.rows, k.P, 1, box)) return false;
+    } else {
+      g->mawsh = g->maw;
+    }
+  } else {
+    g->maw = g->ma;
+    g->mawsh = g->msh;
+  }
+  for (int i = 0; i < 16; ++i)
+    if (!act_map(&g->mb.m[i], k.act, k.K, k.R, 16 * (i + 1))) return false;
+  return true;
+}
+
+// A small cache of recently used map sets per GEMM kind (round-robin
+// replacement); returns false if the encoder rejects the arguments.
+template <bool kGateUp>
+bool gemm_maps(const GemmMapKey &key, GemmMaps *out) {
+  constexpr int kSlots = 16;
+  static GemmMapKey keys[kSlots];
+  static GemmMaps maps[kSlots];
+  static bool used[kSlots] = {};
+  static int next = 0;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < kSlots; ++i)
+    if (used[i] && keys[i] == key) {
+      *out = maps[i];
+      return true;
+    }
+  GemmMaps g;
+  if (!encode_gemm_maps<kGateUp>(key, &g)) return false;
+  keys[next] = key;
+  maps[next] = g;
+  used[next] = true;
+  next = (next + 1) % kSlots;
+  *out = g;
+  return true;
+}
+
 template <bool kGateUp>
 cudaError_t launch_gemm(const moe_layer_desc_t &d, const void *w, const void *w_sh,
                         const __nv_bfloat16 *act, const int32_t *plan, int plan_early,
@@ -714,45 +790,27 @@ cudaError_t launch_gemm(const moe_layer_desc_t &d, const void *w, const void *w_
   const int64_t R = Na + (shared ? d.T : 0);
   const int K = kGateUp ? d.H : d.I;
   const int rows = kGateUp ? d.I : d.H;  // weight rows per half = output columns
-  const int P = kGateUp ? 2 : 1;
-  // rows of each half of W13 / of W2 per tile; gate/up in the wide layout
-  // takes kGateUpColsWide rows of each half
-  CUtensorMap ma, msh, maw, mawsh;
-  TokenMaps mb;
-  if (!weight_map(&ma, w, K, rows, P, d.E, kBM)) return cudaErrorInvalidValue;
-  if (shared) {
-    if (!weight_map(&msh, w_sh, K, rows, P, 1, kBM)) return cudaErrorInvalidValue;
-  } else {
-    msh = ma;
-  }
-  if (kGateUp) {
-    if (!weight_map(&maw, w, K, rows, P, d.E, kGateUpColsWide)) return cudaErrorInvalidValue;
-    if (shared) {
-      if (!weight_map(&mawsh, w_sh, K, rows, P, 1, kGateUpColsWide)) return cudaErrorInvalidValue;
-    } else {
-      mawsh = maw;
-    }
-  } else if (d.H >= 2 * kBM) {
-    // down, pair layout: 256-row boxes
-    if (!weight_map(&maw, w, K, rows, P, d.E, 2 * kBM)) return cudaErrorInvalidValue;
-    if (shared) {
-      if (!weight_map(&mawsh, w_sh, K, rows, P, 1, 2 * kBM)) return cudaErrorInvalidValue;
-    } else {
-      mawsh = maw;
-    }
-  } else {
-    maw = ma;
-    mawsh = msh;
-  }
-  for (int i = 0; i < 16; ++i)
-    if (!act_map(&mb.m[i], act, K, R, 16 * (i + 1))) return cudaErrorInvalidValue;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  GemmMapKey key;
+  memset(&key, 0, sizeof key);
+  key.dev = dev;
+  key.E = d.E;
+  key.K = K;
+  key.rows = rows;
+  key.P = kGateUp ? 2 : 1;
+  key.shared = shared;
+  key.pair_maps = (!kGateUp && d.H >= 2 * kBM) ? 1 : 0;
+  key.R = R;
+  key.w = w;
+  key.w_sh = shared ? w_sh : nullptr;
+  key.act = act;
+  GemmMaps g;
+  if (!gemm_maps<kGateUp>(key, &g)) return cudaErrorInvalidValue;
 
   const size_t smem = C::smem_bytes(nseg);
   auto kern = expert_gemm_kernel<kGateUp>;
   static size_t configured[64] = {};  // per device
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (smem > configured[dev]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
@@ -762,7 +820,8 @@ cudaError_t launch_gemm(const moe_layer_desc_t &d, const void *w, const void *w_
   // one CTA per SM: the device-side plan decides the tiles (and split-K
   // pieces); CTAs without work leave at once
   const int grid = num_sms();
-  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, ma, msh, maw, mawsh, mb, plan,
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, g.ma, g.msh, g.maw, g.mawsh, g.mb,
+                    plan,
                     plan_early, nseg, d.E, K, rows, Na, w_perm, out, split_part, split_cnt, status);
 }
 

@@ -141,6 +141,16 @@ constexpr int kMaxSplit = 16;
 constexpr int kMaxSplitTiles = 1024;
 constexpr size_t kStatusBlockBytes = 256 + 2 * kMaxSplitTiles * 4;
 
+// ------------------------------------------------------ argument checks --
+// Host-side validation shared by every entry point (api.cu, noalloc.cu):
+// descriptor enums and shape limits (MOE_ERR_INVALID_ARG /
+// MOE_ERR_UNSUPPORTED_SHAPE), 16-byte aligned non-null pointers, and the
+// current device's compute capability (10.3, cached per device).
+moe_status_t validate_desc(const moe_layer_desc_t *d);
+bool ok_ptr(const void *p);  // non-null and 16-byte aligned
+bool ok_opt(const void *p);  // null, or 16-byte aligned
+moe_status_t check_device();
+
 // ------------------------------------------------------------- launches --
 // Each returns cudaSuccess or the launch error.
 cudaError_t launch_router_logits(const __nv_bfloat16 *x, const float *w_router, int T, int H, int E,

@@ -58,18 +58,11 @@ extern "C" moe_status_t moe_build_dispatch_noalloc(const moe_layer_desc_t *d,
                                                    int32_t *perm_src, int32_t *inv_pos,
                                                    float *w_perm, int32_t *device_status,
                                                    moe_stream_t stream) {
-  if (d == nullptr) return MOE_ERR_INVALID_ARG;
-  if (d->gating < MOE_GATE_TOPK_SOFTMAX || d->gating > MOE_GATE_SIGMOID_BIAS_RENORM ||
-      (d->has_shared_expert != 0 && d->has_shared_expert != 1))
-    return MOE_ERR_INVALID_ARG;
-  if (d->T < 1 || d->T > kMaxT || d->E < 1 || d->E > kMaxE || d->k < 1 || d->k > d->E ||
-      d->k > kMaxK || (int64_t)d->T * d->k > kMaxAssign || d->H < 64 || d->H > 16384 ||
-      d->H % 64 != 0 || d->I < 64 || d->I > 32768 || d->I % 64 != 0)
-    return MOE_ERR_UNSUPPORTED_SHAPE;
-  auto aligned = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-  if (topk_ids == nullptr || counts == nullptr || offsets == nullptr || perm_src == nullptr ||
-      inv_pos == nullptr || !aligned(topk_ids) || !aligned(counts) || !aligned(offsets) ||
-      !aligned(perm_src) || !aligned(inv_pos) || !aligned(topk_w) || !aligned(w_perm) ||
+  // the same argument checks as moe_build_dispatch (api.cu)
+  moe_status_t st = validate_desc(d);
+  if (st != MOE_OK) return st;
+  if (!ok_ptr(topk_ids) || !ok_ptr(counts) || !ok_ptr(offsets) || !ok_ptr(perm_src) ||
+      !ok_ptr(inv_pos) || !ok_opt(topk_w) || !ok_opt(w_perm) ||
       (device_status != nullptr && (reinterpret_cast<uintptr_t>(device_status) & 3u) != 0))
     return MOE_ERR_INVALID_ARG;
   if (w_perm != nullptr && topk_w == nullptr) return MOE_ERR_INVALID_ARG;
@@ -81,15 +74,10 @@ extern "C" moe_status_t moe_build_dispatch_noalloc(const moe_layer_desc_t *d,
   const size_t table = (size_t)nblk * d->E * sizeof(int32_t);
   if (256 + 2 * table > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED_SHAPE;
 
-  int dev = 0, major = 0, minor = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (major != 10 || minor != 3) return MOE_ERR_UNSUPPORTED_DEVICE;
+  if ((st = check_device()) != MOE_OK) return st;
 
   void *base = nullptr;
-  moe_status_t st = scratch_address(&base);
+  st = scratch_address(&base);
   if (st != MOE_OK) return st;
   unsigned char *scratch = static_cast<unsigned char *>(base);
   uint32_t *status = reinterpret_cast<uint32_t *>(scratch);

@@ -27,3 +27,28 @@ def golden(name):
             else:
                 rows.append(line.split())
     return kv, rows
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Report the routing counts the GPU parity tests collected: tokens whose
+    top-k boundary gap is below 1e-5 (near_ties), near-tie tokens where the GPU
+    chose a different valid set (flips), and clear tokens with two near-equal
+    experts in swapped slots (order_swaps)."""
+    try:
+        from gpu_check import ROUTING_REPORT
+    except Exception:
+        return
+    if not ROUTING_REPORT:
+        return
+    tot = {"tokens": 0, "near_ties": 0, "flips": 0, "order_swaps": 0}
+    terminalreporter.write_sep("-", "routing near-ties (top-k boundary gap < 1e-5)")
+    for label, info in ROUTING_REPORT:
+        for key in tot:
+            tot[key] += info[key]
+        if info["near_ties"] or info["flips"] or info["order_swaps"]:
+            terminalreporter.write_line(
+                f"{label}: tokens={info['tokens']} near_ties={info['near_ties']} "
+                f"flips={info['flips']} order_swaps={info['order_swaps']}")
+    terminalreporter.write_line(
+        f"routing total over {len(ROUTING_REPORT)} checks: tokens={tot['tokens']} "
+        f"near_ties={tot['near_ties']} flips={tot['flips']} order_swaps={tot['order_swaps']}")

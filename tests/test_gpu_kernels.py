@@ -70,7 +70,8 @@ def test_route_matches_oracle(mode, T, H, E, k):
     rs = oracle.router_logits(x, w_r)
     r_ids, r_w, r_gap = oracle.topk_gating(rs, k, mode, b)
     assert np.max(np.abs(s - rs)) <= 1e-4 * max(1.0, float(np.max(np.abs(rs))))
-    info = check_routing(ids, w, {"ids": r_ids, "w": r_w, "gap": r_gap, "logits": rs}, mode, b.numpy())
+    info = check_routing(ids, w, {"ids": r_ids, "w": r_w, "gap": r_gap, "logits": rs}, mode, b.numpy(),
+                         label=f"route mode={mode} T={T} E={E} k={k}")
     if k < E:
         clear = ~(r_gap < NEAR_TIE)
         assert np.allclose(gap[clear], r_gap[clear], atol=1e-5, rtol=0)

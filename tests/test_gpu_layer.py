@@ -1,8 +1,11 @@
 """Whole-layer parity of moe_layer_forward with the CPU oracle on the five
 layer configurations (needs a GB300).
 
-Small batches are checked on every token; large ones on a seeded token sample
-that always holds a token of the hottest and of the coldest touched expert.
+Small batches are checked on every token; large ones on a seeded sample of at
+least 256 tokens that holds the first and last row of every 128-row chunk of
+the two hottest experts and of the shared expert (the GEMMs' token-chunk
+boundaries and both halves of their 256-row tiles), a token of the coldest
+touched expert, and seeded random tokens.
 Routing metadata is compared on all tokens: ids bit-exact off near-ties, and
 counts / offsets / permutation / inverse bit-exact against the oracle's
 dispatch of the same ids."""
@@ -49,7 +52,7 @@ def layer_inputs(name, T, seed=0, uniform=False):
                              full.w2_shared)
 
 
-def check_layer(inputs, n_sample=48):
+def check_layer(inputs, n_sample=256):
     cfg, T = inputs.cfg, inputs.T
     run = LayerRun(inputs)
     y = run.forward()
@@ -59,7 +62,8 @@ def check_layer(inputs, n_sample=48):
     ids, w, gap = oracle.topk_gating(s, cfg.k, cfg.gating, host["sel_bias"])
     ref = {"logits": s, "ids": ids, "w": w, "gap": gap}
     bias = None if host["sel_bias"] is None else host["sel_bias"].numpy()
-    info = check_routing(meta["ids"], meta["w"], ref, cfg.gating, bias)
+    info = check_routing(meta["ids"], meta["w"], ref, cfg.gating, bias,
+                         label=f"{cfg.name} T={T}")
     # dispatch of the ids the GPU routed (a pure integer function of them)
     rc, ro, rp, ri = oracle.dispatch(meta["ids"], cfg.E)
     assert np.array_equal(meta["counts"], rc)
@@ -68,7 +72,8 @@ def check_layer(inputs, n_sample=48):
     assert np.array_equal(meta["inv_pos"], ri)
     assert np.array_equal(meta["w_perm"], meta["w"].reshape(-1)[rp])
     # outputs on the sampled tokens whose routing is not a near-tie
-    toks = sample_tokens(T, n_sample, ref["ids"], rc)
+    toks = sample_tokens(T, n_sample, meta["ids"], rc, perm_src=meta["perm_src"],
+                         offsets=meta["offsets"], shared=bool(cfg.shared))
     toks = [t for t in toks if not (ref["gap"][t] < 1e-5)]
     need = sorted({int(e) for t in toks for e in ref["ids"][t]})
     host = host_copy(inputs, experts=need)
@@ -77,7 +82,8 @@ def check_layer(inputs, n_sample=48):
     got = bf16_np(y[toks])
     r, m = assert_output_close(got, y_ref)
     num, den = oracle.imbalance(rc, T * cfg.k)
-    return {"rel_l2": r, "max_rel": m, "imbalance": num / den, **info}
+    return {"rel_l2": r, "max_rel": m, "imbalance": num / den, "checked_tokens": len(toks),
+            **info}
 
 
 @pytest.mark.parametrize("T", [64, 1, 17])
@@ -87,28 +93,30 @@ def test_tiny_layer(T):
 
 @pytest.mark.parametrize("T", [1, 8, 64, 512, 4096])
 def test_mixtral_layer(T):
-    check_layer(layer_inputs("mixtral", T), n_sample=24)
+    info = check_layer(layer_inputs("mixtral", T))
+    assert info["checked_tokens"] >= min(T, 256)
 
 
 @pytest.mark.parametrize("T", [1, 16, 128, 256, 1024])
 def test_qwen3_layer(T):
-    info = check_layer(layer_inputs("qwen3", T), n_sample=48)
+    info = check_layer(layer_inputs("qwen3", T), n_sample=128)
     if T == 1024:
         assert 2.7 <= info["imbalance"] <= 3.3
 
 
 def test_qwen3_layer_uniform_routing():
-    check_layer(layer_inputs("qwen3", 1024, uniform=True), n_sample=32)
+    check_layer(layer_inputs("qwen3", 1024, uniform=True), n_sample=64)
 
 
 @pytest.mark.parametrize("T", [1, 8, 64, 256, 2048])
 def test_qwen3_tp8_slice_layer(T):
-    check_layer(layer_inputs("qwen3_tp8", T), n_sample=48)
+    check_layer(layer_inputs("qwen3_tp8", T), n_sample=128)
 
 
 @pytest.mark.parametrize("T", [2048, 8192])
 def test_dsv3_layer(T):
-    check_layer(layer_inputs("dsv3", T), n_sample=20)
+    info = check_layer(layer_inputs("dsv3", T))
+    assert info["checked_tokens"] >= 256
 
 
 def test_output_independent_of_batch_neighbours():

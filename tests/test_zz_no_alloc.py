@@ -83,3 +83,27 @@ def test_noalloc_reports_bad_ids_and_rejects_oversize():
     with pytest.raises(moe.MoeError) as ei:
         moe.moe_build_dispatch_noalloc(d, ids, None, *out[:4], None)
     assert ei.value.status == moe.MOE_ERR_UNSUPPORTED_SHAPE
+
+
+def test_noalloc_reserves_no_device_memory_after_the_first_call():
+    # The first call on a device may make the CUDA runtime load this library's
+    # device code and reserve the fixed array (lazy module loading); after it,
+    # calls of any accepted shape reserve nothing: the device's free memory
+    # does not move.  All outputs are allocated before the first reading.
+    shapes = [(4096, 8, 256), (17, 2, 8), (1024, 8, 128), (3000, 32, 64)]
+    bufs = []
+    for T, k, E in shapes:
+        ids = synth.random_ids(T, k, E, T).cuda()
+        w = synth.normal((T, k), T, 7, 1.0, torch.float32).cuda()
+        bufs.append((moe.desc(T, 64, E, k, 64, 0), ids, w, _outputs(T, k, E)))
+    status = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    d, ids, w, out = bufs[0]
+    moe.moe_build_dispatch_noalloc(d, ids, w, *out, status)   # warm-up call
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for rep in range(3):
+        for d, ids, w, out in bufs:
+            moe.moe_build_dispatch_noalloc(d, ids, w, *out, status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert torch.cuda.mem_get_info()[0] == free0, rep
