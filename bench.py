@@ -54,6 +54,11 @@ def parse():
                    help="--sweep: file the lines are appended to")
     p.add_argument("--sweep-configs", default="",
                    help="--sweep: comma-separated layer names to keep (default: all)")
+    p.add_argument("--sweep-max-T", type=int, default=0,
+                   help="--sweep: keep batch sizes up to this many tokens (default: all)")
+    p.add_argument("--path", default="auto", choices=["auto", "chain", "persistent"],
+                   help="execution path of the layer forward: automatic choice (default), "
+                        "the kernel chain, or the persistent single-kernel layer (T <= 16)")
     p.add_argument("--l2-flush", action="store_true",
                    help="write a 256 MB buffer before every timed step (each step then "
                         "timed alone); for layers whose working set fits in L2")
@@ -333,14 +338,27 @@ def new_events(stream, n):
     return evs
 
 
-def time_layer(moe, d, wts, x, y, ws, lay, cfg, T, steps, warmup, pg, stream, l2_flush=False):
+PATHS = {"auto": None, "chain": 1, "persistent": 2}
+
+# the persistent single-kernel layer's shapes (moe_layer_forward_ex)
+DECODE_MAX_T = 16
+
+
+def uses_persistent(cfg, T, path):
+    """Whether a forward of this shape runs as the persistent decode layer."""
+    fits = T <= DECODE_MAX_T and cfg.H >= 256
+    return path == "persistent" or (path == "auto" and fits)
+
+
+def time_layer(moe, d, wts, x, y, ws, lay, cfg, T, steps, warmup, pg, stream, l2_flush=False,
+               path=None):
     """Warm-up, then the timed region (K forwards between two events, barrier +
     synchronize on both sides), then the same K forwards with stage events and
     with per-step events.  Returns the timings, the host time per call and the
     routing counts the workspace holds afterwards."""
     import torch
     for _ in range(warmup):
-        moe.moe_layer_forward(d, wts, x, y, ws)
+        moe.moe_layer_forward(d, wts, x, y, ws, path=path)
     torch.cuda.synchronize()
     st, raw = moe.moe_get_device_status(ws)
     if st != moe.MOE_OK:
@@ -361,7 +379,7 @@ def time_layer(moe, d, wts, x, y, ws, lay, cfg, T, steps, warmup, pg, stream, l2
         for i in range(steps):
             scratch.fill_(i & 0xff)
             ev_a[i].record(stream)
-            moe.moe_layer_forward(d, wts, x, y, ws)
+            moe.moe_layer_forward(d, wts, x, y, ws, path=path)
             ev_b[i].record(stream)
         torch.cuda.synchronize()
         barrier(pg)
@@ -370,7 +388,7 @@ def time_layer(moe, d, wts, x, y, ws, lay, cfg, T, steps, warmup, pg, stream, l2
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(stream)
         for i in range(steps):
-            moe.moe_layer_forward(d, wts, x, y, ws)
+            moe.moe_layer_forward(d, wts, x, y, ws, path=path)
         end.record(stream)
         torch.cuda.synchronize()
         barrier(pg)
@@ -379,7 +397,7 @@ def time_layer(moe, d, wts, x, y, ws, lay, cfg, T, steps, warmup, pg, stream, l2
     # ---- the same K steps again with CUDA events at every stage boundary, on
     # the launching stream: per-kernel durations for the roofline ----
     for i in range(steps):
-        moe.moe_layer_forward(d, wts, x, y, ws, stage_events=stage_ev[i])
+        moe.moe_layer_forward(d, wts, x, y, ws, stage_events=stage_ev[i], path=path)
     torch.cuda.synchronize()
     t_wall1 = time.time()
     st, raw = moe.moe_get_device_status(ws)
@@ -391,7 +409,7 @@ def time_layer(moe, d, wts, x, y, ws, lay, cfg, T, steps, warmup, pg, stream, l2
     step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     step_ev[0].record(stream)
     for i in range(steps):
-        moe.moe_layer_forward(d, wts, x, y, ws)
+        moe.moe_layer_forward(d, wts, x, y, ws, path=path)
         step_ev[i + 1].record(stream)
     torch.cuda.synchronize()
     step_us = sorted(1e3 * step_ev[i].elapsed_time(step_ev[i + 1]) for i in range(steps))
@@ -404,7 +422,7 @@ def time_layer(moe, d, wts, x, y, ws, lay, cfg, T, steps, warmup, pg, stream, l2
     torch.cuda.synchronize()
     h0 = time.perf_counter()
     for _ in range(n_host):
-        moe.moe_layer_forward(d, wts, x, y, ws)
+        moe.moe_layer_forward(d, wts, x, y, ws, path=path)
     host_us = 1e6 * (time.perf_counter() - h0) / n_host
     torch.cuda.synchronize()
 
@@ -432,8 +450,17 @@ def layer_line(cfg, T, args, world, tm, pk, sampler):
     step_s = tm["ms_max"] / 1e3 / args.steps
     value = world * T / step_s
     stage_us = tm["stage_us"]
-    gu_s = stage_us["gateup"] / 1e6
-    gu_gbs = alg["gateup_bytes"] / gu_s / 1e9
+    # the persistent decode layer is one kernel (its stage events all fall at
+    # its end): its roofline is the whole layer's
+    persistent = uses_persistent(cfg, T, args.path)
+    if persistent:
+        kern = "persistent decode layer (router, dispatch, tcgen05 GEMMs, combine)"
+        kern_bytes, kern_us = alg["layer_bytes"], stage_us["route"]
+    else:
+        kern = "expert gate/up GEMM + SwiGLU (tcgen05)"
+        kern_bytes, kern_us = alg["gateup_bytes"], stage_us["gateup"]
+    gu_s = kern_us / 1e6
+    gu_gbs = kern_bytes / gu_s / 1e9
     layer_t_hbm = alg["layer_bytes"] / (pk["hbm_gbs"] * 1e9)
     layer_t_tc = alg["layer_flops"] / (pk["bf16_tflops_sustained"] * 1e12)
     layer_roof = max(layer_t_hbm, layer_t_tc)
@@ -452,11 +479,12 @@ def layer_line(cfg, T, args, world, tm, pk, sampler):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded counter-based generator; random-init weights of the layer shape)",
         "config": workload_config(cfg, T, args.l2_flush),
-        "roofline": {"bound": "hbm", "kernel": "expert gate/up GEMM + SwiGLU (tcgen05)",
+        "roofline": {"bound": "hbm", "kernel": kern,
                      "achieved": gu_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": gu_gbs / pk["hbm_gbs"], "traffic": traffic,
-                     "algorithmic_bytes": alg["gateup_bytes"], "launch_us": stage_us["gateup"],
+                     "frac": gu_gbs / pk["hbm_gbs"], "traffic": None if persistent else traffic,
+                     "algorithmic_bytes": kern_bytes, "launch_us": kern_us,
                      "peak_source": pk["source"]},
+        "path": "persistent" if persistent else "chain",
         "layer_roofline": {"bound": "hbm" if layer_t_hbm >= layer_t_tc else "tensor",
                            "roof_us": layer_roof * 1e6, "step_us": step_s * 1e6,
                            "frac": layer_roof / step_s, "bytes": alg["layer_bytes"],
@@ -470,7 +498,7 @@ def layer_line(cfg, T, args, world, tm, pk, sampler):
         "host_us_per_call": tm["host_us"],
         "routing": {"imbalance_ratio": num / den, "touched_experts": alg["touched"],
                     "near_ties": tm["near_ties"], "near_tie_gap": NEAR_TIE},
-        "gpu_launches": launches_per_step(cfg, T) * args.steps,
+        "gpu_launches": (1 if persistent else launches_per_step(cfg, T)) * args.steps,
         "clocks": sampler.summary(*tm["t_wall"]) if sampler else None,
     }
 
@@ -503,7 +531,7 @@ def run_gpu(args):
     sampler = ClockSampler(uuid) if rank == 0 else None
     time.sleep(0.5 if sampler else 0)
     tm = time_layer(moe, d, wts, inp.x, y, ws, lay, cfg, T, args.steps, args.warmup, pg, stream,
-                    args.l2_flush)
+                    args.l2_flush, PATHS[args.path])
 
     # ---- end to end: pinned host x in, host y out, through the same call ----
     # Every step copies its x from pinned host memory, runs moe_layer_forward
@@ -533,7 +561,8 @@ def run_gpu(args):
             stream.wait_event(h2d_done[b])
             if i >= 2:
                 stream.wait_event(d2h_done[b])    # y_dev[b] of step i-2 is on the host
-            moe.moe_layer_forward(d, wts, x_dev[b], y_dev[b], ws, stream=stream)
+            moe.moe_layer_forward(d, wts, x_dev[b], y_dev[b], ws, stream=stream,
+                                  path=PATHS[args.path])
             fwd_done[b].record(stream)
             s_out.wait_event(fwd_done[b])
             with torch.cuda.stream(s_out):
@@ -639,6 +668,8 @@ def run_sweep(args):
     for name, T in SWEEP:
         if only is not None and name not in only:
             continue
+        if args.sweep_max_T and T > args.sweep_max_T:
+            continue
         cfg = synth.CONFIGS[name]
         if name not in layers:
             layers.clear()
@@ -659,7 +690,7 @@ def run_sweep(args):
         sampler = ClockSampler(uuid)
         time.sleep(0.3)
         tm = time_layer(moe, d, wts, x, y, ws, lay, cfg, T, steps, args.warmup, None, stream,
-                        a.l2_flush)
+                        a.l2_flush, PATHS[args.path])
         sampler.stop()
         line = layer_line(cfg, T, a, 1, tm, pk, sampler)
         line["sweep"] = True

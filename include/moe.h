@@ -289,6 +289,51 @@ moe_status_t moe_layer_forward(const moe_layer_desc_t *d, const moe_layer_weight
                                const void *x, void *y, void *workspace, size_t ws_bytes,
                                moe_stream_t stream, moe_event_t const *stage_events);
 
+/* Execution paths of moe_layer_forward_ex. */
+enum {
+  MOE_PATH_AUTO = 0,        /* the persistent layer where it applies, else the chain */
+  MOE_PATH_KERNEL_CHAIN = 1,/* route, dispatch, gather, two GEMMs, combine: one
+                               launch per stage, linked by programmatic
+                               dependent launch */
+  MOE_PATH_PERSISTENT = 2   /* one cooperative launch for the whole layer */
+};
+
+/*
+ * moe_layer_forward_ex -- moe_layer_forward with a choice of execution path.
+ * Both paths compute the same layer (Moebius reading notes eq. (1)) and
+ * leave the same routing metadata, h and out_perm in the workspace.
+ *
+ * The persistent path runs the layer as phases and tile tasks of one
+ * cooperative kernel with one CTA per SM, the single-kernel MoE layer of the
+ * CS349D lecture 8 notes (section 6, "FlashMoE"): router logits, a bounded
+ * grid barrier, top-k gating and the counting dispatch (repeated in every
+ * CTA), the gate/up and down GEMM tiles with the K steps of all tiles split
+ * evenly over the CTAs (a down tile of expert e starts once every gate/up
+ * tile of e has written its h rows), a second grid barrier and the combine.
+ * It removes the per-stage launches that dominate decode batches.  It takes
+ * shapes with T <= 16 and H >= 256 (MOE_ERR_UNSUPPORTED_SHAPE otherwise when
+ * requested explicitly); x_perm is not written (the gate/up tiles read x
+ * directly).  Every cross-CTA wait gives up after about one second and
+ * latches a timeout (MOE_ERR_TIMEOUT from moe_get_device_status); call
+ * moe_workspace_init before the next use of that workspace.
+ * MOE_PATH_AUTO takes the persistent path for those shapes.
+ *   path: MOE_PATH_*; anything else returns MOE_ERR_INVALID_ARG.
+ *   stage_events (as moe_layer_forward): with the persistent path the first
+ *   event is recorded before the launch and all others after it.
+ */
+moe_status_t moe_layer_forward_ex(const moe_layer_desc_t *d, const moe_layer_weights_t *w,
+                                  const void *x, void *y, void *workspace, size_t ws_bytes,
+                                  moe_stream_t stream, moe_event_t const *stage_events,
+                                  int32_t path);
+
+/* Check of the persistent layer's grid barrier: a two-CTA cooperative launch
+ * waits at that barrier sized for three CTAs.  Both waits give up after about
+ * one second and latch MOE_ERR_TIMEOUT's bit 7 in the status word; the kernel
+ * returns and the context stays usable.  Call moe_workspace_init afterwards
+ * (the barrier's arrival count is left behind).  Asynchronous on `stream`;
+ * MOE_ERR_INVALID_ARG for a NULL, unaligned or too small workspace. */
+moe_status_t moe_check_bounded_grid_wait(void *workspace, size_t ws_bytes, moe_stream_t stream);
+
 /*
  * moe_build_dispatch_noalloc -- moe_build_dispatch for callers that cannot
  * allocate device memory.  The pages have no counterpart: this is an

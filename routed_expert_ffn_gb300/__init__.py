@@ -30,6 +30,10 @@ MOE_GATE_SOFTMAX_TOPK = 1
 MOE_GATE_SOFTMAX_TOPK_RENORM = 2
 MOE_GATE_SIGMOID_BIAS_RENORM = 3
 
+MOE_PATH_AUTO = 0
+MOE_PATH_KERNEL_CHAIN = 1
+MOE_PATH_PERSISTENT = 2
+
 MOE_STAGE_EVENTS = 7
 STAGE_NAMES = ("route", "dispatch", "gather", "gateup", "down", "combine")
 
@@ -90,6 +94,8 @@ def library() -> ctypes.CDLL:
         "moe_combine": ([D, P, P, P, P, P], I32),
         "moe_layer_forward": ([D, ctypes.POINTER(LayerWeights), P, P, P, S, P, P], I32),
         "moe_check_bounded_wait": ([P, S, P], I32),
+        "moe_check_bounded_grid_wait": ([P, S, P], I32),
+        "moe_layer_forward_ex": ([D, ctypes.POINTER(LayerWeights), P, P, P, S, P, P, I32], I32),
         "moe_reshard_ep_to_tp_pack": ([I32, I32, I32, I32, P, P, P, P, P], I32),
         "moe_reshard_tp_to_ep_unpack": ([I32, I32, I32, I32, P, P, P, P, P], I32),
     }
@@ -176,6 +182,14 @@ def moe_get_device_status(ws, clear: bool = True, stream=None):
     return int(st), int(raw.value)
 
 
+def moe_check_bounded_grid_wait(ws, stream=None):
+    """Launch the grid-barrier wait check (about one second on the GPU); read the
+    result with moe_get_device_status (MOE_ERR_TIMEOUT, bit 7), then call
+    moe_workspace_init."""
+    _check("moe_check_bounded_grid_wait",
+           library().moe_check_bounded_grid_wait(_ptr(ws), _nbytes(ws), _stream(stream)))
+
+
 def moe_check_bounded_wait(ws, stream=None):
     """Launch the bounded-wait check (about one second on the GPU); read the
     result with moe_get_device_status (MOE_ERR_TIMEOUT, bit 6)."""
@@ -234,18 +248,25 @@ def layer_weights(w_router, w13, w2, sel_bias=None, w13_shared=None, w2_shared=N
 
 
 def moe_layer_forward(d: LayerDesc, w: LayerWeights, x, y, ws, stream=None,
-                      stage_events: Optional[Sequence] = None):
+                      stage_events: Optional[Sequence] = None, path: int = None):
     """Whole layer forward.  ``stage_events``: None or MOE_STAGE_EVENTS torch.cuda.Event
-    objects (created with enable_timing and already recorded once) or raw handles."""
+    objects (created with enable_timing and already recorded once) or raw handles.
+    ``path``: None (moe_layer_forward, automatic choice) or one of MOE_PATH_*
+    (moe_layer_forward_ex)."""
     ev = None
     if stage_events is not None:
         if len(stage_events) != MOE_STAGE_EVENTS:
             raise ValueError(f"need {MOE_STAGE_EVENTS} events")
         ev = (ctypes.c_void_p * MOE_STAGE_EVENTS)(
             *[e if isinstance(e, int) else e.cuda_event for e in stage_events])
-    _check("moe_layer_forward", library().moe_layer_forward(
-        ctypes.byref(d), ctypes.byref(w), _ptr(x), _ptr(y), _ptr(ws), _nbytes(ws), _stream(stream),
-        ev))
+    if path is None:
+        _check("moe_layer_forward", library().moe_layer_forward(
+            ctypes.byref(d), ctypes.byref(w), _ptr(x), _ptr(y), _ptr(ws), _nbytes(ws),
+            _stream(stream), ev))
+    else:
+        _check("moe_layer_forward_ex", library().moe_layer_forward_ex(
+            ctypes.byref(d), ctypes.byref(w), _ptr(x), _ptr(y), _ptr(ws), _nbytes(ws),
+            _stream(stream), ev, int(path)))
 
 
 def workspace_view(ws, layout: Dict[str, int], name: str, dtype, shape):

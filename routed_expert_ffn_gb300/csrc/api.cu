@@ -193,9 +193,7 @@ moe_status_t moe_get_device_status(void *workspace, size_t ws_bytes, moe_stream_
     if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (raw != nullptr) *raw = (int32_t)word;
-  if (word & (kStatusTimeoutGateUp | kStatusTimeoutDown | kStatusTimeoutRouter |
-              kStatusTimeoutCheck))
-    return MOE_ERR_TIMEOUT;
+  if (word & kStatusTimeoutMask) return MOE_ERR_TIMEOUT;
   if (word & (kStatusBadExpertId | kStatusBadOffsets | kStatusRange)) return MOE_ERR_DEVICE_CHECK;
   return MOE_OK;
 }
@@ -311,9 +309,10 @@ moe_status_t moe_combine(const moe_layer_desc_t *d, const void *out_perm, const 
                                     d->has_shared_expert, bfw(y), (cudaStream_t)stream));
 }
 
-moe_status_t moe_layer_forward(const moe_layer_desc_t *d, const moe_layer_weights_t *w,
-                               const void *x, void *y, void *workspace, size_t ws_bytes,
-                               moe_stream_t stream, moe_event_t const *stage_events) {
+moe_status_t moe_layer_forward_ex(const moe_layer_desc_t *d, const moe_layer_weights_t *w,
+                                  const void *x, void *y, void *workspace, size_t ws_bytes,
+                                  moe_stream_t stream, moe_event_t const *stage_events,
+                                  int32_t path) {
   if (workspace == nullptr || w == nullptr) return MOE_ERR_INVALID_ARG;
   Layout L;
   moe_status_t st = prologue(d, workspace, ws_bytes, &L);
@@ -323,11 +322,22 @@ moe_status_t moe_layer_forward(const moe_layer_desc_t *d, const moe_layer_weight
   if (d->gating == MOE_GATE_SIGMOID_BIAS_RENORM && !ok_ptr(w->sel_bias)) return MOE_ERR_INVALID_ARG;
   if (d->has_shared_expert && (!ok_ptr(w->w13_shared) || !ok_ptr(w->w2_shared)))
     return MOE_ERR_INVALID_ARG;
+  if (path < MOE_PATH_AUTO || path > MOE_PATH_PERSISTENT) return MOE_ERR_INVALID_ARG;
+  const bool persistent_ok = decode_layer_supported(*d);
+  if (path == MOE_PATH_PERSISTENT && !persistent_ok) return MOE_ERR_UNSUPPORTED_SHAPE;
   if ((st = check_device()) != MOE_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
   auto mark = [&](int i) -> cudaError_t {
     return stage_events ? cudaEventRecord((cudaEvent_t)stage_events[i], s) : cudaSuccess;
   };
+  if (path == MOE_PATH_PERSISTENT || (path == MOE_PATH_AUTO && persistent_ok)) {
+    // the whole layer in one launch: every stage boundary is at its end
+    cudaError_t e = mark(0);
+    if (e == cudaSuccess)
+      e = launch_decode_layer(*d, *w, bf(x), bfw(y), workspace, L, s);
+    for (int i = 1; e == cudaSuccess && i < MOE_STAGE_EVENTS; ++i) e = mark(i);
+    return cuda_status(e);
+  }
   uint32_t *status = at<uint32_t>(workspace, L.status);
   float *logits = at<float>(workspace, L.logits);
   int32_t *ids = at<int32_t>(workspace, L.topk_ids);
@@ -373,6 +383,23 @@ moe_status_t moe_layer_forward(const moe_layer_desc_t *d, const moe_layer_weight
     e = launch_combine(out_perm, inv_pos, nullptr, d->T, d->k, d->H, d->has_shared_expert, bfw(y), s);
   if (e == cudaSuccess) e = mark(6);
   return cuda_status(e);
+}
+
+moe_status_t moe_layer_forward(const moe_layer_desc_t *d, const moe_layer_weights_t *w,
+                               const void *x, void *y, void *workspace, size_t ws_bytes,
+                               moe_stream_t stream, moe_event_t const *stage_events) {
+  return moe_layer_forward_ex(d, w, x, y, workspace, ws_bytes, stream, stage_events,
+                              MOE_PATH_AUTO);
+}
+
+moe_status_t moe_check_bounded_grid_wait(void *workspace, size_t ws_bytes, moe_stream_t stream) {
+  if (workspace == nullptr || ws_bytes < kStatusBlockBytes ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return MOE_ERR_INVALID_ARG;
+  moe_status_t st = check_device();
+  if (st != MOE_OK) return st;
+  return cuda_status(
+      launch_grid_wait_check(static_cast<uint32_t *>(workspace), (cudaStream_t)stream));
 }
 
 // Shared checks of the two reshard calls (the two directions take the same

@@ -1,0 +1,1003 @@
+// The whole MoE layer forward for decode batches (T <= kDecodeMaxT) in one
+// persistent, cooperative launch of one CTA per SM.
+//
+// The kernel-chain forward launches route, dispatch, gather, two GEMMs and a
+// combine; at one token the five non-GEMM launches cost about as much as the
+// whole weight stream of a small layer.  Here the stages run as phases and
+// tile tasks of one kernel, the single-kernel MoE layer idea of the CS349D
+// lecture 8 notes (section 6, "FlashMoE：把分布式 MoE 层放进一个内核": one
+// persistent kernel whose blocks take GEMM0 / GEMM1 / combine tile tasks,
+// with no per-stage launches), on one GPU:
+//
+//   A  router      s = W_r x ("MoE推理优化全景指南", "从 Dense FFN 到专家集合"):
+//                  CTA c computes the fp32 logits of experts c, c + G, ...
+//                  for all T tokens (lane-strided products, a shuffle tree,
+//                  the six warps' sums in order).
+//      grid barrier
+//   B  gating and dispatch, redundantly in every CTA (identical inputs and
+//                  code, so identical results; no second barrier): top-k
+//                  and gate weights per token (gating.cuh), then the counting
+//                  dispatch ("MoE推理优化全景指南", "Dispatch 并不是一次普通
+//                  all-to-all"): with T <= 16 each expert's tokens form a
+//                  16-bit mask, count = popcount, offsets = prefix sum, and a
+//                  token's position inside its expert's segment = popcount of
+//                  the mask below it (ascending token order).  CTA 0 writes
+//                  the routing metadata to the workspace.
+//   C  expert GEMMs as tile tasks on the tensor cores (tcgen05, TMEM, TMA):
+//                  gate/up tiles (128 gate + the same 128 up rows of one
+//                  expert's W13, K = H) take x itself as the token operand --
+//                  all T tokens, zero-filled to 16 rows, so no gather is
+//                  needed -- and write h = SiLU(gate) * up for the expert's
+//                  tokens; down tiles (256 rows of W2, K = I) take the
+//                  expert's h rows and write the gate-weighted rows of
+//                  out_perm.  The K steps of all tiles (gate/up first, then
+//                  down) are cut into G equal contiguous ranges, one per CTA
+//                  ("stream-K"), so every SM streams the same weight bytes;
+//                  a tile shared by several CTAs is finished by the last of
+//                  them to arrive, which adds the fp32 partials in CTA order.
+//                  A down tile of expert e waits (bounded) until every
+//                  gate/up tile of e has written its h rows; its weight
+//                  copies are issued before that wait.
+//      grid barrier
+//   D  combine     y[t] = sum_j out_perm[inv_pos[t, j]] (+ the shared
+//                  expert's row), fp32 in slot order, rounded once.
+//
+// Every wait (grid barrier, expert readiness, pipeline barriers) gives up
+// after kWaitLimitNs, latches kStatusTimeoutLayer in the status word and lets
+// the CTA drain and exit; the cooperative launch guarantees that all CTAs are
+// resident, which the cross-CTA waits rely on.
+#include <string.h>
+
+#include <mutex>
+
+#include "gating.cuh"
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kDThreads = 192;  // warps 0-3 epilogue, 4 TMA producer, 5 MMA
+constexpr int kDWarps = kDThreads / 32;
+constexpr uint32_t kDChunk = kBM * kBK * 2;                       // 128 rows x 64 bf16
+constexpr uint32_t kDStageA = 2 * kStageKB * kDChunk;             // 64 KB of weights
+constexpr uint32_t kDStageB = kStageKB * kDecodeMaxT * kBK * 2;   // 4 KB: 16 token rows
+constexpr uint32_t kDStage = kDStageA + kDStageB;
+constexpr int kDStages = 3;
+constexpr uint32_t kDRing = kDStages * kDStage;
+constexpr uint32_t kDTmemCols = 64;   // two buffers of two 16-column accumulators
+constexpr int kDMaxAssign = kDecodeMaxT * kMaxK;
+constexpr int kDSlotFloats = 2 * kBM * kDecodeMaxT;  // one split piece: 2 x 128 x 16 fp32
+static_assert(kStageKB == 2, "a unit of work is two K blocks");
+
+struct DecodeMaps {
+  CUtensorMap gu, gu_sh;  // W13 [E][2][I][H]: box 128 rows x 2 halves x 2 K blocks
+  CUtensorMap dn, dn_sh;  // W2 [E][H][I]: box 256 rows x 2 K blocks
+  CUtensorMap x;          // x [T][H]: box 16 rows x 2 K blocks
+  CUtensorMap h;          // h [R][I]: box 16 rows x 2 K blocks
+};
+
+struct DecodeArgs {
+  const __nv_bfloat16 *x;
+  const float *w_router, *sel_bias;
+  int T, H, E, k, I, gating, shared;
+  float *logits, *topk_w, *gap, *w_perm;
+  int32_t *ids, *counts, *offsets, *perm_src, *inv_pos;
+  __nv_bfloat16 *h;
+  __half *out_perm;
+  __nv_bfloat16 *y;
+  float *part;       // [2 * gridDim.x][kDSlotFloats] split-piece partials (per region)
+  uint32_t *status;  // the workspace status block
+};
+
+// The two regions of work (all gate/up tiles, then all down tiles), each cut
+// into Geff[r] equal contiguous unit ranges, one per CTA: every CTA streams
+// its share of the gate/up weights, then its share of the down weights.
+struct Sched {
+  int J[2], Uper[2], nt;  // tiles per segment, units per tile
+  int U[2], Geff[2];      // units of the region (< 2^24), CTAs that share it
+  int start[2], end[2];   // this CTA's unit range in each region
+};
+
+// Shared memory next to the stage ring.
+struct DSmem {
+  int32_t ids[kDMaxAssign];
+  float w[kDMaxAssign];
+  int32_t perm[kDMaxAssign];  // position -> assignment
+  int32_t inv[kDMaxAssign];   // assignment -> position
+  float wperm[kDMaxAssign];
+  uint32_t mask[kMaxE];       // tokens of each expert (bit t)
+  int32_t offs[kMaxE + 1];
+  int32_t seg_list[kMaxE + 1];  // segments with rows, in order (shared expert last)
+  float red[kDWarps][kDecodeMaxT];
+  int ntouched, last_flag, ok_flag;
+  int done_tok[kDecodeMaxT];  // tokens whose combine this CTA runs next
+  int ndone;
+  uint64_t full[kDStages], empty[kDStages], tfull[2], tempty[2], fin;
+  uint64_t rbar;  // router staging copies
+  uint32_t tmem_slot;
+  int abort_flag;
+  Sched sc;  // indexed by region at run time: kept in shared memory
+};
+constexpr size_t kDSmemBytes = 1024 + kDRing + sizeof(DSmem);
+static_assert(kDSmemBytes <= 232448, "shared memory per CTA");
+
+// One contiguous range of units (pairs of K blocks) of one tile.
+struct Piece {
+  int dn;         // region: 0 gate/up tiles, 1 down tiles
+  int seg, j;     // segment (expert; E = the shared expert) and row block
+  int p0, p1;     // units [p0, p1) of the tile
+  int tu;         // units of the tile
+  int ts;         // first unit of the tile in its region
+};
+
+__device__ __forceinline__ Piece piece_at(const Sched &sc, const int32_t *seg_list, int r,
+                                          int u) {
+  Piece p;
+  p.dn = r;
+  const int q = u / sc.Uper[r];
+  p.ts = q * sc.Uper[r];
+  p.tu = sc.Uper[r];
+  const int ti = q / sc.J[r];
+  p.seg = seg_list[ti];
+  p.j = q - ti * sc.J[r];
+  p.p0 = u - p.ts;
+  p.p1 = min(p.ts + p.tu, sc.end[r]) - p.ts;
+  return p;
+}
+
+// Walks this CTA's pieces: region 0 (gate/up), then region 1 (down).
+struct Cursor {
+  int r, u;
+};
+__device__ __forceinline__ bool next_piece(const Sched &sc, const int32_t *seg_list, Cursor &c,
+                                           Piece &p) {
+  while (c.r < 2) {
+    if (c.u < sc.end[c.r]) {
+      p = piece_at(sc, seg_list, c.r, c.u);
+      c.u = p.ts + p.p1;
+      return true;
+    }
+    if (++c.r < 2) c.u = sc.start[c.r];
+  }
+  return false;
+}
+
+// The CTA whose range of region r holds unit x: the largest c with
+// floor(c * U / Geff) <= x.
+__device__ __forceinline__ int cta_of(const Sched &sc, int r, int x) {
+  return (int)((((int64_t)x + 1) * sc.Geff[r] + sc.U[r] - 1) / sc.U[r] - 1);
+}
+
+// Grid barrier over the CTAs of the (cooperative) launch, used once per
+// launch: every CTA adds 1 to a counter with a release reduction (no reply
+// awaited) and polls it until it reaches `nblocks`; the last CTA to finish
+// the kernel clears it.  Bounded: gives up after kWaitLimitNs, or at once when
+// another CTA has latched a timeout, and then latches kStatusTimeoutLayer.
+// Called by all threads.
+__device__ bool grid_sync(uint32_t *bar, uint32_t nblocks, uint32_t *status, int *s_ok) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    bool ok = true;
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(bar) : "memory");
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 0;; ++it) {
+      if (ld_acquire_gpu(bar) >= nblocks) break;
+      if ((it & 15u) == 15u) {
+        if (ld_acquire_gpu(status) & kStatusTimeoutMask) {
+          ok = false;
+          break;
+        }
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          atomicOr(status, kStatusTimeoutLayer);
+          ok = false;
+          break;
+        }
+      }
+    }
+    *s_ok = ok ? 1 : 0;
+  }
+  __syncthreads();
+  return *s_ok != 0;
+}
+
+// Bounded wait until a counter another CTA advances reaches `target`.
+__device__ bool wait_counter(const uint32_t *cnt, uint32_t target, volatile int *abort_flag,
+                             uint32_t *status) {
+  if (ld_acquire_gpu(cnt) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (ld_acquire_gpu(cnt) >= target) return true;
+    if ((it & 15u) == 15u) {
+      if (*abort_flag || (ld_acquire_gpu(status) & kStatusTimeoutMask)) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicOr(status, kStatusTimeoutLayer);
+        return false;
+      }
+    }
+    __nanosleep(32);
+  }
+}
+
+__device__ __forceinline__ void epi_sync_d() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ bool epi_all_d(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred a, b;\n\t"
+      "setp.ne.u32 a, %1, 0;\n\t"
+      "bar.red.and.pred b, 1, 128, a;\n\t"
+      "selp.u32 %0, 1, 0, b;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)p)
+      : "memory");
+  return r != 0;
+}
+
+// Two floats rounded to bf16 (round to nearest even), packed low first.
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// Four MMAs over one 64-deep K block (16 bf16 = 32 bytes per K16 step inside
+// the 128-byte swizzled rows).
+__device__ __forceinline__ void mma_kblock(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                           uint32_t acc) {
+  umma_bf16(d, a, b, idesc, acc);
+  umma_bf16(d, a + 2, b + 2, idesc, 1u);
+  umma_bf16(d, a + 4, b + 4, idesc, 1u);
+  umma_bf16(d, a + 6, b + 6, idesc, 1u);
+}
+
+// Top-k and gate weights of every token into shared memory, one warp per
+// token (NV logits per lane, E <= 32 * NV).
+template <int NV>
+__device__ __forceinline__ void gate_tokens(const DecodeArgs &a, int T, int E, int k,
+                                            int32_t *ids, float *w, float *gap) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int t = warp; t < T; t += kDWarps) {
+    float s[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int e = lane + 32 * i;
+      s[i] = (e < E) ? __ldcg(a.logits + (size_t)t * E + e) : 0.f;
+    }
+    select_and_gate<NV>(s, lane, t, E, k, a.gating, a.sel_bias, ids, w, gap);
+  }
+}
+
+__global__ void __launch_bounds__(kDThreads, 1)
+    decode_layer_kernel(const __grid_constant__ DecodeMaps maps, const DecodeArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  DSmem &S = *reinterpret_cast<DSmem *>(ring + kDRing);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = a.T, E = a.E, k = a.k, H = a.H, I = a.I;
+  const int Na = T * k;
+  const uint32_t G = gridDim.x;
+  uint32_t *status = a.status;
+  uint32_t *gbar = status + kDecodeBarrierWord;
+  uint32_t *piece_cnt = status + kDecodePieceWord;
+  uint32_t *seg_done = status + kDecodeSegWord;
+  uint32_t *tok_cnt = status + kDecodeTokWord;  // [T][H/256] row-block arrivals
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kDStages; ++i) {
+      mbar_init(&S.full[i], 1);
+      mbar_init(&S.empty[i], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&S.tfull[b], 1);
+      mbar_init(&S.tempty[b], 4);
+    }
+    mbar_init(&S.fin, 1);
+    mbar_init(&S.rbar, 1);
+    S.abort_flag = 0;
+    S.ndone = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&S.tmem_slot, kDTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&maps.gu);
+    tma_prefetch_desc(&maps.gu_sh);
+    tma_prefetch_desc(&maps.dn);
+    tma_prefetch_desc(&maps.dn_sh);
+    tma_prefetch_desc(&maps.x);
+    tma_prefetch_desc(&maps.h);
+  }
+
+  __syncthreads();  // barriers initialised before any thread waits on one
+
+  // ---------------------------------------------------- A: router logits --
+  // Work items are (expert e, group of tokens), at most about one per CTA:
+  // the W_r row of e and the group's x rows are staged in shared memory (the
+  // stage ring, idle until the GEMM phase) by bulk copies, in chunks of H
+  // that fit, then every thread accumulates a strided part of H for every
+  // token of the group; warp sums, then the six warps' sums in order.
+  {
+    const int per_e = max(1, (int)G / E);           // items per expert
+    const int tpc = (T + per_e - 1) / per_e;        // tokens per item
+    const int ngrp = (T + tpc - 1) / tpc;
+    uint32_t rph = 0;
+    for (int item = blockIdx.x; item < E * ngrp; item += G) {
+      const int e = item / ngrp, t0 = (item - e * ngrp) * tpc;
+      const int nt = min(tpc, T - t0);
+      // H chunk: (nt rows of bf16 + one row of fp32) per column fits the ring
+      int hc = (int)(kDRing / (uint32_t)(2 * nt + 4)) & ~63;
+      if (hc > H) hc = H;
+      float acc[kDecodeMaxT];
+#pragma unroll
+      for (int t = 0; t < kDecodeMaxT; ++t) acc[t] = 0.f;
+      float *sw = reinterpret_cast<float *>(ring);
+      uint16_t *sx = reinterpret_cast<uint16_t *>(ring + (size_t)hc * 4);
+      for (int h0 = 0; h0 < H; h0 += hc) {
+        const int hn = min(hc, H - h0);
+        if (threadIdx.x == 0) {
+          mbar_arrive_expect_tx(&S.rbar, (uint32_t)hn * (4 + 2 * nt));
+          bulk_load(sw, a.w_router + (size_t)e * H + h0, (uint32_t)hn * 4, &S.rbar);
+          for (int t = 0; t < nt; ++t)
+            bulk_load(sx + (size_t)t * hc, a.x + (size_t)(t0 + t) * H + h0, (uint32_t)hn * 2,
+                      &S.rbar);
+        }
+        if (!mbar_wait(&S.rbar, rph, &S.abort_flag, status, kStatusTimeoutLayer)) break;
+        rph ^= 1u;
+        for (int hh = threadIdx.x * 4; hh < hn; hh += kDThreads * 4) {
+          const float4 wv = *reinterpret_cast<const float4 *>(sw + hh);
+#pragma unroll
+          for (int t = 0; t < kDecodeMaxT; ++t) {
+            if (t < nt) {
+              const uint2 raw = *reinterpret_cast<const uint2 *>(sx + (size_t)t * hc + hh);
+              // bf16 -> fp32 is exact: the bf16 bits are the top half
+              float v = acc[t];
+              v = fmaf(wv.x, __uint_as_float(raw.x << 16), v);
+              v = fmaf(wv.y, __uint_as_float(raw.x & 0xffff0000u), v);
+              v = fmaf(wv.z, __uint_as_float(raw.y << 16), v);
+              v = fmaf(wv.w, __uint_as_float(raw.y & 0xffff0000u), v);
+              acc[t] = v;
+            }
+          }
+        }
+        // the chunk is consumed (generic reads ordered before the next bulk
+        // copy's writes to the same shared memory) before the next copy lands
+        fence_proxy_async_shared();
+        __syncthreads();
+      }
+#pragma unroll
+      for (int t = 0; t < kDecodeMaxT; ++t) {
+        if (t < nt) {
+          const float v = warp_sum(acc[t]);
+          if (lane == 0) S.red[warp][t] = v;
+        }
+      }
+      __syncthreads();
+      if (warp == 0 && lane < nt) {
+        float v = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < kDWarps; ++ww) v += S.red[ww][lane];
+        a.logits[(size_t)(t0 + lane) * E + e] = v;
+      }
+      __syncthreads();
+    }
+  }
+  bool ok = grid_sync(gbar, G, status, &S.ok_flag);
+
+  // ------------------------------------------- B: gating and dispatch --
+  if (ok) {
+    const int nv = (E + 31) / 32;
+    float *gap_out = blockIdx.x == 0 ? a.gap : nullptr;
+    if (nv <= 1)
+      gate_tokens<1>(a, T, E, k, S.ids, S.w, gap_out);
+    else if (nv <= 2)
+      gate_tokens<2>(a, T, E, k, S.ids, S.w, gap_out);
+    else if (nv <= 4)
+      gate_tokens<4>(a, T, E, k, S.ids, S.w, gap_out);
+    else if (nv <= 8)
+      gate_tokens<8>(a, T, E, k, S.ids, S.w, gap_out);
+    else
+      gate_tokens<16>(a, T, E, k, S.ids, S.w, gap_out);
+    __syncthreads();
+    if (warp == 0) {
+      // the counting dispatch in one warp: per-expert token masks (the k
+      // experts of a token are distinct), counts and offsets by a warp scan
+      // over lane-owned expert ranges, then every assignment's position
+      for (int e = lane; e < E; e += 32) S.mask[e] = 0u;
+      __syncwarp();
+      for (int i = lane; i < Na; i += 32) atomicOr(&S.mask[S.ids[i]], 1u << (i / k));
+      __syncwarp();
+      const int per = (E + 31) / 32;
+      int sum = 0, nf = 0;
+      for (int q = 0; q < per; ++q) {
+        const int e = lane * per + q;
+        if (e < E) {
+          const int c = __popc(S.mask[e]);
+          sum += c;
+          nf += c > 0 ? 1 : 0;
+        }
+      }
+      int incl = sum, inclf = nf;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        const int uf = __shfl_up_sync(0xffffffffu, inclf, o);
+        if (lane >= o) {
+          incl += u;
+          inclf += uf;
+        }
+      }
+      int run = incl - sum, frun = inclf - nf;
+      for (int q = 0; q < per; ++q) {
+        const int e = lane * per + q;
+        if (e < E) {
+          const int c = __popc(S.mask[e]);
+          S.offs[e] = run;
+          if (c > 0) S.seg_list[frun++] = e;
+          run += c;
+        }
+      }
+      if (lane == 31) {
+        S.offs[E] = Na;
+        int n = inclf;
+        if (a.shared) S.seg_list[n++] = E;
+        S.ntouched = n;
+      }
+      __syncwarp();
+      for (int i = lane; i < Na; i += 32) {
+        const int e = S.ids[i], t = i / k;
+        const int pos = S.offs[e] + __popc(S.mask[e] & ((1u << t) - 1u));
+        S.perm[pos] = i;
+        S.inv[i] = pos;
+        S.wperm[pos] = S.w[i];
+      }
+    }
+    __syncthreads();
+    if (blockIdx.x == 0) {
+      for (int i = threadIdx.x; i < Na; i += kDThreads) {
+        a.ids[i] = S.ids[i];
+        a.topk_w[i] = S.w[i];
+        a.perm_src[i] = S.perm[i];
+        a.inv_pos[i] = S.inv[i];
+        a.w_perm[i] = S.wperm[i];
+      }
+      for (int e = threadIdx.x; e <= E; e += kDThreads) {
+        a.offsets[e] = S.offs[e];
+        if (e < E) a.counts[e] = __popc(S.mask[e]);
+      }
+    }
+  }
+
+  // ------------------------------------------------ C: expert GEMM tiles --
+  if (threadIdx.x == 0) {
+    Sched &w = S.sc;
+    w.J[0] = (I + kBM - 1) / kBM;            // gate/up: 128 h columns per tile
+    w.Uper[0] = (H / kBK + 1) / 2;           // K = H
+    w.J[1] = (H + 2 * kBM - 1) / (2 * kBM);  // down: 256 W2 rows per tile
+    w.Uper[1] = (I / kBK + 1) / 2;           // K = I
+    w.nt = ok ? S.ntouched : 0;
+    for (int r = 0; r < 2; ++r) {
+      w.U[r] = w.nt * w.J[r] * w.Uper[r];
+      w.Geff[r] = min((int)G, w.U[r]);
+      if ((int)blockIdx.x < w.Geff[r]) {
+        w.start[r] = (int)((int64_t)blockIdx.x * w.U[r] / w.Geff[r]);
+        w.end[r] = (int)(((int64_t)blockIdx.x + 1) * w.U[r] / w.Geff[r]);
+      } else {
+        w.start[r] = w.end[r] = w.U[r];
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = S.tmem_slot;
+  const Sched &sc = S.sc;
+  const int JG = sc.J[0];
+  auto seg_row = [&](int s) { return s < E ? S.offs[s] : Na; };
+  auto seg_rows = [&](int s) { return s < E ? S.offs[s + 1] - S.offs[s] : T; };
+
+  if (warp == 4) {
+    // ---------------------------------------------------- TMA producer --
+    if (lane == 0) {
+      uint32_t st = 0, ph = 0, issued = 0;
+      bool pok = true;
+      // token-row copies of down units queued until their expert's h is
+      // complete (their weight copies are already in flight)
+      int nq = 0;
+      uint32_t q_st[kDStages];
+      int q_seg[kDStages], q_row[kDStages], q_kb[kDStages];
+      int ready = -1;  // last segment seen complete
+      auto flush = [&]() -> bool {
+        for (int i = 0; i < nq; ++i) {
+          if (q_seg[i] != ready) {
+            if (!wait_counter(seg_done + q_seg[i], (uint32_t)JG, &S.abort_flag, status))
+              return false;
+            ready = q_seg[i];
+            fence_proxy_async_global();
+          }
+          tma_load_3d(ring + q_st[i] * kDStage + kDStageA, &maps.h, &S.full[q_st[i]], 0, q_row[i],
+                      q_kb[i]);
+        }
+        nq = 0;
+        return true;
+      };
+      Cursor cur = {0, sc.start[0]};
+      Piece pc;
+      while (pok && next_piece(sc, S.seg_list, cur, pc)) {
+        const bool sh = pc.seg >= E;
+        const CUtensorMap *ma =
+            pc.dn ? (sh ? &maps.dn_sh : &maps.dn) : (sh ? &maps.gu_sh : &maps.gu);
+        const int ecoord = sh ? 0 : pc.seg;
+        const int arow = pc.dn ? pc.j * 2 * kBM : pc.j * kBM;
+        const int row0 = seg_row(pc.seg);
+        for (int v = pc.p0; v < pc.p1; ++v) {
+          const int kb = 2 * v;
+          if (nq > 0 && issued >= (uint32_t)kDStages && !flush()) {
+            pok = false;
+            break;
+          }
+          if (!mbar_wait(&S.empty[st], ph ^ 1u, &S.abort_flag, status, kStatusTimeoutLayer)) {
+            pok = false;
+            break;
+          }
+          uint8_t *dst = ring + st * kDStage;
+          mbar_arrive_expect_tx(&S.full[st], kDStage);
+          tma_load_5d(dst, ma, &S.full[st], 0, arow, 0, kb, ecoord);
+          if (!pc.dn) {
+            tma_load_3d(dst + kDStageA, &maps.x, &S.full[st], 0, 0, kb);
+          } else {
+            if (pc.seg != ready && nq == 0 &&
+                ld_acquire_gpu(seg_done + pc.seg) >= (uint32_t)JG) {
+              ready = pc.seg;
+              fence_proxy_async_global();
+            }
+            if (pc.seg == ready && nq == 0) {
+              tma_load_3d(dst + kDStageA, &maps.h, &S.full[st], 0, row0, kb);
+            } else {
+              q_st[nq] = st;
+              q_seg[nq] = pc.seg;
+              q_row[nq] = row0;
+              q_kb[nq] = kb;
+              ++nq;
+            }
+          }
+          ++issued;
+          if (++st == (uint32_t)kDStages) {
+            st = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (pok && nq > 0) pok = flush();
+      // drain: every issued copy lands before the CTA may exit
+      const uint32_t n = issued < (uint32_t)kDStages ? issued : (uint32_t)kDStages;
+      for (uint32_t i = 0; i < n; ++i) {
+        st = st == 0 ? kDStages - 1 : st - 1;
+        if (st == (uint32_t)kDStages - 1) ph ^= 1u;
+        mbar_wait_drain(&S.full[st], ph);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------------ MMA issuer --
+    if (lane == 0) {
+      uint32_t st = 0, ph = 0, tl = 0;
+      bool mok = true;
+      const uint64_t desc0 = sdesc_k_sw128(smem_u32(ring));
+      const uint32_t id = idesc_bf16_f32(kBM, kDecodeMaxT);
+      Cursor cur = {0, sc.start[0]};
+      Piece pc;
+      for (; mok && next_piece(sc, S.seg_list, cur, pc); ++tl) {
+        const uint32_t buf = tl & 1u, use = tl >> 1;
+        if (!mbar_wait(&S.tempty[buf], (use & 1u) ^ 1u, &S.abort_flag, status,
+                       kStatusTimeoutLayer))
+          break;
+        tc_fence_after();
+        const uint32_t d0 = tmem_base + buf * 32u;
+        for (int v = pc.p0; v < pc.p1; ++v) {
+          if (!mbar_wait(&S.full[st], ph, &S.abort_flag, status, kStatusTimeoutLayer)) {
+            mok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = desc0 + st * (kDStage >> 4);
+          const uint64_t bdesc = adesc + (kDStageA >> 4);
+#pragma unroll
+          for (int c = 0; c < kStageKB; ++c) {
+            const uint32_t acc = (v != pc.p0 || c != 0) ? 1u : 0u;
+            const uint64_t ac = adesc + c * ((2 * kDChunk) >> 4);
+            const uint64_t bc = bdesc + c * ((kDecodeMaxT * kBK * 2) >> 4);
+            // gate/up: gate rows, then up rows; down: W2 rows [0,128), [128,256)
+            mma_kblock(d0, ac, bc, id, acc);
+            mma_kblock(d0 + 16, ac + (kDChunk >> 4), bc, id, acc);
+          }
+          umma_commit(&S.empty[st]);
+          if (++st == (uint32_t)kDStages) {
+            st = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!mok) break;
+        umma_commit(&S.tfull[buf]);
+      }
+      umma_commit(&S.fin);
+      mbar_wait_drain(&S.fin, 0);
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------- epilogue --
+    const int r = warp * 32 + lane;  // TMEM lane = weight row of the tile
+    uint32_t tl = 0;
+    bool range_bad = false;
+    Cursor cur = {0, sc.start[0]};
+    Piece pc;
+    for (; next_piece(sc, S.seg_list, cur, pc); ++tl) {
+      const uint32_t buf = tl & 1u, use = tl >> 1;
+      const bool waited =
+          mbar_wait(&S.tfull[buf], use & 1u, &S.abort_flag, status, kStatusTimeoutLayer);
+      if (!epi_all_d(waited && !S.abort_flag)) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + ((uint32_t)(warp * 32) << 16) + buf * 32u;
+      uint32_t v0[16], v1[16];
+      tmem_ld16(tb, v0);
+      tmem_ld16(tb + 16, v1);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.tempty[buf]);  // the accumulator buffer is free
+      float g[16], uu[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        g[q] = __uint_as_float(v0[q]);
+        uu[q] = __uint_as_float(v1[q]);
+      }
+      const int s = pc.seg, row0 = seg_row(s), m = seg_rows(s);
+      if (!(pc.p0 == 0 && pc.p1 == pc.tu)) {
+        // A piece of a tile shared by CTAs c0..c1 (c0 holds the tile's first
+        // units, at the end of its range: its piece comes last in time; the
+        // others hold pieces at the start of theirs).  c1..c0+1 store the
+        // fp32 partial of the live token columns (gate/up: the T tokens,
+        // down: the segment's m rows) and signal with a release reduction;
+        // c0 waits (bounded) for the c1 - c0 signals and adds the partials
+        // to its own in CTA order.  No wait points to a piece that waits.
+        const int ncol4 = ((pc.dn ? m : T) + 3) & ~3;
+        const int c0 = cta_of(sc, pc.dn, pc.ts), c1 = cta_of(sc, pc.dn, pc.ts + pc.tu - 1);
+        uint32_t *cnt = piece_cnt + pc.dn * kDecodeMaxCtas + c0;
+        const size_t base = (size_t)pc.dn * kDSlotFloats + (size_t)r * 32;
+        if ((int)blockIdx.x != c0) {
+          float *mine = a.part + (size_t)(2 * blockIdx.x) * kDSlotFloats + base;
+#pragma unroll
+          for (int q = 0; q < 16; q += 4) {
+            if (q < ncol4) {
+              *reinterpret_cast<float4 *>(mine + q) =
+                  make_float4(g[q], g[q + 1], g[q + 2], g[q + 3]);
+              *reinterpret_cast<float4 *>(mine + 16 + q) =
+                  make_float4(uu[q], uu[q + 1], uu[q + 2], uu[q + 3]);
+            }
+          }
+          // release: the barrier orders every thread's partial before
+          // thread 0's release reduction
+          epi_sync_d();
+          if (r == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(cnt) : "memory");
+          continue;
+        }
+        // acquire: thread 0 sees all c1 - c0 signals, then the barrier
+        // orders the reads below after its acquire
+        if (r == 0) {
+          const bool got = wait_counter(cnt, (uint32_t)(c1 - c0), &S.abort_flag, status);
+          S.last_flag = got ? 1 : 0;
+          if (got) *cnt = 0u;  // every signal of this launch has arrived
+        }
+        epi_sync_d();
+        if (!S.last_flag) continue;
+        // add the other pieces in CTA order; four slots' loads in flight
+#pragma unroll
+        for (int q = 0; q < 16; q += 4) {
+          if (q < ncol4) {
+            float4 ag = make_float4(g[q], g[q + 1], g[q + 2], g[q + 3]);
+            float4 au = make_float4(uu[q], uu[q + 1], uu[q + 2], uu[q + 3]);
+            for (int cc = c0 + 1; cc <= c1; cc += 4) {
+              float4 lg[4], lu[4];
+#pragma unroll
+              for (int z = 0; z < 4; ++z) {
+                lg[z] = lu[z] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (cc + z <= c1) {
+                  const float *pp = a.part + (size_t)(2 * (cc + z)) * kDSlotFloats + base + q;
+                  lg[z] = __ldcg(reinterpret_cast<const float4 *>(pp));
+                  lu[z] = __ldcg(reinterpret_cast<const float4 *>(pp + 16));
+                }
+              }
+#pragma unroll
+              for (int z = 0; z < 4; ++z) {
+                if (cc + z <= c1) {
+                  ag.x += lg[z].x;
+                  ag.y += lg[z].y;
+                  ag.z += lg[z].z;
+                  ag.w += lg[z].w;
+                  au.x += lu[z].x;
+                  au.y += lu[z].y;
+                  au.z += lu[z].z;
+                  au.w += lu[z].w;
+                }
+              }
+            }
+            g[q] = ag.x;
+            g[q + 1] = ag.y;
+            g[q + 2] = ag.z;
+            g[q + 3] = ag.w;
+            uu[q] = au.x;
+            uu[q + 1] = au.y;
+            uu[q + 2] = au.z;
+            uu[q + 3] = au.w;
+          }
+        }
+      }
+      if (!pc.dn) {
+        // h[row0 + n][j*128 + r] = SiLU(gate) * up of the segment's n-th token
+        const int col = pc.j * kBM + r;
+#pragma unroll
+        for (int n = 0; n < kDecodeMaxT; ++n) {
+          if (n < m) {
+            const int t = s < E ? S.perm[row0 + n] / k : n;
+            float gv = 0.f, uv = 0.f;
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              gv = (q == t) ? g[q] : gv;
+              uv = (q == t) ? uu[q] : uv;
+            }
+            if (col < I)
+              a.h[(size_t)(row0 + n) * I + col] =
+                  __float2bfloat16_rn(gv / (1.0f + __expf(-gv)) * uv);
+          }
+        }
+        // h is read by tensor copies (async proxy) of other CTAs' down tiles:
+        // each writer orders its stores for the async proxy, the barrier
+        // orders them before thread 0's release of the readiness count
+        fence_proxy_async_global();
+        epi_sync_d();
+        if (r == 0)
+          asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(seg_done + s) : "memory");
+      } else {
+        // out_perm[row0 + n][j*256 + half*128 + r] = w_perm * (W2 h)
+#pragma unroll
+        for (int n = 0; n < kDecodeMaxT; ++n) {
+          if (n < m) {
+            const int pos = row0 + n;
+            const float wv = pos < Na ? S.wperm[pos] : 1.0f;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const int col = pc.j * 2 * kBM + hh * kBM + r;
+              const float val = (hh ? uu[n] : g[n]) * wv;
+              range_bad |= !(fabsf(val) <= 65504.0f);
+              if (col < H)
+                a.out_perm[(size_t)pos * H + col] =
+                    __float2half_rn(fminf(fmaxf(val, -65504.0f), 65504.0f));
+            }
+          }
+        }
+        // One arrival per token of the segment on the counter of (token,
+        // this tile's 256 columns); the arrival that completes one (all k
+        // routed rows, and the shared row, of those columns written) makes
+        // this CTA combine those columns of that token.  Release: the
+        // barrier orders every thread's rows before the arriving threads'
+        // fences; acquire: the completing thread's fence after its arrival.
+        epi_sync_d();
+        if (r < m) {
+          const int t = s < E ? S.perm[row0 + r] / k : r;
+          const uint32_t target = (uint32_t)(k + a.shared);
+          __threadfence();
+          if (atomicInc(tok_cnt + t * sc.J[1] + pc.j, target - 1) == target - 1) {  // wraps to 0
+            __threadfence();
+            S.done_tok[atomicAdd(&S.ndone, 1)] = t;
+          }
+        }
+        epi_sync_d();
+        // D: combine, y[t, cols] = sum_j out_perm[inv_pos[t, j], cols] (+ the
+        // shared expert's row), fp32 in slot order, rounded once: 32 vectors
+        // of 8 columns per token, eight rows' loads in flight per vector
+        const int ndone = S.ndone;
+        const int nrow = k + a.shared;
+        for (int task = r; task < ndone * 32; task += 128) {
+          const int t = S.done_tok[task >> 5];
+          const int col = pc.j * 2 * kBM + (task & 31) * 8;
+          if (col >= H) continue;
+          float acc[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+          for (int j0 = 0; j0 < nrow; j0 += 8) {
+            uint4 raw[8];
+#pragma unroll
+            for (int z = 0; z < 8; ++z) {
+              const int jj = j0 + z;
+              if (jj < nrow) {
+                const int pos = jj < k ? S.inv[t * k + jj] : Na + t;
+                raw[z] = __ldcg(reinterpret_cast<const uint4 *>(a.out_perm + (size_t)pos * H + col));
+              }
+            }
+#pragma unroll
+            for (int z = 0; z < 8; ++z) {
+              if (j0 + z < nrow) {
+                const uint32_t wd[4] = {raw[z].x, raw[z].y, raw[z].z, raw[z].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&wd[q]));
+                  acc[2 * q] += f.x;
+                  acc[2 * q + 1] += f.y;
+                }
+              }
+            }
+          }
+          uint4 o;
+          o.x = bf16x2_bits(acc[0], acc[1]);
+          o.y = bf16x2_bits(acc[2], acc[3]);
+          o.z = bf16x2_bits(acc[4], acc[5]);
+          o.w = bf16x2_bits(acc[6], acc[7]);
+          *reinterpret_cast<uint4 *>(a.y + (size_t)t * H + col) = o;
+        }
+        epi_sync_d();
+        if (r == 0) S.ndone = 0;
+      }
+    }
+    if (range_bad) atomicOr(status, kStatusRange);
+  }
+
+  // The last CTA to finish clears the grid barrier and the readiness
+  // counters: every CTA has passed the barrier and its last readiness check
+  // by then.
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicInc(gbar + 2, G - 1) == G - 1) {  // wraps to 0
+      __threadfence();
+      gbar[0] = 0u;
+      for (int i = 0; i < sc.nt; ++i) seg_done[S.seg_list[i]] = 0u;
+    }
+  }
+
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kDTmemCols);
+  }
+}
+
+// Both CTAs of a two-CTA cooperative launch wait at a grid barrier sized for
+// three: the waits run out and latch kStatusTimeoutLayer.
+__global__ void __launch_bounds__(32) grid_wait_check_kernel(uint32_t *status) {
+  __shared__ int s_ok;
+  grid_sync(status + kDecodeBarrierWord, gridDim.x + 1, status, &s_ok);
+  // (the barrier's count is left at gridDim.x: moe_workspace_init clears it)
+}
+
+// Tensor maps of one launch, cached by everything they depend on.
+struct DecodeKey {
+  int dev, T, H, E, I, k, shared;
+  const void *w13, *w2, *w13s, *w2s, *x, *h;
+  bool operator==(const DecodeKey &o) const { return memcmp(this, &o, sizeof o) == 0; }
+};
+
+bool decode_maps(const DecodeKey &key, DecodeMaps *out) {
+  constexpr int kSlots = 8;
+  static DecodeKey keys[kSlots];
+  static DecodeMaps maps[kSlots];
+  static bool used[kSlots] = {};
+  static int next = 0;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < kSlots; ++i)
+    if (used[i] && keys[i] == key) {
+      *out = maps[i];
+      return true;
+    }
+  DecodeMaps m;
+  const int64_t R = (int64_t)key.T * key.k + (key.shared ? key.T : 0);
+  if (!weight_map(&m.gu, key.w13, key.H, key.I, 2, key.E, kBM)) return false;
+  if (!weight_map(&m.dn, key.w2, key.I, key.H, 1, key.E, 2 * kBM)) return false;
+  if (key.shared) {
+    if (!weight_map(&m.gu_sh, key.w13s, key.H, key.I, 2, 1, kBM)) return false;
+    if (!weight_map(&m.dn_sh, key.w2s, key.I, key.H, 1, 1, 2 * kBM)) return false;
+  } else {
+    m.gu_sh = m.gu;
+    m.dn_sh = m.dn;
+  }
+  if (!act_map(&m.x, key.x, key.H, key.T, kDecodeMaxT)) return false;
+  if (!act_map(&m.h, key.h, key.I, R, kDecodeMaxT)) return false;
+  keys[next] = key;
+  maps[next] = m;
+  used[next] = true;
+  next = (next + 1) % kSlots;
+  *out = m;
+  return true;
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_cooperative(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                               cudaStream_t s, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+}  // namespace
+
+bool decode_layer_supported(const moe_layer_desc_t &d) {
+  return d.T <= kDecodeMaxT && d.H >= 2 * kBM && (int64_t)d.T * d.k <= kDMaxAssign &&
+         num_sms() <= kDecodeMaxCtas;
+}
+
+cudaError_t launch_decode_layer(const moe_layer_desc_t &d, const moe_layer_weights_t &w,
+                                const __nv_bfloat16 *x, __nv_bfloat16 *y, void *workspace,
+                                const Layout &L, cudaStream_t s) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  DecodeKey key;
+  memset(&key, 0, sizeof key);
+  key.dev = dev;
+  key.T = d.T;
+  key.H = d.H;
+  key.E = d.E;
+  key.I = d.I;
+  key.k = d.k;
+  key.shared = d.has_shared_expert ? 1 : 0;
+  key.w13 = w.w13;
+  key.w2 = w.w2;
+  key.w13s = key.shared ? w.w13_shared : nullptr;
+  key.w2s = key.shared ? w.w2_shared : nullptr;
+  key.x = x;
+  key.h = ws + L.h;
+  DecodeMaps maps;
+  if (!decode_maps(key, &maps)) return cudaErrorInvalidValue;
+  DecodeArgs a;
+  a.x = x;
+  a.w_router = w.w_router;
+  a.sel_bias = w.sel_bias;
+  a.T = d.T;
+  a.H = d.H;
+  a.E = d.E;
+  a.k = d.k;
+  a.I = d.I;
+  a.gating = d.gating;
+  a.shared = key.shared;
+  a.logits = reinterpret_cast<float *>(ws + L.logits);
+  a.topk_w = reinterpret_cast<float *>(ws + L.topk_w);
+  a.gap = reinterpret_cast<float *>(ws + L.gap);
+  a.w_perm = reinterpret_cast<float *>(ws + L.w_perm);
+  a.ids = reinterpret_cast<int32_t *>(ws + L.topk_ids);
+  a.counts = reinterpret_cast<int32_t *>(ws + L.counts);
+  a.offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
+  a.perm_src = reinterpret_cast<int32_t *>(ws + L.perm_src);
+  a.inv_pos = reinterpret_cast<int32_t *>(ws + L.inv_pos);
+  a.h = reinterpret_cast<__nv_bfloat16 *>(ws + L.h);
+  a.out_perm = reinterpret_cast<__half *>(ws + L.out_perm);
+  a.y = y;
+  a.part = reinterpret_cast<float *>(ws + L.split_part);
+  a.status = reinterpret_cast<uint32_t *>(ws + L.status);
+  static bool configured[64] = {};
+  if (!configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(decode_layer_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kDSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  return launch_cooperative(decode_layer_kernel, dim3(num_sms()), dim3(kDThreads), kDSmemBytes, s,
+                            maps, a);
+}
+
+cudaError_t launch_grid_wait_check(uint32_t *status_block, cudaStream_t s) {
+  return launch_cooperative(grid_wait_check_kernel, dim3(2), dim3(32), 0, s, status_block);
+}
+
+}  // namespace moe

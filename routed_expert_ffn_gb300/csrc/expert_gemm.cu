@@ -682,6 +682,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- host --
 
+}  // namespace
+
 // Weight map: W viewed as [E][P][rows][K] (P = 2 halves of W13, or 1 for
 // W2) with K split into 64-element blocks, the block index ordered after the
 // rows: dims {64, rows, P, K/64, E}.  A box [kStageKB][P][box_rows][64] lands
@@ -703,6 +705,8 @@ bool act_map(CUtensorMap *m, const void *a, int K, int64_t R, int box_rows) {
   const cuuint32_t box[3] = {(cuuint32_t)kBK, (cuuint32_t)box_rows, (cuuint32_t)kStageKB};
   return encode_bf16_map(m, a, 3, dims, strides, box);
 }
+
+namespace {
 
 // The tensor maps of one GEMM launch.  Encoding them takes host time on every
 // call (about 20 cuTensorMapEncodeTiled calls per GEMM), so the sets of recent

@@ -98,6 +98,10 @@ constexpr uint32_t kStatusBadOffsets = 1u << 3;
 constexpr uint32_t kStatusTimeoutRouter = 1u << 4;
 constexpr uint32_t kStatusRange = 1u << 5;  // a gate-weighted expert output beyond fp16 range
 constexpr uint32_t kStatusTimeoutCheck = 1u << 6;  // the bounded-wait check ran out (expected)
+constexpr uint32_t kStatusTimeoutLayer = 1u << 7;  // a wait of the persistent decode layer ran out
+constexpr uint32_t kStatusTimeoutMask =
+    kStatusTimeoutGateUp | kStatusTimeoutDown | kStatusTimeoutRouter | kStatusTimeoutCheck |
+    kStatusTimeoutLayer;
 
 // A bounded pipeline wait gives up after this long (the longest legitimate
 // wait is one tile's mainloop, well under a millisecond).
@@ -139,7 +143,25 @@ inline int plan_ints(int nseg) { return 3 * (nseg + 1) + 4; }
 constexpr int kSplitMaxRows = 32;
 constexpr int kMaxSplit = 16;
 constexpr int kMaxSplitTiles = 1024;
-constexpr size_t kStatusBlockBytes = 256 + 2 * kMaxSplitTiles * 4;
+
+// Persistent decode layer (decode_layer.cu): batches of up to kDecodeMaxT
+// tokens run the whole layer in one cooperative launch of one CTA per SM.
+// Its counters follow the split-K counters in the status block: the grid
+// barrier's arrival count, a count of finished CTAs, one arrival counter per
+// (token, 256 output columns) (their combine runs when all of the token's
+// rows of those columns are written), one arrival counter per CTA and
+// work region (gate/up, down) for the pieces of a tile split between CTAs,
+// and one readiness counter per segment
+// (gate/up tiles finished).  Each returns to zero by the end of the launch
+// (the generation only ever grows).
+constexpr int kDecodeMaxT = 16;
+constexpr int kDecodeMaxCtas = 256;
+// words: +0 grid barrier arrivals, +2 finished CTAs
+constexpr int kDecodeBarrierWord = kSplitCounterWord + 2 * kMaxSplitTiles;
+constexpr int kDecodePieceWord = kDecodeBarrierWord + 32;
+constexpr int kDecodeSegWord = kDecodePieceWord + 2 * kDecodeMaxCtas;
+constexpr int kDecodeTokWord = kDecodeSegWord + kMaxE + 16;  // [16][H/256 <= 64]
+constexpr size_t kStatusBlockBytes = (size_t)(kDecodeTokWord + kDecodeMaxT * 64) * 4;
 
 // ------------------------------------------------------ argument checks --
 // Host-side validation shared by every entry point (api.cu, noalloc.cu):
@@ -203,6 +225,21 @@ cudaError_t launch_expert_down(const moe_layer_desc_t &d, const void *w2, const 
 cudaError_t launch_combine(const __half *out_perm, const int32_t *inv_pos,
                            const float *topk_w, int T, int k, int H, int shared, __nv_bfloat16 *y,
                            cudaStream_t s);
+// The persistent decode layer (decode_layer.cu): the whole forward in one
+// cooperative launch for shapes decode_layer_supported accepts.
+bool decode_layer_supported(const moe_layer_desc_t &d);
+cudaError_t launch_decode_layer(const moe_layer_desc_t &d, const moe_layer_weights_t &w,
+                                const __nv_bfloat16 *x, __nv_bfloat16 *y, void *workspace,
+                                const Layout &L, cudaStream_t s);
+// Two CTAs of one cooperative launch meet at the decode layer's grid barrier
+// sized for three: both waits run out after kWaitLimitNs and latch
+// kStatusTimeoutLayer (decode_layer.cu).
+cudaError_t launch_grid_wait_check(uint32_t *status_block, cudaStream_t s);
+// Tensor maps of the expert GEMMs (expert_gemm.cu): weights [E][P][rows][K]
+// as {64, rows, P, K/64, E} with boxes of box_rows rows and kStageKB K
+// blocks; token rows [R][K] as {64, R, K/64} with boxes of box_rows rows.
+bool weight_map(CUtensorMap *m, const void *w, int K, int rows, int P, int E, int box_rows);
+bool act_map(CUtensorMap *m, const void *a, int K, int64_t R, int box_rows);
 // One thread waits on an mbarrier nothing arrives on (waitcheck.cu).
 cudaError_t launch_bounded_wait_check(uint32_t *status, cudaStream_t s);
 // EP <-> TP expert-weight reshard permute (reshard.cu); a null source skips
@@ -318,6 +355,36 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity) 
     if ((it & 63u) == 63u && globaltimer_ns() - t0 > kWaitLimitNs / 10) return false;
   }
   return false;
+}
+
+// Acquire load of a flag another CTA releases (gpu scope).
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Orders this thread's generic-proxy global accesses with its async-proxy
+// (TMA) accesses: written by a generic store, read by a tensor copy.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Bulk copy of `bytes` (a multiple of 16) from global to shared memory, both
+// addresses 16-byte aligned; completion on an mbarrier.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
+                                          uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Orders this thread's generic-proxy shared-memory accesses with later
+// async-proxy (bulk / tensor copy) accesses of the same memory.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // --- TMA (tensor tiles, global -> shared, completion on an mbarrier) ---

@@ -12,6 +12,7 @@
 //    finish gates every token.
 #include <float.h>
 
+#include "gating.cuh"
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -24,98 +25,6 @@ namespace {
 #define MOE_TOPK_BATCH 8
 #endif
 constexpr int kTopkSplitBatch = MOE_TOPK_BATCH;
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-__device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + expf(-z)); }
-
-// Selection and gate weights of token t from its fp32 logits s (lane holds
-// experts lane, lane+32, ...).  The whole warp calls it.
-template <int NV>
-__device__ __forceinline__ void select_and_gate(const float (&s)[NV], int lane, int t, int E, int k,
-                                                int gating, const float *__restrict__ sel_bias,
-                                                int32_t *__restrict__ ids, float *__restrict__ wout,
-                                                float *__restrict__ gap) {
-  float key[NV];
-#pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int e = lane + 32 * i;
-    key[i] = -FLT_MAX;
-    if (e < E)
-      key[i] = (gating == MOE_GATE_SIGMOID_BIAS_RENORM) ? sigmoidf_(s[i]) + sel_bias[e] : s[i];
-  }
-
-  uint32_t taken = 0;
-  int my_id = 0;
-  float my_s = 0.f, kth_key = 0.f, next_key = 0.f;
-  const int rounds = (k < E) ? k + 1 : k;
-  for (int j = 0; j < rounds; ++j) {
-    float bk = -FLT_MAX;
-    int bi = 0x7fffffff;
-    float bs = 0.f;
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u)) {
-        if (key[i] > bk || (key[i] == bk && e < bi)) {
-          bk = key[i];
-          bi = e;
-          bs = s[i];
-        }
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      const float os = __shfl_xor_sync(0xffffffffu, bs, o);
-      if (ok > bk || (ok == bk && oi < bi)) {
-        bk = ok;
-        bi = oi;
-        bs = os;
-      }
-    }
-    if (j < k) {
-      if (lane == j) {
-        my_id = bi;
-        my_s = bs;
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      kth_key = bk;
-    } else {
-      next_key = bk;
-    }
-  }
-
-  float wv = 0.f;
-  const bool mine = lane < k;
-  if (gating == MOE_GATE_TOPK_SOFTMAX) {
-    const float m = __shfl_sync(0xffffffffu, my_s, 0);  // slot 0 holds the largest kept logit
-    const float ev = mine ? expf(my_s - m) : 0.f;
-    wv = ev / warp_sum(ev);
-  } else if (gating == MOE_GATE_SOFTMAX_TOPK || gating == MOE_GATE_SOFTMAX_TOPK_RENORM) {
-    const float m = __shfl_sync(0xffffffffu, my_s, 0);  // largest logit of all E
-    float part = 0.f;
-#pragma unroll
-    for (int i = 0; i < NV; ++i)
-      if (lane + 32 * i < E) part += expf(s[i] - m);
-    const float zsum = warp_sum(part);
-    const float p = mine ? expf(my_s - m) / zsum : 0.f;
-    wv = (gating == MOE_GATE_SOFTMAX_TOPK) ? p : p / warp_sum(p);
-  } else {
-    const float a = mine ? sigmoidf_(my_s) : 0.f;
-    wv = a / warp_sum(a);
-  }
-  if (mine) {
-    ids[(size_t)t * k + lane] = my_id;
-    wout[(size_t)t * k + lane] = wv;
-  }
-  if (gap != nullptr && lane == 0) gap[t] = (k < E) ? kth_key - next_key : 0.f;
-}
 
 // NV = logits per lane (E <= 32 * NV).
 template <int NV>

@@ -118,9 +118,10 @@ def check_routing(gpu_ids: np.ndarray, gpu_w: np.ndarray, ref: Dict[str, np.ndar
 class LayerRun:
     """One moe_layer_forward of a seeded workload on cuda:0."""
 
-    def __init__(self, inputs: synth.LayerInputs):
+    def __init__(self, inputs: synth.LayerInputs, path: Optional[int] = None):
         cfg, T = inputs.cfg, inputs.T
         self.inputs = inputs
+        self.path = path     # None: moe_layer_forward's own choice; else MOE_PATH_*
         self.d = moe.desc(T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.gating, cfg.shared)
         self.ws = moe.alloc_workspace(self.d)
         self.layout = moe.moe_workspace_layout(self.d)
@@ -129,7 +130,7 @@ class LayerRun:
         self.y = torch.empty((T, cfg.H), dtype=torch.bfloat16, device="cuda")
 
     def forward(self):
-        moe.moe_layer_forward(self.d, self.w, self.inputs.x, self.y, self.ws)
+        moe.moe_layer_forward(self.d, self.w, self.inputs.x, self.y, self.ws, path=self.path)
         torch.cuda.synchronize()
         st, raw = moe.moe_get_device_status(self.ws)
         assert st == moe.MOE_OK, (st, raw)

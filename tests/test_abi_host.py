@@ -157,3 +157,21 @@ def test_bounded_wait_check_validates_before_launch(lib):
     assert lib.moe_check_bounded_wait(0x10010, 1 << 20, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_check_bounded_wait(0x10000, 16, None) == moe.MOE_ERR_INVALID_ARG
 
+
+
+def test_forward_path_validation_before_launch(lib):
+    w = moe.LayerWeights(FAKE, None, FAKE, FAKE, None, None)
+    fwd = lambda d, path: lib.moe_layer_forward_ex(ctypes.byref(d), ctypes.byref(w), FAKE, FAKE,
+                                                   FAKE, moe.moe_workspace_size(d), None, None,
+                                                   path)
+    # an unknown path
+    assert fwd(qwen3(T=4), 3) == moe.MOE_ERR_INVALID_ARG
+    assert fwd(qwen3(T=4), -1) == moe.MOE_ERR_INVALID_ARG
+    # the persistent layer takes at most 16 tokens and H >= 256
+    assert fwd(qwen3(T=17), moe.MOE_PATH_PERSISTENT) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    assert fwd(qwen3(T=4, H=128), moe.MOE_PATH_PERSISTENT) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    # valid otherwise: the device check, which fails without a GPU
+    for path in (moe.MOE_PATH_AUTO, moe.MOE_PATH_KERNEL_CHAIN, moe.MOE_PATH_PERSISTENT):
+        assert fwd(qwen3(T=4), path) in (moe.MOE_ERR_CUDA, moe.MOE_ERR_UNSUPPORTED_DEVICE)
+    assert lib.moe_check_bounded_grid_wait(None, 1 << 20, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_check_bounded_grid_wait(0x10000, 16, None) == moe.MOE_ERR_INVALID_ARG

@@ -15,6 +15,7 @@ import pytest
 import torch
 
 import oracle
+import routed_expert_ffn_gb300 as moe
 import synth
 from gpu_check import LayerRun, assert_output_close, bf16_np, check_routing, host_copy, sample_tokens
 
@@ -52,9 +53,9 @@ def layer_inputs(name, T, seed=0, uniform=False):
                              full.w2_shared)
 
 
-def check_layer(inputs, n_sample=256):
+def check_layer(inputs, n_sample=256, path=None):
     cfg, T = inputs.cfg, inputs.T
-    run = LayerRun(inputs)
+    run = LayerRun(inputs, path)
     y = run.forward()
     meta = run.metadata()
     host = host_copy(inputs, experts=[])
@@ -63,7 +64,7 @@ def check_layer(inputs, n_sample=256):
     ref = {"logits": s, "ids": ids, "w": w, "gap": gap}
     bias = None if host["sel_bias"] is None else host["sel_bias"].numpy()
     info = check_routing(meta["ids"], meta["w"], ref, cfg.gating, bias,
-                         label=f"{cfg.name} T={T}")
+                         label=f"{cfg.name} T={T}" + ("" if path is None else f" path={path}"))
     # dispatch of the ids the GPU routed (a pure integer function of them)
     rc, ro, rp, ri = oracle.dispatch(meta["ids"], cfg.E)
     assert np.array_equal(meta["counts"], rc)
@@ -160,7 +161,7 @@ def test_tile_plan(name, T):
     and compared exactly."""
     inputs = layer_inputs(name, T)
     cfg = inputs.cfg
-    run = LayerRun(inputs)
+    run = LayerRun(inputs, moe.MOE_PATH_KERNEL_CHAIN)   # the plan drives the chain's GEMMs
     run.forward()
     counts = run.metadata()["counts"].tolist()
     ms = counts + ([T] if cfg.shared else [])

@@ -63,7 +63,8 @@ def test_stage_calls_match_layer_forward(T):
     inp = inputs("chain", T, 512, 16, 4, 256, synth.GATE_SOFTMAX_TOPK_RENORM,
                  skew=("zipf", 1.1, 0.3))
     cfg = inp.cfg
-    run = LayerRun(inp)
+    # the kernel chain: the stage calls below are its stages
+    run = LayerRun(inp, moe.MOE_PATH_KERNEL_CHAIN)
     y_fused = run.forward().clone()
     meta = run.metadata()
 
@@ -94,25 +95,28 @@ def test_stage_calls_match_layer_forward(T):
     assert torch.equal(y, y_fused)
 
 
-@pytest.mark.parametrize("name,T", [("qwen3", 1), ("qwen3", 300)])
-def test_layer_forward_replays_from_a_cuda_graph(name, T):
+@pytest.mark.parametrize("name,T,path", [("qwen3", 1, None), ("qwen3", 1, 1), ("qwen3", 300, None),
+                                         ("qwen3_tp8", 8, 2)])
+def test_layer_forward_replays_from_a_cuda_graph(name, T, path):
     """The forward makes no host synchronisation or host-side decision on
-    device data, so it can be captured in a CUDA graph; replays give exactly
-    the eager result (and leave the split-K and router counters at zero)."""
+    device data, so it can be captured in a CUDA graph (the persistent decode
+    layer's cooperative launch included); replays give exactly the eager
+    result (and leave the split-K, router, barrier and readiness counters at
+    zero)."""
     cfg = synth.CONFIGS[name]
     inp = synth.make_layer(cfg, T, 0, device="cuda")
-    run = LayerRun(inp)
+    run = LayerRun(inp, path)
     y_eager = run.forward().clone()
     y = torch.empty_like(y_eager)
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
-        moe.moe_layer_forward(run.d, run.w, inp.x, y, run.ws, stream=s)   # warm-up on s
+        moe.moe_layer_forward(run.d, run.w, inp.x, y, run.ws, stream=s, path=path)  # warm-up on s
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
-        moe.moe_layer_forward(run.d, run.w, inp.x, y, run.ws, stream=s)
+        moe.moe_layer_forward(run.d, run.w, inp.x, y, run.ws, stream=s, path=path)
     for _ in range(3):
         y.zero_()
         g.replay()
