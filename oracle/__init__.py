@@ -131,6 +131,55 @@ def dispatch(ids, E: int):
     return counts, offsets, perm_src, inv_pos
 
 
+# ---------------------------------------------- capacity and token dropping --
+# "MoE推理优化全景指南", section "Capacity、padding 与 token dropping": an expert's
+# capacity is C = ceil(capacity_factor * N_a / E); assignments beyond C are
+# dropped.  CS349D lecture 8 notes, section 1.4 ("容量因子与丢 token"): a dropped
+# (token, expert) pair contributes 0, nothing else changes.  Reading: the
+# first C assignments of each expert in token order are kept (the dispatch
+# layout's order inside a segment); the kept gate weights are not
+# renormalised.
+
+def expert_capacity(cf_num: int, cf_den: int, n_assign: int, E: int) -> int:
+    """C = ceil(cf * N_a / E) for a capacity factor cf = cf_num / cf_den, in
+    exact integer arithmetic."""
+    if cf_num <= 0 or cf_den <= 0 or E <= 0 or n_assign <= 0:
+        raise ValueError("capacity factor, assignments and experts must be positive")
+    num, den = cf_num * n_assign, cf_den * E
+    return -(-num // den)
+
+
+def capacity_dispatch(ids, E: int, C: int):
+    """The dispatch of the kept assignments: (counts[E] kept per expert,
+    offsets[E+1], perm_src[n_kept] position -> assignment, inv_pos[T*k]
+    assignment -> position or -1 when dropped).  Kept: the first C
+    assignments of each expert in token order."""
+    counts, offsets, perm, _ = dispatch(ids, E)
+    n = perm.shape[0]
+    kept = np.minimum(counts, C).astype(np.int32)
+    offs = np.zeros(E + 1, dtype=np.int32)
+    perm_c = []
+    inv_c = np.full(n, -1, dtype=np.int32)
+    for e in range(E):
+        offs[e] = len(perm_c)
+        for r in range(int(kept[e])):
+            a = int(perm[offsets[e] + r])
+            inv_c[a] = len(perm_c)
+            perm_c.append(a)
+    offs[E] = len(perm_c)
+    return kept, offs, np.asarray(perm_c, dtype=np.int32), inv_c
+
+
+def kept_weights(ids, w, E: int, C: int) -> np.ndarray:
+    """Gate weights with every dropped assignment's weight set to 0 (its
+    contribution to the layer output); the kept weights unchanged."""
+    ia = _np(ids, np.int32)
+    _, _, _, inv_c = capacity_dispatch(ia, E, C)
+    wk = np.array(_np(w, np.float64), copy=True).reshape(-1)
+    wk[inv_c < 0] = 0.0
+    return wk.reshape(ia.shape)
+
+
 def imbalance(counts, n_assign: int) -> Tuple[int, int]:
     """Imbalance ratio max_e n_e / (N_a/E) as an exact fraction (num, den)."""
     c = _np(counts, np.int32)
