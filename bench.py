@@ -56,6 +56,9 @@ def parse():
                    help="--sweep: comma-separated layer names to keep (default: all)")
     p.add_argument("--sweep-max-T", type=int, default=0,
                    help="--sweep: keep batch sizes up to this many tokens (default: all)")
+    p.add_argument("--capacity-factor", type=float, default=0.0,
+                   help="time moe_layer_forward_capacity with C = ceil(cf * T * k / E) "
+                        "(0: the dropless layer)")
     p.add_argument("--path", default="auto", choices=["auto", "chain", "persistent"],
                    help="execution path of the layer forward: automatic choice (default), "
                         "the kernel chain, or the persistent single-kernel layer (T <= 16)")
@@ -351,12 +354,32 @@ def uses_persistent(cfg, T, path):
 
 
 def time_layer(moe, d, wts, x, y, ws, lay, cfg, T, steps, warmup, pg, stream, l2_flush=False,
-               path=None):
+               path=None, capacity=0):
     """Warm-up, then the timed region (K forwards between two events, barrier +
     synchronize on both sides), then the same K forwards with stage events and
     with per-step events.  Returns the timings, the host time per call and the
-    routing counts the workspace holds afterwards."""
+    routing counts the workspace holds afterwards.  capacity > 0: the
+    capacity-limited forward (its stage events all fall around the call)."""
     import torch
+    if capacity > 0:
+        real = moe
+
+        class _Moe:
+            MOE_OK = real.MOE_OK
+            MOE_STAGE_EVENTS = real.MOE_STAGE_EVENTS
+            STAGE_NAMES = real.STAGE_NAMES
+            moe_get_device_status = staticmethod(real.moe_get_device_status)
+            workspace_view = staticmethod(real.workspace_view)
+
+            @staticmethod
+            def moe_layer_forward(d_, w_, x_, y_, ws_, stream=None, stage_events=None, path=None):
+                if stage_events is not None:
+                    stage_events[0].record(torch.cuda.current_stream())
+                real.moe_layer_forward_capacity(d_, w_, x_, y_, capacity, ws_, stream=stream)
+                if stage_events is not None:
+                    for e in stage_events[1:]:
+                        e.record(torch.cuda.current_stream())
+        moe = _Moe
     for _ in range(warmup):
         moe.moe_layer_forward(d, wts, x, y, ws, path=path)
     torch.cuda.synchronize()
@@ -433,10 +456,14 @@ def time_layer(moe, d, wts, x, y, ws, lay, cfg, T, steps, warmup, pg, stream, l2
     stage_us = {n: 1e3 * v / steps for n, v in stage_ms.items()}
     counts = moe.workspace_view(ws, lay, "counts", torch.int32, (cfg.E,)).cpu().tolist()
     gap = moe.workspace_view(ws, lay, "gap", torch.float32, (T,)).cpu()
+    dropped = 0
+    if capacity > 0:
+        inv = moe.workspace_view(ws, lay, "inv_pos", torch.int32, (T * cfg.k,)).cpu()
+        dropped = int((inv < 0).sum().item())
     near_ties = int((gap < NEAR_TIE).sum().item()) if cfg.k < cfg.E else 0
     return {"ms_max": ms_max, "stage_us": stage_us, "step_spread": step_spread,
             "host_us": host_us, "counts": counts, "near_ties": near_ties,
-            "t_wall": (t_wall0, t_wall1)}
+            "capacity": capacity, "dropped": dropped, "t_wall": (t_wall0, t_wall1)}
 
 
 # top-k boundary gaps below this are near-ties (the configuration statement)
@@ -452,9 +479,11 @@ def layer_line(cfg, T, args, world, tm, pk, sampler):
     stage_us = tm["stage_us"]
     # the persistent decode layer is one kernel (its stage events all fall at
     # its end): its roofline is the whole layer's
-    persistent = uses_persistent(cfg, T, args.path)
-    if persistent:
-        kern = "persistent decode layer (router, dispatch, tcgen05 GEMMs, combine)"
+    persistent = uses_persistent(cfg, T, args.path) and not tm["capacity"]
+    whole = persistent or tm["capacity"] > 0
+    if whole:
+        kern = ("persistent decode layer (router, dispatch, tcgen05 GEMMs, combine)"
+                if persistent else "capacity-limited layer forward (kernel chain)")
         kern_bytes, kern_us = alg["layer_bytes"], stage_us["route"]
     else:
         kern = "expert gate/up GEMM + SwiGLU (tcgen05)"
@@ -481,7 +510,7 @@ def layer_line(cfg, T, args, world, tm, pk, sampler):
         "config": workload_config(cfg, T, args.l2_flush),
         "roofline": {"bound": "hbm", "kernel": kern,
                      "achieved": gu_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": gu_gbs / pk["hbm_gbs"], "traffic": None if persistent else traffic,
+                     "frac": gu_gbs / pk["hbm_gbs"], "traffic": None if whole else traffic,
                      "algorithmic_bytes": kern_bytes, "launch_us": kern_us,
                      "peak_source": pk["source"]},
         "path": "persistent" if persistent else "chain",
@@ -497,8 +526,11 @@ def layer_line(cfg, T, args, world, tm, pk, sampler):
         "step_us_spread": tm["step_spread"],
         "host_us_per_call": tm["host_us"],
         "routing": {"imbalance_ratio": num / den, "touched_experts": alg["touched"],
-                    "near_ties": tm["near_ties"], "near_tie_gap": NEAR_TIE},
-        "gpu_launches": (1 if persistent else launches_per_step(cfg, T)) * args.steps,
+                    "near_ties": tm["near_ties"], "near_tie_gap": NEAR_TIE,
+                    **({"capacity": tm["capacity"], "dropped_assignments": tm["dropped"]}
+                       if tm["capacity"] else {})},
+        "gpu_launches": (1 if persistent else launches_per_step(cfg, T, tm["capacity"] > 0))
+                        * args.steps,
         "clocks": sampler.summary(*tm["t_wall"]) if sampler else None,
     }
 
@@ -530,8 +562,10 @@ def run_gpu(args):
     uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
     sampler = ClockSampler(uuid) if rank == 0 else None
     time.sleep(0.5 if sampler else 0)
+    cap = (moe.moe_expert_capacity(args.capacity_factor, T, cfg.k, cfg.E)
+           if args.capacity_factor > 0 else 0)
     tm = time_layer(moe, d, wts, inp.x, y, ws, lay, cfg, T, args.steps, args.warmup, pg, stream,
-                    args.l2_flush, PATHS[args.path])
+                    args.l2_flush, PATHS[args.path], cap)
 
     # ---- end to end: pinned host x in, host y out, through the same call ----
     # Every step copies its x from pinned host memory, runs moe_layer_forward
@@ -561,8 +595,11 @@ def run_gpu(args):
             stream.wait_event(h2d_done[b])
             if i >= 2:
                 stream.wait_event(d2h_done[b])    # y_dev[b] of step i-2 is on the host
-            moe.moe_layer_forward(d, wts, x_dev[b], y_dev[b], ws, stream=stream,
-                                  path=PATHS[args.path])
+            if cap:
+                moe.moe_layer_forward_capacity(d, wts, x_dev[b], y_dev[b], cap, ws, stream=stream)
+            else:
+                moe.moe_layer_forward(d, wts, x_dev[b], y_dev[b], ws, stream=stream,
+                                      path=PATHS[args.path])
             fwd_done[b].record(stream)
             s_out.wait_event(fwd_done[b])
             with torch.cuda.stream(s_out):
@@ -689,8 +726,10 @@ def run_sweep(args):
         a.l2_flush = name == "tiny"
         sampler = ClockSampler(uuid)
         time.sleep(0.3)
+        cap = (moe.moe_expert_capacity(args.capacity_factor, T, cfg.k, cfg.E)
+               if args.capacity_factor > 0 else 0)
         tm = time_layer(moe, d, wts, x, y, ws, lay, cfg, T, steps, args.warmup, None, stream,
-                        a.l2_flush, PATHS[args.path])
+                        a.l2_flush, PATHS[args.path], cap)
         sampler.stop()
         line = layer_line(cfg, T, a, 1, tm, pk, sampler)
         line["sweep"] = True
@@ -701,12 +740,12 @@ def run_sweep(args):
         del ws, y, x
 
 
-def launches_per_step(cfg, T):
-    """Kernels one moe_layer_forward launches: router (one fused kernel up to 32
-    tokens, else W_r split + tensor-core router + gating),
-    dispatch (one kernel up to 2048 assignments, else three), gather + plan,
-    gate/up GEMM, down GEMM, combine."""
-    return (1 if T <= 32 else 3) + (1 if T * cfg.k <= 2048 else 3) + 4
+def launches_per_step(cfg, T, capacity=False):
+    """Kernels one kernel-chain forward launches: router (one fused kernel up to
+    32 tokens, else W_r split + tensor-core router + gating), dispatch (one
+    kernel up to 2048 assignments, else three), [the capacity compaction],
+    gather + plan, gate/up GEMM, down GEMM, combine."""
+    return (1 if T <= 32 else 3) + (1 if T * cfg.k <= 2048 else 3) + 4 + (1 if capacity else 0)
 
 
 def kernel_sources_sha():

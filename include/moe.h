@@ -326,6 +326,37 @@ moe_status_t moe_layer_forward_ex(const moe_layer_desc_t *d, const moe_layer_wei
                                   moe_stream_t stream, moe_event_t const *stage_events,
                                   int32_t path);
 
+/*
+ * Capacity limit ("MoE推理优化全景指南", section "Capacity、padding 与 token
+ * dropping": C = ceil(capacity factor x N_a / E); an expert takes at most C
+ * assignments and the rest are dropped; CS349D lecture 8 notes, section 1.4:
+ * a dropped (token, expert) pair contributes 0 to the token's output).
+ * Inference engines are dropless (moe_layer_forward); these calls reproduce
+ * the capacity-limited layer of training systems, with a bounded number of
+ * rows per expert.
+ *
+ * moe_expert_capacity -- C = ceil(cf * T * k / E) for cf = cf_num / cf_den,
+ * in exact integer arithmetic (host only; 0 for a non-positive argument or
+ * cf_num, cf_den above 2^30).
+ */
+int32_t moe_expert_capacity(int64_t cf_num, int64_t cf_den, int32_t T, int32_t k, int32_t E);
+
+/*
+ * moe_layer_forward_capacity -- the layer with at most `capacity` assignments
+ * per routed expert: of each expert's assignments the first `capacity` in
+ * token order are kept, the rest dropped (weight 0; the kept gate weights are
+ * not renormalised).  The shared expert is never limited.  Kernel chain path;
+ * the workspace then holds the kept layout: counts = kept rows per expert,
+ * offsets over the kept rows (offsets[E] = kept assignments), perm_src over
+ * them (-1 past offsets[E]), inv_pos = -1 for a dropped assignment, and the
+ * shared expert's rows at [offsets[E], offsets[E] + T) of x_perm, h and
+ * out_perm.  capacity >= 1 (MOE_ERR_INVALID_ARG otherwise); other arguments as
+ * moe_layer_forward.
+ */
+moe_status_t moe_layer_forward_capacity(const moe_layer_desc_t *d, const moe_layer_weights_t *w,
+                                        const void *x, void *y, int32_t capacity,
+                                        void *workspace, size_t ws_bytes, moe_stream_t stream);
+
 /* Check of the persistent layer's grid barrier: a two-CTA cooperative launch
  * waits at that barrier sized for three CTAs.  Both waits give up after about
  * one second and latch MOE_ERR_TIMEOUT's bit 7 in the status word; the kernel

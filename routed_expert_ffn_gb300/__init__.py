@@ -95,6 +95,8 @@ def library() -> ctypes.CDLL:
         "moe_layer_forward": ([D, ctypes.POINTER(LayerWeights), P, P, P, S, P, P], I32),
         "moe_check_bounded_wait": ([P, S, P], I32),
         "moe_check_bounded_grid_wait": ([P, S, P], I32),
+        "moe_expert_capacity": ([ctypes.c_int64, ctypes.c_int64, I32, I32, I32], I32),
+        "moe_layer_forward_capacity": ([D, ctypes.POINTER(LayerWeights), P, P, I32, P, S, P], I32),
         "moe_layer_forward_ex": ([D, ctypes.POINTER(LayerWeights), P, P, P, S, P, P, I32], I32),
         "moe_reshard_ep_to_tp_pack": ([I32, I32, I32, I32, P, P, P, P, P], I32),
         "moe_reshard_tp_to_ep_unpack": ([I32, I32, I32, I32, P, P, P, P, P], I32),
@@ -267,6 +269,26 @@ def moe_layer_forward(d: LayerDesc, w: LayerWeights, x, y, ws, stream=None,
         _check("moe_layer_forward_ex", library().moe_layer_forward_ex(
             ctypes.byref(d), ctypes.byref(w), _ptr(x), _ptr(y), _ptr(ws), _nbytes(ws),
             _stream(stream), ev, int(path)))
+
+
+def moe_expert_capacity(cf, T: int, k: int, E: int) -> int:
+    """C = ceil(cf * T * k / E); cf a Fraction, an int, or a float (taken as the
+    nearest fraction with a denominator up to 10^6)."""
+    from fractions import Fraction
+    f = Fraction(cf).limit_denominator(10 ** 6)
+    c = library().moe_expert_capacity(f.numerator, f.denominator, T, k, E)
+    if c <= 0:
+        raise ValueError("invalid capacity factor or shape")
+    return int(c)
+
+
+def moe_layer_forward_capacity(d: LayerDesc, w: LayerWeights, x, y, capacity: int, ws,
+                               stream=None):
+    """Layer forward with at most ``capacity`` assignments per routed expert
+    (the first ones in token order; the rest dropped)."""
+    _check("moe_layer_forward_capacity", library().moe_layer_forward_capacity(
+        ctypes.byref(d), ctypes.byref(w), _ptr(x), _ptr(y), int(capacity), _ptr(ws), _nbytes(ws),
+        _stream(stream)))
 
 
 def workspace_view(ws, layout: Dict[str, int], name: str, dtype, shape):

@@ -56,6 +56,11 @@ Layout make_layout(const moe_layer_desc_t &d) {
   L.perm_src = take((size_t)Na * 4);
   L.inv_pos = take((size_t)Na * 4);
   L.w_perm = take((size_t)Na * 4);
+  L.cap_counts = take((size_t)d.E * 4);
+  L.cap_offsets = take((size_t)(d.E + 1) * 4);
+  L.cap_perm = take((size_t)Na * 4);
+  L.cap_inv = take((size_t)Na * 4);
+  L.cap_wperm = take((size_t)Na * 4);
   L.x_perm = take((size_t)L.rows * d.H * 2);
   L.h = take((size_t)L.rows * d.I * 2);
   L.out_perm = take((size_t)L.rows * d.H * 2);
@@ -390,6 +395,75 @@ moe_status_t moe_layer_forward(const moe_layer_desc_t *d, const moe_layer_weight
                                moe_stream_t stream, moe_event_t const *stage_events) {
   return moe_layer_forward_ex(d, w, x, y, workspace, ws_bytes, stream, stage_events,
                               MOE_PATH_AUTO);
+}
+
+int32_t moe_expert_capacity(int64_t cf_num, int64_t cf_den, int32_t T, int32_t k, int32_t E) {
+  if (cf_num <= 0 || cf_den <= 0 || T < 1 || k < 1 || E < 1) return 0;
+  if (cf_num > ((int64_t)1 << 30) || cf_den > ((int64_t)1 << 30)) return 0;
+  const int64_t num = cf_num * ((int64_t)T * k), den = cf_den * E;  // < 2^55, < 2^40
+  const int64_t c = (num + den - 1) / den;
+  return c > ((int64_t)1 << 30) ? ((int32_t)1 << 30) : (int32_t)c;
+}
+
+moe_status_t moe_layer_forward_capacity(const moe_layer_desc_t *d, const moe_layer_weights_t *w,
+                                        const void *x, void *y, int32_t capacity,
+                                        void *workspace, size_t ws_bytes, moe_stream_t stream) {
+  if (workspace == nullptr || w == nullptr) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  moe_status_t st = prologue(d, workspace, ws_bytes, &L);
+  if (st != MOE_OK) return st;
+  if (!ok_ptr(x) || !ok_ptr(y) || !ok_ptr(w->w_router) || !ok_ptr(w->w13) || !ok_ptr(w->w2))
+    return MOE_ERR_INVALID_ARG;
+  if (d->gating == MOE_GATE_SIGMOID_BIAS_RENORM && !ok_ptr(w->sel_bias)) return MOE_ERR_INVALID_ARG;
+  if (d->has_shared_expert && (!ok_ptr(w->w13_shared) || !ok_ptr(w->w2_shared)))
+    return MOE_ERR_INVALID_ARG;
+  if (capacity < 1) return MOE_ERR_INVALID_ARG;
+  if ((st = check_device()) != MOE_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t *status = at<uint32_t>(workspace, L.status);
+  float *tw = at<float>(workspace, L.topk_w);
+  int32_t *ids = at<int32_t>(workspace, L.topk_ids);
+  int32_t *offsets = at<int32_t>(workspace, L.offsets);
+  int32_t *perm_src = at<int32_t>(workspace, L.perm_src);
+  int32_t *inv_pos = at<int32_t>(workspace, L.inv_pos);
+  float *w_perm = at<float>(workspace, L.w_perm);
+  int32_t *plan = at<int32_t>(workspace, L.plan);
+  __nv_bfloat16 *x_perm = at<__nv_bfloat16>(workspace, L.x_perm);
+  __nv_bfloat16 *h = at<__nv_bfloat16>(workspace, L.h);
+  __half *out_perm = at<__half>(workspace, L.out_perm);
+  float *split_part = at<float>(workspace, L.split_part);
+  uint32_t *split_cnt = at<uint32_t>(workspace, L.status) + kSplitCounterWord;
+  // route; the dropless dispatch into scratch; the kept assignments' layout
+  // into the workspace's routing buffers; then the chain as without a limit,
+  // the tile plan written by the gather from the kept layout
+  cudaError_t e = route(*d, L, bf(x), w->w_router, w->sel_bias, at<float>(workspace, L.logits),
+                        ids, tw, at<float>(workspace, L.gap), workspace, s);
+  if (e == cudaSuccess)
+    e = launch_dispatch(ids, tw, d->T, d->k, d->E, at<int32_t>(workspace, L.blk_counts),
+                        at<int32_t>(workspace, L.blk_base), at<int32_t>(workspace, L.cap_counts),
+                        at<int32_t>(workspace, L.cap_offsets), at<int32_t>(workspace, L.cap_perm),
+                        at<int32_t>(workspace, L.cap_inv), at<float>(workspace, L.cap_wperm),
+                        status, nullptr, d->H, d->I, d->has_shared_expert, s);
+  if (e == cudaSuccess)
+    e = launch_capacity(at<int32_t>(workspace, L.cap_counts), at<int32_t>(workspace, L.cap_offsets),
+                        at<int32_t>(workspace, L.cap_perm), at<float>(workspace, L.cap_wperm),
+                        d->T, d->k, d->E, capacity, at<int32_t>(workspace, L.counts), offsets,
+                        perm_src, inv_pos, w_perm, s);
+  if (e == cudaSuccess)
+    e = launch_gather_plan(bf(x), perm_src,
+                           (int64_t)d->T * d->H * 2 > kGatherByTokenBytes ? inv_pos : nullptr,
+                           offsets, d->T, d->k, d->E, d->H, d->I, d->has_shared_expert, x_perm,
+                           plan, status, s);
+  if (e == cudaSuccess)
+    e = launch_expert_gateup(*d, w->w13, w->w13_shared, x_perm, plan, 0, split_part, split_cnt, h,
+                             status, s);
+  if (e == cudaSuccess)
+    e = launch_expert_down(*d, w->w2, w->w2_shared, h, plan, w_perm, split_part,
+                           split_cnt + kMaxSplitTiles, out_perm, status, s);
+  if (e == cudaSuccess)
+    e = launch_combine(out_perm, inv_pos, nullptr, d->T, d->k, d->H, d->has_shared_expert, bfw(y),
+                       s, offsets + d->E);
+  return cuda_status(e);
 }
 
 moe_status_t moe_check_bounded_grid_wait(void *workspace, size_t ws_bytes, moe_stream_t stream) {

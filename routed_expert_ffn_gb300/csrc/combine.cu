@@ -16,8 +16,8 @@ namespace {
 
 __global__ void __launch_bounds__(256)
     combine_kernel(const __half *__restrict__ out_perm, const int32_t *__restrict__ inv_pos,
-                   const float *__restrict__ topk_w, int T, int k, int H, int shared,
-                   __nv_bfloat16 *__restrict__ y) {
+                   const float *__restrict__ topk_w, const int32_t *__restrict__ shared_base,
+                   int T, int k, int H, int shared, __nv_bfloat16 *__restrict__ y) {
   pdl_wait();
   pdl_launch_dependents();
   const int t = blockIdx.x;
@@ -61,7 +61,12 @@ __global__ void __launch_bounds__(256)
       if (j0 + i < k) add(raw[i], wt[i]);
     }
   }
-  if (shared) add(reinterpret_cast<const uint4 *>(out_perm + (Na + t) * H)[v], 1.0f);
+  // the shared expert's row: after the routed rows (at *shared_base when
+  // given: the kept rows under a capacity limit end there)
+  if (shared) {
+    const int64_t sb = shared_base != nullptr ? (int64_t)*shared_base : Na;
+    add(reinterpret_cast<const uint4 *>(out_perm + (sb + t) * H)[v], 1.0f);
+  }
   uint4 o;
   __nv_bfloat162 *q = reinterpret_cast<__nv_bfloat162 *>(&o);
 #pragma unroll
@@ -73,11 +78,11 @@ __global__ void __launch_bounds__(256)
 
 cudaError_t launch_combine(const __half *out_perm, const int32_t *inv_pos,
                            const float *topk_w, int T, int k, int H, int shared, __nv_bfloat16 *y,
-                           cudaStream_t s) {
+                           cudaStream_t s, const int32_t *shared_base) {
   const int nv = H / 8;
   dim3 grid(T, (nv + 255) / 256);
-  return launch_pdl(combine_kernel, grid, dim3(256), 0, s, out_perm, inv_pos, topk_w, T, k, H,
-                    shared, y);
+  return launch_pdl(combine_kernel, grid, dim3(256), 0, s, out_perm, inv_pos, topk_w, shared_base,
+                    T, k, H, shared, y);
 }
 
 }  // namespace moe

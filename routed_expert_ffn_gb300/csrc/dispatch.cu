@@ -136,6 +136,9 @@ __global__ void __launch_bounds__(256)
     return;
   }
   // ---- gather ----
+  // the shared expert's rows start at offsets[E] (= Na without a capacity
+  // limit, else the number of kept assignments)
+  const int64_t sb = offsets[E];
   const int lane = threadIdx.x & 31;
   constexpr int kBatch = 8;  // 16-byte loads in flight per lane before their stores
   const int nv = H / 8;
@@ -164,7 +167,7 @@ __global__ void __launch_bounds__(256)
           row = p;
         } else {
           if (!shared) break;
-          row = Na + t;
+          row = sb + t;
         }
         uint4 *dst = reinterpret_cast<uint4 *>(x_perm + row * H);
 #pragma unroll
@@ -177,11 +180,11 @@ __global__ void __launch_bounds__(256)
   const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (row >= R) return;
   int64_t src = -1;
-  if (row < Na) {
+  if (row < sb) {
     const int32_t a = perm_src[row];
     if (a >= 0 && a < Na) src = a / k;
-  } else {
-    src = row - Na;
+  } else if (shared && row < sb + T) {
+    src = row - sb;
   }
   uint4 *dst = reinterpret_cast<uint4 *>(x_perm + row * H);
   if (src < 0) {
@@ -219,7 +222,90 @@ __global__ void __launch_bounds__(kSmallThreads)
                                           pa.num_sms, pa.status);
 }
 
+// Capacity limit ("MoE推理优化全景指南", "Capacity、padding 与 token
+// dropping": an expert takes at most C assignments, the rest are dropped).
+// From the dropless layout, keep the first C positions of every expert's
+// segment (its first C tokens in token order) in a compact layout: every
+// block computes the kept counts' prefix sum over E (E <= 512), then moves its
+// positions.  A dropped assignment gets inv_pos -1 (the combine skips it);
+// positions past the kept rows get perm_src -1 (the gather zeroes them).
+constexpr int kCapThreads = 256;
+
+__global__ void __launch_bounds__(kCapThreads)
+    capacity_kernel(const int32_t *__restrict__ counts, const int32_t *__restrict__ offsets,
+                    const int32_t *__restrict__ perm_src, const float *__restrict__ w_perm,
+                    int64_t Na, int E, int C, int32_t *__restrict__ counts_c,
+                    int32_t *__restrict__ offsets_c, int32_t *__restrict__ perm_c,
+                    int32_t *__restrict__ inv_c, float *__restrict__ w_perm_c) {
+  pdl_wait();
+  pdl_launch_dependents();
+  __shared__ int s_off[kMaxE + 1], s_offc[kMaxE + 1];
+  __shared__ int warp_tot[32];
+  __shared__ int total;
+  constexpr int kPer = (kMaxE + kCapThreads - 1) / kCapThreads;  // experts per thread
+  int kept[kPer], sum = 0;
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const int e = threadIdx.x * kPer + q;
+    kept[q] = (e < E) ? min(counts[e], C) : 0;
+    sum += kept[q];
+  }
+  int run = block_exclusive_scan(sum, warp_tot, &total);
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const int e = threadIdx.x * kPer + q;
+    if (e < E) {
+      s_offc[e] = run;
+      s_off[e] = offsets[e];
+      if (blockIdx.x == 0) {
+        counts_c[e] = kept[q];
+        offsets_c[e] = run;
+      }
+    }
+    run += kept[q];
+  }
+  if (threadIdx.x == 0) {
+    s_off[E] = offsets[E];
+    s_offc[E] = total;
+    if (blockIdx.x == 0) offsets_c[E] = total;
+  }
+  __syncthreads();
+  const int64_t p = (int64_t)blockIdx.x * kCapThreads + threadIdx.x;
+  if (p >= Na) return;
+  if (p >= total) perm_c[p] = -1;  // past the kept rows
+  if (p >= s_off[E]) return;       // (a layout with dropped bad ids ends early)
+  int lo = 0, hi = E;              // s_off[lo] <= p < s_off[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_off[mid] <= p)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  const int r = (int)(p - s_off[lo]);
+  const int32_t a = perm_src[p];
+  if (a < 0 || a >= Na) return;
+  if (r < C) {
+    const int np = s_offc[lo] + r;
+    perm_c[np] = a;
+    inv_c[a] = np;
+    if (w_perm != nullptr) w_perm_c[np] = w_perm[p];
+  } else {
+    inv_c[a] = -1;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_capacity(const int32_t *counts, const int32_t *offsets, const int32_t *perm_src,
+                            const float *w_perm, int T, int k, int E, int C, int32_t *counts_c,
+                            int32_t *offsets_c, int32_t *perm_c, int32_t *inv_c, float *w_perm_c,
+                            cudaStream_t s) {
+  const int64_t Na = (int64_t)T * k;
+  const int blocks = (int)((Na + kCapThreads - 1) / kCapThreads);
+  return launch_pdl(capacity_kernel, dim3(blocks), dim3(kCapThreads), 0, s, counts, offsets,
+                    perm_src, w_perm, Na, E, C, counts_c, offsets_c, perm_c, inv_c, w_perm_c);
+}
 
 cudaError_t launch_dispatch(const int32_t *ids, const float *topk_w, int T, int k, int E,
                             int32_t *blk_counts, int32_t *blk_base, int32_t *counts,

@@ -73,7 +73,6 @@ static __device__ void write_tile_plan(const int32_t *__restrict__ offsets, int 
                                 int I, int shared, int32_t *__restrict__ plan, int num_sms,
                                 uint32_t *__restrict__ status) {
   const int64_t Na = (int64_t)T * k;
-  const int64_t R = Na + (shared ? T : 0);
   __shared__ int warp_tot[32];
   __shared__ int tot_gu, tot_dn, bad, max_m, n_chunks, n_wide, st_narrow, st_wide;
   const int nseg = E + (shared ? 1 : 0);
@@ -114,7 +113,9 @@ static __device__ void write_tile_plan(const int32_t *__restrict__ offsets, int 
       atomicAdd(&st_narrow, (m + kTileRowsGateUp - 1) / kTileRowsGateUp);
       atomicAdd(&st_wide, 2 * ((m + kTileRowsDown - 1) / kTileRowsDown));
     }
-    if (s < nseg) seg_row[s] = bad ? 0 : ((s < E) ? offsets[s] : (int)Na);
+    // the shared expert's rows follow the routed rows: at offsets[E] (= T*k
+    // without a capacity limit)
+    if (s < nseg) seg_row[s] = bad ? 0 : offsets[s < E ? s : E];
   }
   __syncthreads();
   // Pipeline layouts.  Down: "wide" (stages of 256 token rows) when most
@@ -163,7 +164,7 @@ static __device__ void write_tile_plan(const int32_t *__restrict__ offsets, int 
     run_dn += dn[q];
   }
   if (threadIdx.x == 0) {
-    seg_row[nseg] = bad ? 0 : (int)R;
+    seg_row[nseg] = bad ? 0 : offsets[E] + (shared ? T : 0);
     pref_gu[nseg] = tot_gu;
     pref_dn[nseg] = tot_dn;
     plan[3 * (nseg + 1)] = choose_split(tot_gu, H / kBK, num_sms, max_m);

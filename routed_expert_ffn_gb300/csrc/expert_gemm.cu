@@ -504,7 +504,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           bits = __bfloat16_as_ushort(__float2bfloat16_rn(g[q] / (1.0f + __expf(-g[q])) * u[q]));
         } else {
           const float val = g[q] * sW[n0 + q];
-          range_bad |= !(fabsf(val) <= 65504.0f);
+          // only stored columns count: the others hold whatever token rows
+          // follow the tile's (another segment's, or never written)
+          if (n0 + q < t.nrows) range_bad |= !(fabsf(val) <= 65504.0f);
           bits = __half_as_ushort(__float2half_rn(fminf(fmaxf(val, -65504.0f), 65504.0f)));
         }
         so[q * kBM + r] = bits;
@@ -563,7 +565,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!kGateUp) {
         for (int n = r; n < kTileRowsDown; n += 128) {
           const int64_t row = (int64_t)t.row0 + n;
-          sW[n] = (n < t.nrows && w_perm != nullptr && row < Na) ? w_perm[row] : 1.0f;
+          // routed segments: the gate weight; the shared expert: weight 1
+          sW[n] = (n < t.nrows && w_perm != nullptr && t.seg < E && row < Na) ? w_perm[row]
+                                                                              : 1.0f;
         }
         epi_sync();
       }

@@ -111,6 +111,7 @@ constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;
 
 struct Layout {
   size_t status, route_part, router_w, blk_counts, blk_base, plan, x_perm, h, out_perm;
+  size_t cap_counts, cap_offsets, cap_perm, cap_inv, cap_wperm;  // dropless dispatch under a capacity
   size_t split_part;
   size_t logits, topk_ids, topk_w, gap, counts, offsets, perm_src, inv_pos, w_perm;
   size_t total;
@@ -222,9 +223,19 @@ cudaError_t launch_expert_down(const moe_layer_desc_t &d, const void *w2, const 
                                const __nv_bfloat16 *h, const int32_t *plan, const float *w_perm,
                                float *split_part, uint32_t *split_cnt, __half *out_perm,
                                uint32_t *status, cudaStream_t s);
+// shared_base: null (the shared expert's rows at T*k) or a device pointer to
+// their first row (offsets[E] under a capacity limit).
 cudaError_t launch_combine(const __half *out_perm, const int32_t *inv_pos,
                            const float *topk_w, int T, int k, int H, int shared, __nv_bfloat16 *y,
-                           cudaStream_t s);
+                           cudaStream_t s, const int32_t *shared_base = nullptr);
+// Capacity limit (dispatch.cu): from a dropless dispatch (counts, offsets,
+// perm_src, w_perm of T*k assignments) the layout of the kept assignments --
+// the first C of each expert in token order -- with inv_pos = -1 for a
+// dropped assignment and perm_src = -1 past the kept rows.
+cudaError_t launch_capacity(const int32_t *counts, const int32_t *offsets, const int32_t *perm_src,
+                            const float *w_perm, int T, int k, int E, int C, int32_t *counts_c,
+                            int32_t *offsets_c, int32_t *perm_c, int32_t *inv_c, float *w_perm_c,
+                            cudaStream_t s);
 // The persistent decode layer (decode_layer.cu): the whole forward in one
 // cooperative launch for shapes decode_layer_supported accepts.
 bool decode_layer_supported(const moe_layer_desc_t &d);

@@ -147,6 +147,8 @@ def test_binding_passes_pointer_width_arguments(lib):
                 assert a is ctypes.c_void_p or issubclass(a, ctypes._Pointer), (name, decl)
             elif decl.startswith("size_t"):
                 assert a is ctypes.c_size_t, (name, decl)
+            elif decl.startswith("int64_t"):
+                assert a is ctypes.c_int64, (name, decl)
             else:
                 assert a is ctypes.c_int32, (name, decl)
 
@@ -175,3 +177,19 @@ def test_forward_path_validation_before_launch(lib):
         assert fwd(qwen3(T=4), path) in (moe.MOE_ERR_CUDA, moe.MOE_ERR_UNSUPPORTED_DEVICE)
     assert lib.moe_check_bounded_grid_wait(None, 1 << 20, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_check_bounded_grid_wait(0x10000, 16, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_expert_capacity_host_helper(lib):
+    import oracle
+    for (num, den), T, k, E in [((5, 4), 5, 1, 8), ((1, 1), 16, 1, 8), ((1, 1), 17, 1, 8),
+                                ((2, 1), 8192, 8, 128), ((5, 4), 1024, 8, 128),
+                                ((3, 7), 33, 4, 16)]:
+        assert lib.moe_expert_capacity(num, den, T, k, E) == oracle.expert_capacity(num, den, T * k, E)
+    assert lib.moe_expert_capacity(0, 1, 5, 1, 8) == 0
+    assert moe.moe_expert_capacity(1.25, 5, 1, 8) == 1
+    w = moe.LayerWeights(FAKE, None, FAKE, FAKE, None, None)
+    d = qwen3(T=64)
+    call = lambda c: lib.moe_layer_forward_capacity(ctypes.byref(d), ctypes.byref(w), FAKE, FAKE, c,
+                                                     FAKE, moe.moe_workspace_size(d), None)
+    assert call(0) == moe.MOE_ERR_INVALID_ARG
+    assert call(4) in (moe.MOE_ERR_CUDA, moe.MOE_ERR_UNSUPPORTED_DEVICE)
