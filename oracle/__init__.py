@@ -180,6 +180,100 @@ def kept_weights(ids, w, E: int, C: int) -> np.ndarray:
     return wk.reshape(ia.shape)
 
 
+# --------------------------------------------------- FP8 expert weights --
+# "MoE推理优化全景指南", section "量化与 offload 并非独立开关", "专家权重量化":
+# FP8 expert weights cut weight capacity and bandwidth; the scale layout is
+# the implementation's choice.  Reading: OCP FP8 E4M3 ("fn": no infinities;
+# 1 sign, 4 exponent bits with bias 7, 3 mantissa bits; normal values
+# 2^(E-7) * (1 + m/8), subnormal m * 2^-9, largest 448, code 0x7F / 0xFF is
+# NaN), one power-of-two scale 2^s per block of 128 rows x 128 columns of each
+# weight matrix, s the smallest integer with max|w| / 2^s <= 448, codes by
+# round-to-nearest-even of w / 2^s, saturating at +-448.  A power-of-two scale
+# makes code * 2^s exact in bf16, so the dequantised weights are bf16 tensors
+# and the layer is the unchanged definition over them.
+
+FP8_BLOCK = 128
+FP8_MAX = 448.0
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Values (float64) of E4M3 codes (uint8 array); NaN for 0x7F / 0xFF."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    normal = np.ldexp(1.0 + m / 8.0, (e - 7).astype(np.int64))
+    sub = np.ldexp(m.astype(np.float64), -9)
+    v = sign * np.where(e == 0, sub, normal)
+    return np.where((c & 0x7F) == 0x7F, np.nan, v)
+
+
+_E4M3_POS = e4m3_decode(np.arange(0x7F, dtype=np.uint8))  # codes 0..126, ascending
+
+
+def e4m3_encode(v) -> np.ndarray:
+    """Round float64 values to E4M3 codes: nearest value, ties to the even code
+    (mantissa bit 0 clear), saturating at +-448; the sign bit follows the
+    value's sign (so -0 gives 0x80)."""
+    a = np.asarray(v, dtype=np.float64)
+    mag = np.minimum(np.abs(a), FP8_MAX)
+    hi = np.clip(np.searchsorted(_E4M3_POS, mag, side="left"), 0, 126)
+    lo = np.clip(hi - 1, 0, 126)
+    d_hi = _E4M3_POS[hi] - mag
+    d_lo = mag - _E4M3_POS[lo]
+    pick_lo = (d_lo < d_hi) | ((d_lo == d_hi) & (lo % 2 == 0))
+    code = np.where(pick_lo, lo, hi).astype(np.int64)
+    code = np.where(mag == _E4M3_POS[hi], hi, code)
+    code = code | np.where(np.signbit(a), 0x80, 0)
+    return code.astype(np.uint8)
+
+
+def fp8_block_exponent(amax: float) -> int:
+    """The smallest integer s with amax / 2^s <= 448 (0 for an all-zero block)."""
+    if amax == 0.0:
+        return 0
+    _, x = np.frexp(amax)
+    s = int(x) - 9
+    while amax / 2.0 ** s > FP8_MAX:
+        s += 1
+    while amax / 2.0 ** (s - 1) <= FP8_MAX:
+        s -= 1
+    return s
+
+
+def quantize_fp8(w) -> Tuple[np.ndarray, np.ndarray]:
+    """E4M3 codes [n, rows, K] and block exponents [n, ceil(rows/128),
+    ceil(K/128)] (int8) of bf16 matrices w [n, rows, K]."""
+    wa = _np(w, np.float64) if not isinstance(w, torch.Tensor) else w.double().numpy()
+    n, rows, K = wa.shape
+    B = FP8_BLOCK
+    nr, nk = -(-rows // B), -(-K // B)
+    q = np.empty(wa.shape, dtype=np.uint8)
+    sc = np.empty((n, nr, nk), dtype=np.int8)
+    for i in range(n):
+        for r in range(nr):
+            for c in range(nk):
+                blk = wa[i, r * B:(r + 1) * B, c * B:(c + 1) * B]
+                s = fp8_block_exponent(float(np.max(np.abs(blk))))
+                sc[i, r, c] = s
+                q[i, r * B:(r + 1) * B, c * B:(c + 1) * B] = e4m3_encode(blk / 2.0 ** s)
+    return q, sc
+
+
+def dequantize_fp8(q, sc) -> torch.Tensor:
+    """bf16 tensor [n, rows, K] of code * 2^s (exact in bf16)."""
+    qa = np.asarray(q, dtype=np.uint8)
+    n, rows, K = qa.shape
+    B = FP8_BLOCK
+    s = np.asarray(sc, dtype=np.int64)
+    full = np.repeat(np.repeat(s, B, axis=1), B, axis=2)[:, :rows, :K]
+    v = np.ldexp(e4m3_decode(qa), full)
+    t = torch.from_numpy(v).to(torch.bfloat16)
+    if not np.array_equal(t.double().numpy(), v):
+        raise ValueError("dequantised weights not exact in bf16")
+    return t
+
+
 def imbalance(counts, n_assign: int) -> Tuple[int, int]:
     """Imbalance ratio max_e n_e / (N_a/E) as an exact fraction (num, den)."""
     c = _np(counts, np.int32)
