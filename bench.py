@@ -56,6 +56,9 @@ def parse():
                    help="--sweep: comma-separated layer names to keep (default: all)")
     p.add_argument("--sweep-max-T", type=int, default=0,
                    help="--sweep: keep batch sizes up to this many tokens (default: all)")
+    p.add_argument("--weights", default="bf16", choices=["bf16", "fp8"],
+                   help="expert weight format: bf16, or E4M3 codes with a power-of-two scale "
+                        "per 128x128 block (moe_layer_forward_fp8, T <= 16)")
     p.add_argument("--capacity-factor", type=float, default=0.0,
                    help="time moe_layer_forward_capacity with C = ceil(cf * T * k / E) "
                         "(0: the dropless layer)")
@@ -198,18 +201,22 @@ def expert_gemm_utilisation(m_rows, peak_flops, hbm_bytes_per_s):
     return min(1.0, m_rows / ridge_rows(peak_flops, hbm_bytes_per_s))
 
 
-def algorithmic(cfg, T, counts):
-    """Algorithmic bytes and flops of one step and of the gate/up GEMM."""
+def algorithmic(cfg, T, counts, weight_bytes=2):
+    """Algorithmic bytes and flops of one step and of the gate/up GEMM
+    (weight_bytes per expert weight: 2 for bf16, 1 for FP8 codes, whose block
+    exponents add 1/16384)."""
     touched = int(sum(1 for c in counts if c > 0))
     H, I, E, k = cfg.H, cfg.I, cfg.E, cfg.k
-    per_expert = expert_bytes(H, I)
+    per_expert = expert_bytes(H, I, weight_bytes)
+    if weight_bytes == 1:
+        per_expert += -(-expert_params(H, I) // (128 * 128))
     nsh = 1 if cfg.shared else 0
     layer_bytes = (touched + nsh) * per_expert + E * H * 4 + 2 * T * H * 2
     layer_flops = 2 * T * k * 3 * H * I + nsh * 2 * T * 3 * H * I + 2 * T * H * E
     rows = T * k + nsh * T
     # the gate/up kernel reads each token row of x once from HBM (its k-fold
     # reuse is served by L2) and writes h
-    gateup_bytes = (touched + nsh) * 2 * I * H * 2 + T * H * 2 + rows * I * 2
+    gateup_bytes = (touched + nsh) * 2 * I * H * weight_bytes + T * H * 2 + rows * I * 2
     gateup_flops = 2 * rows * 2 * I * H
     return {"touched": touched, "layer_bytes": layer_bytes, "layer_flops": layer_flops,
             "gateup_bytes": gateup_bytes, "gateup_flops": gateup_flops}
@@ -354,34 +361,32 @@ def uses_persistent(cfg, T, path):
 
 
 def time_layer(moe, d, wts, x, y, ws, lay, cfg, T, steps, warmup, pg, stream, l2_flush=False,
-               path=None, capacity=0):
+               path=None, capacity=0, fp8_weights=None):
     """Warm-up, then the timed region (K forwards between two events, barrier +
     synchronize on both sides), then the same K forwards with stage events and
     with per-step events.  Returns the timings, the host time per call and the
     routing counts the workspace holds afterwards.  capacity > 0: the
-    capacity-limited forward (its stage events all fall around the call)."""
+    capacity-limited forward; fp8_weights: the FP8-weight forward (both one
+    call whose stage events all fall around it)."""
     import torch
-    if capacity > 0:
-        real = moe
 
-        class _Moe:
-            MOE_OK = real.MOE_OK
-            MOE_STAGE_EVENTS = real.MOE_STAGE_EVENTS
-            STAGE_NAMES = real.STAGE_NAMES
-            moe_get_device_status = staticmethod(real.moe_get_device_status)
-            workspace_view = staticmethod(real.workspace_view)
+    def fwd(stage_events=None):
+        if capacity <= 0 and fp8_weights is None:
+            moe.moe_layer_forward(d, wts, x, y, ws, stage_events=stage_events, path=path)
+            return
+        cur = torch.cuda.current_stream()
+        if stage_events is not None:
+            stage_events[0].record(cur)
+        if fp8_weights is not None:
+            moe.moe_layer_forward_fp8(d, fp8_weights, x, y, ws)
+        else:
+            moe.moe_layer_forward_capacity(d, wts, x, y, capacity, ws)
+        if stage_events is not None:
+            for e in stage_events[1:]:
+                e.record(cur)
 
-            @staticmethod
-            def moe_layer_forward(d_, w_, x_, y_, ws_, stream=None, stage_events=None, path=None):
-                if stage_events is not None:
-                    stage_events[0].record(torch.cuda.current_stream())
-                real.moe_layer_forward_capacity(d_, w_, x_, y_, capacity, ws_, stream=stream)
-                if stage_events is not None:
-                    for e in stage_events[1:]:
-                        e.record(torch.cuda.current_stream())
-        moe = _Moe
     for _ in range(warmup):
-        moe.moe_layer_forward(d, wts, x, y, ws, path=path)
+        fwd()
     torch.cuda.synchronize()
     st, raw = moe.moe_get_device_status(ws)
     if st != moe.MOE_OK:
@@ -402,7 +407,7 @@ def time_layer(moe, d, wts, x, y, ws, lay, cfg, T, steps, warmup, pg, stream, l2
         for i in range(steps):
             scratch.fill_(i & 0xff)
             ev_a[i].record(stream)
-            moe.moe_layer_forward(d, wts, x, y, ws, path=path)
+            fwd()
             ev_b[i].record(stream)
         torch.cuda.synchronize()
         barrier(pg)
@@ -411,7 +416,7 @@ def time_layer(moe, d, wts, x, y, ws, lay, cfg, T, steps, warmup, pg, stream, l2
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(stream)
         for i in range(steps):
-            moe.moe_layer_forward(d, wts, x, y, ws, path=path)
+            fwd()
         end.record(stream)
         torch.cuda.synchronize()
         barrier(pg)
@@ -420,7 +425,7 @@ def time_layer(moe, d, wts, x, y, ws, lay, cfg, T, steps, warmup, pg, stream, l2
     # ---- the same K steps again with CUDA events at every stage boundary, on
     # the launching stream: per-kernel durations for the roofline ----
     for i in range(steps):
-        moe.moe_layer_forward(d, wts, x, y, ws, stage_events=stage_ev[i], path=path)
+        fwd(stage_ev[i])
     torch.cuda.synchronize()
     t_wall1 = time.time()
     st, raw = moe.moe_get_device_status(ws)
@@ -432,7 +437,7 @@ def time_layer(moe, d, wts, x, y, ws, lay, cfg, T, steps, warmup, pg, stream, l2
     step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     step_ev[0].record(stream)
     for i in range(steps):
-        moe.moe_layer_forward(d, wts, x, y, ws, path=path)
+        fwd()
         step_ev[i + 1].record(stream)
     torch.cuda.synchronize()
     step_us = sorted(1e3 * step_ev[i].elapsed_time(step_ev[i + 1]) for i in range(steps))
@@ -445,7 +450,7 @@ def time_layer(moe, d, wts, x, y, ws, lay, cfg, T, steps, warmup, pg, stream, l2
     torch.cuda.synchronize()
     h0 = time.perf_counter()
     for _ in range(n_host):
-        moe.moe_layer_forward(d, wts, x, y, ws, path=path)
+        fwd()
     host_us = 1e6 * (time.perf_counter() - h0) / n_host
     torch.cuda.synchronize()
 
@@ -473,13 +478,14 @@ NEAR_TIE = 1e-5
 def layer_line(cfg, T, args, world, tm, pk, sampler):
     """The JSON line of one layer measurement (without e2e / cpu_baseline)."""
     counts = tm["counts"]
-    alg = algorithmic(cfg, T, counts)
+    fp8 = getattr(args, "weights", "bf16") == "fp8"
+    alg = algorithmic(cfg, T, counts, 1 if fp8 else 2)
     step_s = tm["ms_max"] / 1e3 / args.steps
     value = world * T / step_s
     stage_us = tm["stage_us"]
     # the persistent decode layer is one kernel (its stage events all fall at
     # its end): its roofline is the whole layer's
-    persistent = uses_persistent(cfg, T, args.path) and not tm["capacity"]
+    persistent = (uses_persistent(cfg, T, args.path) and not tm["capacity"]) or fp8
     whole = persistent or tm["capacity"] > 0
     if whole:
         kern = ("persistent decode layer (router, dispatch, tcgen05 GEMMs, combine)"
@@ -506,6 +512,7 @@ def layer_line(cfg, T, args, world, tm, pk, sampler):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": tm["ms_max"] / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "weights": "fp8-e4m3, power-of-two scale per 128x128 block" if fp8 else "bf16",
         "data": "synthetic (seeded counter-based generator; random-init weights of the layer shape)",
         "config": workload_config(cfg, T, args.l2_flush),
         "roofline": {"bound": "hbm", "kernel": kern,
@@ -564,8 +571,14 @@ def run_gpu(args):
     time.sleep(0.5 if sampler else 0)
     cap = (moe.moe_expert_capacity(args.capacity_factor, T, cfg.k, cfg.E)
            if args.capacity_factor > 0 else 0)
+    wq = None
+    if args.weights == "fp8":   # quantised once, before the timed region
+        qd = moe.quantize_layer_fp8(inp.w13, inp.w2, inp.w13_shared, inp.w2_shared)
+        wq = moe.layer_weights_fp8(inp.w_router, qd, inp.sel_bias)
+        inp.w13 = inp.w2 = inp.w13_shared = inp.w2_shared = None   # keep only the codes
+        torch.cuda.empty_cache()
     tm = time_layer(moe, d, wts, inp.x, y, ws, lay, cfg, T, args.steps, args.warmup, pg, stream,
-                    args.l2_flush, PATHS[args.path], cap)
+                    args.l2_flush, PATHS[args.path], cap, wq)
 
     # ---- end to end: pinned host x in, host y out, through the same call ----
     # Every step copies its x from pinned host memory, runs moe_layer_forward
@@ -595,7 +608,9 @@ def run_gpu(args):
             stream.wait_event(h2d_done[b])
             if i >= 2:
                 stream.wait_event(d2h_done[b])    # y_dev[b] of step i-2 is on the host
-            if cap:
+            if wq is not None:
+                moe.moe_layer_forward_fp8(d, wq, x_dev[b], y_dev[b], ws, stream=stream)
+            elif cap:
                 moe.moe_layer_forward_capacity(d, wts, x_dev[b], y_dev[b], cap, ws, stream=stream)
             else:
                 moe.moe_layer_forward(d, wts, x_dev[b], y_dev[b], ws, stream=stream,
@@ -626,7 +641,8 @@ def run_gpu(args):
     line["e2e"] = {"value": world * T * e_steps / (e_ms / 1e3), "unit": "tokens/s",
                    "h2d_bytes_per_step": T * cfg.H * 2, "d2h_bytes_per_step": T * cfg.H * 2}
     if not args.no_cpu_baseline:
-        hin = host_inputs(cfg, T, args.seed, experts_from_gpu=inp)
+        hin = (host_inputs(cfg, T, args.seed) if args.weights == "fp8"
+               else host_inputs(cfg, T, args.seed, experts_from_gpu=inp))
         n, dt, threads = cpu_oracle_sample(hin, args.cpu_tokens)
         line["cpu_baseline"] = {"value": n / dt, "unit": "tokens/s", "cores": threads,
                                 "kind": "oracle", "cpu_model": cpu_model(),
@@ -711,6 +727,7 @@ def run_sweep(args):
         if name not in layers:
             layers.clear()
             torch.cuda.empty_cache()
+            torch.cuda.empty_cache()
             layers[name] = synth.make_layer(cfg, 1, args.seed, device="cuda")
         full = layers[name]
         x = synth.make_tokens(cfg, T, args.seed, device="cuda")
@@ -728,8 +745,14 @@ def run_sweep(args):
         time.sleep(0.3)
         cap = (moe.moe_expert_capacity(args.capacity_factor, T, cfg.k, cfg.E)
                if args.capacity_factor > 0 else 0)
+        wq = None
+        if args.weights == "fp8":
+            if name + "_fp8" not in layers:
+                layers[name + "_fp8"] = moe.quantize_layer_fp8(full.w13, full.w2,
+                                                               full.w13_shared, full.w2_shared)
+            wq = moe.layer_weights_fp8(w_r, layers[name + "_fp8"], b)
         tm = time_layer(moe, d, wts, x, y, ws, lay, cfg, T, steps, args.warmup, None, stream,
-                        a.l2_flush, PATHS[args.path], cap)
+                        a.l2_flush, PATHS[args.path], cap, wq)
         sampler.stop()
         line = layer_line(cfg, T, a, 1, tm, pk, sampler)
         line["sweep"] = True

@@ -115,6 +115,30 @@ typedef struct {
   const void *w2_shared;
 } moe_layer_weights_t;
 
+/* Layer weights with FP8 expert matrices (moe_layer_forward_fp8): the router
+ * and selection bias as in moe_layer_weights_t; every expert matrix as E4M3
+ * codes (one byte per weight, same shape and order as the bf16 tensors) with
+ * one int8 block exponent s per 128 x 128 block (weight = code * 2^s),
+ * written by moe_quantize_fp8:
+ *  w13        [E,2I,H] E4M3;  w13_scale [E,2,ceil(I/128),ceil(H/128)] int8
+ *             (the gate half's blocks, then the up half's)
+ *  w2         [E,H,I] E4M3;   w2_scale [E,ceil(H/128),ceil(I/128)] int8
+ *  w13_shared [2I,H] / w13_shared_scale [2,ceil(I/128),ceil(H/128)] and
+ *  w2_shared [H,I] / w2_shared_scale [ceil(H/128),ceil(I/128)]: required iff
+ *             has_shared_expert. */
+typedef struct {
+  const float *w_router;
+  const float *sel_bias;
+  const void *w13;
+  const int8_t *w13_scale;
+  const void *w2;
+  const int8_t *w2_scale;
+  const void *w13_shared;
+  const int8_t *w13_shared_scale;
+  const void *w2_shared;
+  const int8_t *w2_shared_scale;
+} moe_layer_weights_fp8_t;
+
 /* Byte offsets (from the workspace base) of the buffers moe_layer_forward
  * leaves in the workspace, for inspection after the stream has synchronised.
  * R = T*k + (has_shared_expert ? T : 0) permuted rows. */
@@ -325,6 +349,40 @@ moe_status_t moe_layer_forward_ex(const moe_layer_desc_t *d, const moe_layer_wei
                                   const void *x, void *y, void *workspace, size_t ws_bytes,
                                   moe_stream_t stream, moe_event_t const *stage_events,
                                   int32_t path);
+
+/*
+ * FP8 expert weights ("MoE推理优化全景指南", section "量化与 offload 并非独立开关",
+ * "专家权重量化": FP8 cuts the expert weights' capacity and bandwidth; the
+ * scale layout is the implementation's choice).  Format: OCP FP8 E4M3 codes
+ * with one power-of-two scale per block of 128 rows x 128 columns of each
+ * matrix.  Because the scale is a power of two, code * 2^s is exact in bf16:
+ * the FP8 layer computes the bf16 layer over the dequantised weights, with
+ * half the weight bytes to stream.
+ *
+ * moe_quantize_fp8 -- quantise n bf16 matrices w [n][rows][K] to E4M3 codes q
+ * [n][rows][K] and block exponents scale_exp [n][ceil(rows/128)][ceil(K/128)]:
+ * s = the smallest integer with max|w| / 2^s <= 448 over the block (0 for an
+ * all-zero block), code = round-to-nearest-even of w / 2^s, saturating at
+ * +-448.  For W13 [E,2I,H] pass n = 2E, rows = I; for W2 [E,H,I] n = E,
+ * rows = H.  Limits: n, rows >= 1, 64 <= K, K % 64 == 0; w and q 16-byte
+ * aligned (MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED_SHAPE otherwise).
+ * Asynchronous on `stream`; the caller owns every buffer.
+ */
+moe_status_t moe_quantize_fp8(const void *w, int32_t n, int32_t rows, int32_t K, void *q,
+                              int8_t *scale_exp, moe_stream_t stream);
+
+/*
+ * moe_layer_forward_fp8 -- the layer forward (Moebius reading notes eq. (1))
+ * with FP8 expert weights (moe_layer_weights_fp8_t), for decode batches: the
+ * persistent single-kernel layer of moe_layer_forward_ex, its weight copies
+ * streaming E4M3 codes that converter warps turn into bf16 operand tiles
+ * (times the block scale) for the tensor cores.  Shapes: T <= 16 and
+ * H >= 256 (MOE_ERR_UNSUPPORTED_SHAPE otherwise); other arguments as
+ * moe_layer_forward.
+ */
+moe_status_t moe_layer_forward_fp8(const moe_layer_desc_t *d, const moe_layer_weights_fp8_t *w,
+                                   const void *x, void *y, void *workspace, size_t ws_bytes,
+                                   moe_stream_t stream);
 
 /*
  * Capacity limit ("MoE推理优化全景指南", section "Capacity、padding 与 token

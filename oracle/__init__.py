@@ -60,6 +60,8 @@ def _load():
         lib.oracle_expert_ffn.restype = None
         lib.oracle_layer_tokens.argtypes = [P, I64, I64, I64, P, P, P, P, P, P, P, I64, P, I32]
         lib.oracle_layer_tokens.restype = None
+        lib.oracle_quantize_fp8.argtypes = [P, I64, I64, I64, P, P, I32]
+        lib.oracle_quantize_fp8.restype = None
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = I32
         _lib = lib
@@ -208,55 +210,72 @@ def e4m3_decode(codes) -> np.ndarray:
     return np.where((c & 0x7F) == 0x7F, np.nan, v)
 
 
-_E4M3_POS = e4m3_decode(np.arange(0x7F, dtype=np.uint8))  # codes 0..126, ascending
-
-
 def e4m3_encode(v) -> np.ndarray:
     """Round float64 values to E4M3 codes: nearest value, ties to the even code
     (mantissa bit 0 clear), saturating at +-448; the sign bit follows the
-    value's sign (so -0 gives 0x80)."""
+    value's sign (so -0 gives 0x80).  Below 2^-6 the codes are multiples of
+    2^-9 (code = m); in the binade [2^e, 2^(e+1)) they are 2^e * (1 + m/8)
+    (code = (e + 7) * 8 + m), and rounding m up to 8 is the next binade's
+    first code."""
     a = np.asarray(v, dtype=np.float64)
     mag = np.minimum(np.abs(a), FP8_MAX)
-    hi = np.clip(np.searchsorted(_E4M3_POS, mag, side="left"), 0, 126)
-    lo = np.clip(hi - 1, 0, 126)
-    d_hi = _E4M3_POS[hi] - mag
-    d_lo = mag - _E4M3_POS[lo]
-    pick_lo = (d_lo < d_hi) | ((d_lo == d_hi) & (lo % 2 == 0))
-    code = np.where(pick_lo, lo, hi).astype(np.int64)
-    code = np.where(mag == _E4M3_POS[hi], hi, code)
+    sub = mag < 2.0 ** -6
+    _, x = np.frexp(np.where(sub, 1.0, mag))      # mag = f * 2^x, f in [0.5, 1)
+    e = x.astype(np.int64) - 1                     # mag in [2^e, 2^(e+1))
+    m_norm = np.rint((np.ldexp(np.where(sub, 1.0, mag), -e) - 1.0) * 8.0).astype(np.int64)
+    code_norm = (e + 7) * 8 + m_norm
+    code_sub = np.rint(np.ldexp(mag, 9)).astype(np.int64)   # 0 .. 8 (8 = 2^-6, code 0x08)
+    code = np.minimum(np.where(sub, code_sub, code_norm), 0x7E)
     code = code | np.where(np.signbit(a), 0x80, 0)
     return code.astype(np.uint8)
 
 
 def fp8_block_exponent(amax: float) -> int:
-    """The smallest integer s with amax / 2^s <= 448 (0 for an all-zero block)."""
-    if amax == 0.0:
-        return 0
+    """The smallest integer s with amax / 2^s <= 448 (0 for an all-zero
+    block), clamped to [-15, 7]."""
+    return int(_block_exponents(np.asarray([amax], dtype=np.float64))[0])
+
+
+FP8_EXP_MIN, FP8_EXP_MAX = -15, 7   # code * 2^s exact in fp16 (and bf16)
+
+
+def _block_exponents(amax: np.ndarray) -> np.ndarray:
     _, x = np.frexp(amax)
-    s = int(x) - 9
-    while amax / 2.0 ** s > FP8_MAX:
-        s += 1
-    while amax / 2.0 ** (s - 1) <= FP8_MAX:
-        s -= 1
-    return s
+    s = x.astype(np.int64) - 9                     # amax / 2^s in [256, 512)
+    s = np.where(np.ldexp(amax, -s) > FP8_MAX, s + 1, s)
+    s = np.where(np.ldexp(amax, -(s - 1)) <= FP8_MAX, s - 1, s)
+    s = np.clip(s, FP8_EXP_MIN, FP8_EXP_MAX)
+    return np.where(amax == 0.0, 0, s)
 
 
 def quantize_fp8(w) -> Tuple[np.ndarray, np.ndarray]:
     """E4M3 codes [n, rows, K] and block exponents [n, ceil(rows/128),
-    ceil(K/128)] (int8) of bf16 matrices w [n, rows, K]."""
-    wa = _np(w, np.float64) if not isinstance(w, torch.Tensor) else w.double().numpy()
+    ceil(K/128)] (int8) of bf16 matrices w [n, rows, K]: per 128 x 128
+    block, s = the smallest integer with max|w| / 2^s <= 448, then the codes
+    of w / 2^s."""
+    wa = w.double().numpy() if isinstance(w, torch.Tensor) else _np(w, np.float64)
     n, rows, K = wa.shape
     B = FP8_BLOCK
     nr, nk = -(-rows // B), -(-K // B)
-    q = np.empty(wa.shape, dtype=np.uint8)
+    pad = np.zeros((n, nr * B, nk * B))
+    pad[:, :rows, :K] = wa
+    blocks = pad.reshape(n, nr, B, nk, B)
+    amax = np.max(np.abs(blocks), axis=(2, 4))                       # [n, nr, nk]
+    sc = _block_exponents(amax)
+    scaled = np.ldexp(blocks, -sc[:, :, None, :, None])
+    q = e4m3_encode(scaled).reshape(n, nr * B, nk * B)[:, :rows, :K]
+    return np.ascontiguousarray(q), sc.astype(np.int8)
+
+
+def quantize_fp8_c(w, nthreads: int = 0) -> Tuple[np.ndarray, np.ndarray]:
+    """quantize_fp8 by the oracle's C implementation (the same definition,
+    block by block, OpenMP over blocks): for large weight sets."""
+    wa = _u16(w)
+    n, rows, K = wa.shape
+    nr, nk = -(-rows // FP8_BLOCK), -(-K // FP8_BLOCK)
+    q = np.empty((n, rows, K), dtype=np.uint8)
     sc = np.empty((n, nr, nk), dtype=np.int8)
-    for i in range(n):
-        for r in range(nr):
-            for c in range(nk):
-                blk = wa[i, r * B:(r + 1) * B, c * B:(c + 1) * B]
-                s = fp8_block_exponent(float(np.max(np.abs(blk))))
-                sc[i, r, c] = s
-                q[i, r * B:(r + 1) * B, c * B:(c + 1) * B] = e4m3_encode(blk / 2.0 ** s)
+    _load().oracle_quantize_fp8(_p(wa), n, rows, K, _p(q), _p(sc), nthreads or max_threads())
     return q, sc
 
 

@@ -251,3 +251,65 @@ void oracle_layer_tokens(const uint16_t *x, int64_t H, int64_t I, int64_t k, con
     }
     (void)nthreads;
 }
+
+/* ---------------------------------------------------- FP8 expert weights --
+ * "MoE推理优化全景指南", section "量化与 offload 并非独立开关", "专家权重量化".
+ * E4M3 codes with one power-of-two scale per 128 x 128 block: s = the
+ * smallest integer with max|w| / 2^s <= 448 (0 for an all-zero block),
+ * clamped to [-15, 7] so that code * 2^s is exact in fp16, code
+ * = the E4M3 value nearest to w / 2^s (ties to the even code, saturating at
+ * 448).  In the binade [2^e, 2^(e+1)) with e >= -6 the E4M3 values are
+ * 2^e * (1 + m/8), code (e + 7) * 8 + m; below 2^-6 they are m * 2^-9, code
+ * m; rounding m up to 8 lands on the next binade's first code.  nearbyint
+ * rounds half to even under the default rounding mode. */
+static uint8_t oracle_e4m3(double v) {
+  double a = fabs(v);
+  if (a > 448.0) a = 448.0;
+  int64_t code;
+  if (a < ldexp(1.0, -6)) {
+    code = (int64_t)nearbyint(ldexp(a, 9));
+  } else {
+    int x;
+    frexp(a, &x); /* a = f * 2^x, f in [0.5, 1) */
+    const int e = x - 1;
+    code = (int64_t)(e + 7) * 8 + (int64_t)nearbyint((ldexp(a, -e) - 1.0) * 8.0);
+  }
+  if (code > 0x7E) code = 0x7E;
+  if (signbit(v)) code |= 0x80;
+  return (uint8_t)code;
+}
+
+void oracle_quantize_fp8(const uint16_t *w, int64_t n, int64_t rows, int64_t K, uint8_t *q,
+                         int8_t *scale, int nthreads) {
+  const int64_t B = 128;
+  const int64_t nr = (rows + B - 1) / B, nk = (K + B - 1) / B;
+  const int64_t nblocks = n * nr * nk;
+#pragma omp parallel for num_threads(nthreads > 0 ? nthreads : 1) schedule(dynamic, 16)
+  for (int64_t b = 0; b < nblocks; ++b) {
+    const int64_t c = b % nk, r = (b / nk) % nr, i = b / (nk * nr);
+    const int64_t r0 = r * B, c0 = c * B;
+    const int64_t r1 = r0 + B < rows ? r0 + B : rows, c1 = c0 + B < K ? c0 + B : K;
+    double amax = 0.0;
+    for (int64_t rr = r0; rr < r1; ++rr)
+      for (int64_t cc = c0; cc < c1; ++cc) {
+        const double v = fabs(bf16_value(w[(i * rows + rr) * K + cc]));
+        if (v > amax) amax = v;
+      }
+    int s = 0;
+    if (amax > 0.0) {
+      int x;
+      frexp(amax, &x);
+      s = x - 9;
+      while (ldexp(amax, -s) > 448.0) ++s;
+      while (ldexp(amax, -(s - 1)) <= 448.0) --s;
+    }
+    if (s < -15) s = -15; /* code * 2^s exact in fp16 */
+    if (s > 7) s = 7;
+    scale[b] = (int8_t)s;
+    for (int64_t rr = r0; rr < r1; ++rr)
+      for (int64_t cc = c0; cc < c1; ++cc) {
+        const int64_t idx = (i * rows + rr) * K + cc;
+        q[idx] = oracle_e4m3(ldexp(bf16_value(w[idx]), -s));
+      }
+  }
+}

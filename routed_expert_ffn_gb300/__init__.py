@@ -64,6 +64,14 @@ _LAYOUT_FIELDS = ("status", "logits", "topk_ids", "topk_w", "gap", "counts", "of
                   "perm_src", "inv_pos", "w_perm", "x_perm", "h", "out_perm", "plan", "total")
 
 
+class LayerWeightsFp8(ctypes.Structure):
+    _fields_ = [("w_router", ctypes.c_void_p), ("sel_bias", ctypes.c_void_p),
+                ("w13", ctypes.c_void_p), ("w13_scale", ctypes.c_void_p),
+                ("w2", ctypes.c_void_p), ("w2_scale", ctypes.c_void_p),
+                ("w13_shared", ctypes.c_void_p), ("w13_shared_scale", ctypes.c_void_p),
+                ("w2_shared", ctypes.c_void_p), ("w2_shared_scale", ctypes.c_void_p)]
+
+
 class WorkspaceLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in _LAYOUT_FIELDS]
 
@@ -96,6 +104,8 @@ def library() -> ctypes.CDLL:
         "moe_check_bounded_wait": ([P, S, P], I32),
         "moe_check_bounded_grid_wait": ([P, S, P], I32),
         "moe_expert_capacity": ([ctypes.c_int64, ctypes.c_int64, I32, I32, I32], I32),
+        "moe_quantize_fp8": ([P, I32, I32, I32, P, P, P], I32),
+        "moe_layer_forward_fp8": ([D, ctypes.POINTER(LayerWeightsFp8), P, P, P, S, P], I32),
         "moe_layer_forward_capacity": ([D, ctypes.POINTER(LayerWeights), P, P, I32, P, S, P], I32),
         "moe_layer_forward_ex": ([D, ctypes.POINTER(LayerWeights), P, P, P, S, P, P, I32], I32),
         "moe_reshard_ep_to_tp_pack": ([I32, I32, I32, I32, P, P, P, P, P], I32),
@@ -288,6 +298,51 @@ def moe_layer_forward_capacity(d: LayerDesc, w: LayerWeights, x, y, capacity: in
     (the first ones in token order; the rest dropped)."""
     _check("moe_layer_forward_capacity", library().moe_layer_forward_capacity(
         ctypes.byref(d), ctypes.byref(w), _ptr(x), _ptr(y), int(capacity), _ptr(ws), _nbytes(ws),
+        _stream(stream)))
+
+
+def moe_quantize_fp8(w, n: int, rows: int, K: int, q, scale_exp, stream=None):
+    """E4M3 codes q [n,rows,K] (uint8) and block exponents scale_exp
+    [n, ceil(rows/128), ceil(K/128)] (int8) of bf16 matrices w [n,rows,K]."""
+    _check("moe_quantize_fp8", library().moe_quantize_fp8(
+        _ptr(w), int(n), int(rows), int(K), _ptr(q), _ptr(scale_exp), _stream(stream)))
+
+
+def quantize_layer_fp8(w13, w2, w13_shared=None, w2_shared=None):
+    """Device tensors (codes and block exponents) of a layer's expert weights:
+    w13 [E,2I,H] and w2 [E,H,I] bf16 (and the shared expert's)."""
+    import torch
+    out = {}
+
+    def q(name, w, n, rows, K, lead):
+        codes = torch.empty(tuple(w.shape), dtype=torch.uint8, device=w.device)
+        sc = torch.empty(lead + (-(-rows // 128), -(-K // 128)), dtype=torch.int8,
+                         device=w.device)
+        moe_quantize_fp8(w, n, rows, K, codes, sc)
+        out[name] = codes
+        out[name + "_scale"] = sc
+
+    E, I2, H = w13.shape
+    q("w13", w13, 2 * E, I2 // 2, H, (E, 2))      # [E,2,ceil(I/128),ceil(H/128)]
+    q("w2", w2, E, H, I2 // 2, (E,))              # [E,ceil(H/128),ceil(I/128)]
+    if w13_shared is not None:
+        q("w13_shared", w13_shared, 2, I2 // 2, H, (2,))
+        q("w2_shared", w2_shared, 1, H, I2 // 2, ())
+    return out
+
+
+def layer_weights_fp8(w_router, q: Dict, sel_bias=None) -> LayerWeightsFp8:
+    """The C struct over quantised expert weights (quantize_layer_fp8's dict)."""
+    g = lambda k: _ptr(q.get(k))
+    return LayerWeightsFp8(_ptr(w_router), _ptr(sel_bias), g("w13"), g("w13_scale"), g("w2"),
+                           g("w2_scale"), g("w13_shared"), g("w13_shared_scale"), g("w2_shared"),
+                           g("w2_shared_scale"))
+
+
+def moe_layer_forward_fp8(d: LayerDesc, w: LayerWeightsFp8, x, y, ws, stream=None):
+    """Layer forward with FP8 expert weights (decode batches, T <= 16)."""
+    _check("moe_layer_forward_fp8", library().moe_layer_forward_fp8(
+        ctypes.byref(d), ctypes.byref(w), _ptr(x), _ptr(y), _ptr(ws), _nbytes(ws),
         _stream(stream)))
 
 

@@ -466,6 +466,37 @@ moe_status_t moe_layer_forward_capacity(const moe_layer_desc_t *d, const moe_lay
   return cuda_status(e);
 }
 
+moe_status_t moe_quantize_fp8(const void *w, int32_t n, int32_t rows, int32_t K, void *q,
+                              int8_t *scale_exp, moe_stream_t stream) {
+  if (!ok_ptr(w) || !ok_ptr(q) || scale_exp == nullptr) return MOE_ERR_INVALID_ARG;
+  if (n < 1 || rows < 1 || K < 64 || K % 64 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((int64_t)n * rows * K >= ((int64_t)1 << 40)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  moe_status_t st = check_device();
+  if (st != MOE_OK) return st;
+  return cuda_status(launch_quantize_fp8(bf(w), n, rows, K, static_cast<uint8_t *>(q), scale_exp,
+                                         (cudaStream_t)stream));
+}
+
+moe_status_t moe_layer_forward_fp8(const moe_layer_desc_t *d, const moe_layer_weights_fp8_t *w,
+                                   const void *x, void *y, void *workspace, size_t ws_bytes,
+                                   moe_stream_t stream) {
+  if (workspace == nullptr || w == nullptr) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  moe_status_t st = prologue(d, workspace, ws_bytes, &L);
+  if (st != MOE_OK) return st;
+  if (!ok_ptr(x) || !ok_ptr(y) || !ok_ptr(w->w_router) || !ok_ptr(w->w13) || !ok_ptr(w->w2) ||
+      w->w13_scale == nullptr || w->w2_scale == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (d->gating == MOE_GATE_SIGMOID_BIAS_RENORM && !ok_ptr(w->sel_bias)) return MOE_ERR_INVALID_ARG;
+  if (d->has_shared_expert && (!ok_ptr(w->w13_shared) || !ok_ptr(w->w2_shared) ||
+                               w->w13_shared_scale == nullptr || w->w2_shared_scale == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (!decode_layer_supported(*d)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((st = check_device()) != MOE_OK) return st;
+  return cuda_status(
+      launch_decode_layer_fp8(*d, *w, bf(x), bfw(y), workspace, L, (cudaStream_t)stream));
+}
+
 moe_status_t moe_check_bounded_grid_wait(void *workspace, size_t ws_bytes, moe_stream_t stream) {
   if (workspace == nullptr || ws_bytes < kStatusBlockBytes ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)

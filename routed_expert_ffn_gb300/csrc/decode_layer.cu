@@ -48,6 +48,8 @@
 // resident, which the cross-CTA waits rely on.
 #include <string.h>
 
+#include <cuda_fp8.h>
+
 #include <mutex>
 
 #include "gating.cuh"
@@ -58,7 +60,10 @@ namespace moe {
 namespace {
 
 constexpr int kDThreads = 192;  // warps 0-3 epilogue, 4 TMA producer, 5 MMA
-constexpr int kDWarps = kDThreads / 32;
+// FP8 weights: four more warps (6-9) convert the staged E4M3 weight tiles
+// to the bf16 operand tiles the MMA reads
+constexpr int kDThreads8 = 320;
+constexpr int kDMaxWarps = kDThreads8 / 32;
 constexpr uint32_t kDChunk = kBM * kBK * 2;                       // 128 rows x 64 bf16
 constexpr uint32_t kDStageA = 2 * kStageKB * kDChunk;             // 64 KB of weights
 constexpr uint32_t kDStageB = kStageKB * kDecodeMaxT * kBK * 2;   // 4 KB: 16 token rows
@@ -69,12 +74,26 @@ constexpr uint32_t kDTmemCols = 64;   // two buffers of two 16-column accumulato
 constexpr int kDMaxAssign = kDecodeMaxT * kMaxK;
 constexpr int kDSlotFloats = 2 * kBM * kDecodeMaxT;  // one split piece: 2 x 128 x 16 fp32
 static_assert(kStageKB == 2, "a unit of work is two K blocks");
+// FP8 ring: staging stages of one unit's E4M3 weights (two K blocks x 256
+// rows x 64 bytes) filled by tensor copies, and operand stages of one K
+// block (256 bf16 weight rows written by the converters + 16 token rows by
+// a tensor copy) read by the MMA
+constexpr uint32_t kF8Stage = 2 * 2 * kBM * kBK;           // 32 KB
+constexpr int kF8Stages = 4;
+constexpr uint32_t kOpA = 2 * kBM * kBK * 2;               // 32 KB: two 128-row halves
+constexpr uint32_t kOpB = kDecodeMaxT * kBK * 2;           // 2 KB
+constexpr uint32_t kOpStage = kOpA + kOpB;
+constexpr int kOpStages = 2;
+static_assert(kF8Stages * kF8Stage + kOpStages * kOpStage <= kDStages * kDStage,
+              "the FP8 ring fits the stage ring");
+static_assert((kF8Stages * kF8Stage) % 1024 == 0 && kOpStage % 1024 == 0 && kOpA % 1024 == 0,
+              "operand tiles 1024-byte aligned (128-byte swizzle)");
 
 struct DecodeMaps {
   CUtensorMap gu, gu_sh;  // W13 [E][2][I][H]: box 128 rows x 2 halves x 2 K blocks
   CUtensorMap dn, dn_sh;  // W2 [E][H][I]: box 256 rows x 2 K blocks
-  CUtensorMap x;          // x [T][H]: box 16 rows x 2 K blocks
-  CUtensorMap h;          // h [R][I]: box 16 rows x 2 K blocks
+  CUtensorMap x;          // x [T][H]: box 16 rows x 2 K blocks (FP8 weights: 1)
+  CUtensorMap h;          // h [R][I]: box 16 rows x 2 K blocks (FP8 weights: 1)
 };
 
 struct DecodeArgs {
@@ -88,6 +107,10 @@ struct DecodeArgs {
   __nv_bfloat16 *y;
   float *part;       // [2 * gridDim.x][kDSlotFloats] split-piece partials (per region)
   uint32_t *status;  // the workspace status block
+  // FP8 weights: block exponents (scale 2^s per 128 x 128 block), W13
+  // [E][2][ceil(I/128)][ceil(H/128)], W2 [E][ceil(H/128)][ceil(I/128)]
+  const int8_t *s13, *s2, *s13_sh, *s2_sh;
+  __half *x16;  // FP8 weights: x in fp16, the tensor-core operand of the gate/up tiles
 };
 
 // The two regions of work (all gate/up tiles, then all down tiles), each cut
@@ -109,11 +132,12 @@ struct DSmem {
   uint32_t mask[kMaxE];       // tokens of each expert (bit t)
   int32_t offs[kMaxE + 1];
   int32_t seg_list[kMaxE + 1];  // segments with rows, in order (shared expert last)
-  float red[kDWarps][kDecodeMaxT];
+  float red[kDMaxWarps][kDecodeMaxT];
   int ntouched, last_flag, ok_flag;
   int done_tok[kDecodeMaxT];  // tokens whose combine this CTA runs next
   int ndone;
   uint64_t full[kDStages], empty[kDStages], tfull[2], tempty[2], fin;
+  uint64_t st_full[kF8Stages], st_empty[kF8Stages], op_full[kOpStages], op_empty[kOpStages];
   uint64_t rbar;  // router staging copies
   uint32_t tmem_slot;
   int abort_flag;
@@ -257,7 +281,7 @@ template <int NV>
 __device__ __forceinline__ void gate_tokens(const DecodeArgs &a, int T, int E, int k,
                                             int32_t *ids, float *w, float *gap) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int t = warp; t < T; t += kDWarps) {
+  for (int t = warp; t < T; t += (int)(blockDim.x >> 5)) {
     float s[NV];
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
@@ -268,8 +292,27 @@ __device__ __forceinline__ void gate_tokens(const DecodeArgs &a, int T, int E, i
   }
 }
 
-__global__ void __launch_bounds__(kDThreads, 1)
+// Two E4M3 codes (the low 16 bits of `two`) times 2^s as two fp16 values,
+// packed low first: one conversion (E4M3 is a subset of fp16) and one fp16
+// multiply by the power of two, exact for block exponents in [-15, 7].
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two, __half2 scale) {
+  const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xffffu), __NV_E4M3);
+  const __half2 v = __hmul2(*reinterpret_cast<const __half2 *>(&hr), scale);
+  return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// Instruction descriptor, kind::f16 with fp16 A and B (format 0 in bits 7-9
+// and 10-12), fp32 accumulator (bits 4-5 = 1), both K-major, N >> 3 in bits
+// 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+template <bool kFp8>
+__global__ void __launch_bounds__(kFp8 ? kDThreads8 : kDThreads, 1)
     decode_layer_kernel(const __grid_constant__ DecodeMaps maps, const DecodeArgs a) {
+  constexpr int kNT = kFp8 ? kDThreads8 : kDThreads;  // threads of the CTA
+  constexpr int kNW = kNT / 32;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -295,6 +338,16 @@ __global__ void __launch_bounds__(kDThreads, 1)
     }
     mbar_init(&S.fin, 1);
     mbar_init(&S.rbar, 1);
+    if (kFp8) {
+      for (int i = 0; i < kF8Stages; ++i) {
+        mbar_init(&S.st_full[i], 1);   // the producer's expected bytes
+        mbar_init(&S.st_empty[i], 4);  // the four converter warps
+      }
+      for (int i = 0; i < kOpStages; ++i) {
+        mbar_init(&S.op_full[i], 5);   // token-row copy + four converter warps
+        mbar_init(&S.op_empty[i], 1);  // the MMA's commit
+      }
+    }
     S.abort_flag = 0;
     S.ndone = 0;
     fence_mbar_init();
@@ -347,7 +400,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
         }
         if (!mbar_wait(&S.rbar, rph, &S.abort_flag, status, kStatusTimeoutLayer)) break;
         rph ^= 1u;
-        for (int hh = threadIdx.x * 4; hh < hn; hh += kDThreads * 4) {
+        for (int hh = threadIdx.x * 4; hh < hn; hh += kNT * 4) {
           const float4 wv = *reinterpret_cast<const float4 *>(sw + hh);
 #pragma unroll
           for (int t = 0; t < kDecodeMaxT; ++t) {
@@ -379,13 +432,32 @@ __global__ void __launch_bounds__(kDThreads, 1)
       if (warp == 0 && lane < nt) {
         float v = 0.f;
 #pragma unroll
-        for (int ww = 0; ww < kDWarps; ++ww) v += S.red[ww][lane];
+        for (int ww = 0; ww < kNW; ++ww) v += S.red[ww][lane];
         a.logits[(size_t)(t0 + lane) * E + e] = v;
       }
       __syncthreads();
     }
   }
+  if (kFp8) {
+    // x in fp16 for the gate/up tiles' tensor copies (exact for |x| in
+    // [2^-14, 65504]; below, fp16's subnormal steps of 2^-24)
+    const int64_t nv = (int64_t)T * H / 8;
+    for (int64_t i = (int64_t)blockIdx.x * kNT + threadIdx.x; i < nv; i += (int64_t)G * kNT) {
+      const uint4 r = reinterpret_cast<const uint4 *>(a.x)[i];
+      const uint32_t wd[4] = {r.x, r.y, r.z, r.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const __half2 hv = __floats2half2_rn(__uint_as_float(wd[q] << 16),
+                                             __uint_as_float(wd[q] & 0xffff0000u));
+        o[q] = *reinterpret_cast<const uint32_t *>(&hv);
+      }
+      reinterpret_cast<uint4 *>(a.x16)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    fence_proxy_async_global();  // read by tensor copies after the barrier
+  }
   bool ok = grid_sync(gbar, G, status, &S.ok_flag);
+  if (kFp8) fence_proxy_async_global();
 
   // ------------------------------------------- B: gating and dispatch --
   if (ok) {
@@ -457,14 +529,14 @@ __global__ void __launch_bounds__(kDThreads, 1)
     }
     __syncthreads();
     if (blockIdx.x == 0) {
-      for (int i = threadIdx.x; i < Na; i += kDThreads) {
+      for (int i = threadIdx.x; i < Na; i += kNT) {
         a.ids[i] = S.ids[i];
         a.topk_w[i] = S.w[i];
         a.perm_src[i] = S.perm[i];
         a.inv_pos[i] = S.inv[i];
         a.w_perm[i] = S.wperm[i];
       }
-      for (int e = threadIdx.x; e <= E; e += kDThreads) {
+      for (int e = threadIdx.x; e <= E; e += kNT) {
         a.offsets[e] = S.offs[e];
         if (e < E) a.counts[e] = __popc(S.mask[e]);
       }
@@ -499,7 +571,210 @@ __global__ void __launch_bounds__(kDThreads, 1)
   auto seg_row = [&](int s) { return s < E ? S.offs[s] : Na; };
   auto seg_rows = [&](int s) { return s < E ? S.offs[s + 1] - S.offs[s] : T; };
 
-  if (warp == 4) {
+  if (kFp8 && warp == 4) {
+    // ------------------------------------------- TMA producer, FP8 weights --
+    // lane 0: each unit's E4M3 weights into the staging ring; lane 1: each
+    // K block's token rows (x, or the expert's h rows once complete) into the
+    // operand ring.  Two threads, so a down tile waiting for its h does not
+    // hold back the weight copies behind it.
+    if (lane == 0) {
+      uint32_t st = 0, ph = 0, issued = 0;
+      bool pok = true;
+      Cursor cur = {0, sc.start[0]};
+      Piece pc;
+      while (pok && next_piece(sc, S.seg_list, cur, pc)) {
+        const bool sh = pc.seg >= E;
+        const CUtensorMap *ma =
+            pc.dn ? (sh ? &maps.dn_sh : &maps.dn) : (sh ? &maps.gu_sh : &maps.gu);
+        const int ecoord = sh ? 0 : pc.seg;
+        const int arow = pc.dn ? pc.j * 2 * kBM : pc.j * kBM;
+        for (int v = pc.p0; v < pc.p1; ++v) {
+          if (!mbar_wait(&S.st_empty[st], ph ^ 1u, &S.abort_flag, status, kStatusTimeoutLayer)) {
+            pok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&S.st_full[st], kF8Stage);
+          tma_load_5d(ring + st * kF8Stage, ma, &S.st_full[st], 0, arow, 0, 2 * v, ecoord);
+          ++issued;
+          if (++st == (uint32_t)kF8Stages) {
+            st = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      const uint32_t n = issued < (uint32_t)kF8Stages ? issued : (uint32_t)kF8Stages;
+      for (uint32_t i = 0; i < n; ++i) {
+        st = st == 0 ? kF8Stages - 1 : st - 1;
+        if (st == (uint32_t)kF8Stages - 1) ph ^= 1u;
+        mbar_wait_drain(&S.st_full[st], ph);
+      }
+    } else if (lane == 1) {
+      uint8_t *op = ring + kF8Stages * kF8Stage;
+      uint32_t st = 0, ph = 0, issued = 0;
+      bool pok = true;
+      int ready = -1;  // last segment seen complete
+      Cursor cur = {0, sc.start[0]};
+      Piece pc;
+      while (pok && next_piece(sc, S.seg_list, cur, pc)) {
+        if (pc.dn && pc.seg != ready) {
+          if (!wait_counter(seg_done + pc.seg, (uint32_t)JG, &S.abort_flag, status)) break;
+          ready = pc.seg;
+          fence_proxy_async_global();  // h was written by other CTAs' stores
+        }
+        const int row0 = seg_row(pc.seg);
+        for (int v = pc.p0; pok && v < pc.p1; ++v) {
+          for (int hk = 0; hk < kStageKB; ++hk) {
+            if (!mbar_wait(&S.op_empty[st], ph ^ 1u, &S.abort_flag, status,
+                           kStatusTimeoutLayer)) {
+              pok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&S.op_full[st], kOpB);
+            tma_load_3d(op + st * kOpStage + kOpA, pc.dn ? &maps.h : &maps.x, &S.op_full[st], 0,
+                        pc.dn ? row0 : 0, 2 * v + hk);
+            ++issued;
+            if (++st == (uint32_t)kOpStages) {
+              st = 0;
+              ph ^= 1u;
+            }
+          }
+        }
+      }
+      const uint32_t n = issued < (uint32_t)kOpStages ? issued : (uint32_t)kOpStages;
+      for (uint32_t i = 0; i < n; ++i) {
+        st = st == 0 ? kOpStages - 1 : st - 1;
+        if (st == (uint32_t)kOpStages - 1) ph ^= 1u;
+        mbar_wait_drain(&S.op_full[st], ph);
+      }
+    }
+    __syncwarp();
+  } else if (kFp8 && warp == 5) {
+    // ----------------------------------------------- MMA issuer, FP8 weights --
+    if (lane == 0) {
+      uint8_t *op = ring + kF8Stages * kF8Stage;
+      uint32_t st = 0, ph = 0, tl = 0;
+      bool mok = true;
+      const uint64_t desc0 = sdesc_k_sw128(smem_u32(op));
+      const uint32_t id = idesc_f16_f32(kBM, kDecodeMaxT);  // fp16 x fp16 -> fp32
+      Cursor cur = {0, sc.start[0]};
+      Piece pc;
+      for (; mok && next_piece(sc, S.seg_list, cur, pc); ++tl) {
+        const uint32_t buf = tl & 1u, use = tl >> 1;
+        if (!mbar_wait(&S.tempty[buf], (use & 1u) ^ 1u, &S.abort_flag, status,
+                       kStatusTimeoutLayer))
+          break;
+        tc_fence_after();
+        const uint32_t d0 = tmem_base + buf * 32u;
+        for (int v = pc.p0; mok && v < pc.p1; ++v) {
+          for (int hk = 0; hk < kStageKB; ++hk) {
+            if (!mbar_wait(&S.op_full[st], ph, &S.abort_flag, status, kStatusTimeoutLayer)) {
+              mok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t adesc = desc0 + st * (kOpStage >> 4);
+            const uint64_t bdesc = adesc + (kOpA >> 4);
+            const uint32_t acc = (v != pc.p0 || hk != 0) ? 1u : 0u;
+            // gate/up: gate rows, then up rows; down: W2 rows [0,128), [128,256)
+            mma_kblock(d0, adesc, bdesc, id, acc);
+            mma_kblock(d0 + 16, adesc + ((kBM * kBK * 2) >> 4), bdesc, id, acc);
+            umma_commit(&S.op_empty[st]);
+            if (++st == (uint32_t)kOpStages) {
+              st = 0;
+              ph ^= 1u;
+            }
+          }
+        }
+        if (!mok) break;
+        umma_commit(&S.tfull[buf]);
+      }
+      umma_commit(&S.fin);
+      mbar_wait_drain(&S.fin, 0);
+    }
+    __syncwarp();
+  } else if (kFp8 && warp >= 6) {
+    // ------------------------------------------- converters (FP8 weights) --
+    // Each K block of a staged unit: the two 128-row halves (128 rows x 64
+    // E4M3 codes each) become 128 rows x 64 fp16 in the 128-byte swizzled
+    // K-major layout the MMA reads, each code times its block's scale.  The
+    // MMA runs on fp16 operands: E4M3 codes convert to fp16 in one
+    // instruction, and the token rows (x, h) are fp16 in this mode.
+    // Thread ct takes 16-byte chunks ct, ct+128, ... of a half: a warp reads
+    // 512 consecutive bytes and writes eight whole swizzled rows.
+    const int ct = threadIdx.x - 6 * 32;
+    uint8_t *op = ring + kF8Stages * kF8Stage;
+    uint32_t s1 = 0, p1 = 0, s2 = 0, p2 = 0;
+    bool cok = true;
+    const int nrb13 = (I + kBM - 1) / kBM, nkb13 = (H + kBM - 1) / kBM;
+    const int nrb2 = (H + kBM - 1) / kBM, nkb2 = (I + kBM - 1) / kBM;
+    Cursor cur = {0, sc.start[0]};
+    Piece pc;
+    while (cok && next_piece(sc, S.seg_list, cur, pc)) {
+      const bool sh = pc.seg >= E;
+      const int ex = sh ? 0 : pc.seg;
+      for (int v = pc.p0; cok && v < pc.p1; ++v) {
+        __half2 scl[2];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          int e8 = 0;
+          if (!pc.dn) {
+            e8 = (sh ? a.s13_sh : a.s13)[((ex * 2 + half) * nrb13 + pc.j) * nkb13 + v];
+          } else if (2 * pc.j + half < nrb2) {  // (a half past H holds zero weights)
+            e8 = (sh ? a.s2_sh : a.s2)[(ex * nrb2 + 2 * pc.j + half) * nkb2 + v];
+          }
+          scl[half] = __float2half2_rn(ldexpf(1.0f, e8));  // 2^e8, exact in fp16
+        }
+        if (!mbar_wait(&S.st_full[s1], p1, &S.abort_flag, status, kStatusTimeoutLayer)) {
+          cok = false;
+          break;
+        }
+        const uint8_t *src = ring + s1 * kF8Stage;
+        for (int hk = 0; hk < kStageKB; ++hk) {
+          if (!mbar_wait(&S.op_empty[s2], p2 ^ 1u, &S.abort_flag, status, kStatusTimeoutLayer)) {
+            cok = false;
+            break;
+          }
+          uint8_t *dst = op + s2 * kOpStage;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const uint8_t *rs = src + (hk * 2 + half) * (kBM * kBK);
+            uint8_t *rd = dst + half * (kBM * kBK * 2);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int ci = ct + 128 * i;  // chunk: row ci / 4, codes (ci % 4) * 16 ..
+              const int row = ci >> 2, c = ci & 3;
+              const uint4 raw = *reinterpret_cast<const uint4 *>(rs + ci * 16);
+              const uint32_t wd[4] = {raw.x, raw.y, raw.z, raw.w};
+              uint32_t b[8];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                b[2 * q] = e4m3x2_to_f16x2(wd[q], scl[half]);
+                b[2 * q + 1] = e4m3x2_to_f16x2(wd[q] >> 16, scl[half]);
+              }
+              const int sw = row & 7;
+              *reinterpret_cast<uint4 *>(rd + row * 128 + (((2 * c) ^ sw) << 4)) =
+                  make_uint4(b[0], b[1], b[2], b[3]);
+              *reinterpret_cast<uint4 *>(rd + row * 128 + (((2 * c + 1) ^ sw) << 4)) =
+                  make_uint4(b[4], b[5], b[6], b[7]);
+            }
+          }
+          fence_proxy_async_shared();  // generic stores, read by the MMA (async proxy)
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.op_full[s2]);
+          if (++s2 == (uint32_t)kOpStages) {
+            s2 = 0;
+            p2 ^= 1u;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.st_empty[s1]);
+        if (++s1 == (uint32_t)kF8Stages) {
+          s1 = 0;
+          p1 ^= 1u;
+        }
+      }
+    }
+  } else if (warp == 4) {
     // ---------------------------------------------------- TMA producer --
     if (lane == 0) {
       uint32_t st = 0, ph = 0, issued = 0;
@@ -581,7 +856,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (!kFp8 && warp == 5) {
     // ------------------------------------------------------ MMA issuer --
     if (lane == 0) {
       uint32_t st = 0, ph = 0, tl = 0;
@@ -748,9 +1023,17 @@ __global__ void __launch_bounds__(kDThreads, 1)
               gv = (q == t) ? g[q] : gv;
               uv = (q == t) ? uu[q] : uv;
             }
-            if (col < I)
-              a.h[(size_t)(row0 + n) * I + col] =
-                  __float2bfloat16_rn(gv / (1.0f + __expf(-gv)) * uv);
+            if (col < I) {
+              const float hv = gv / (1.0f + __expf(-gv)) * uv;
+              uint16_t bits;
+              if (kFp8) {  // fp16 operand of the down tiles
+                range_bad |= !(fabsf(hv) <= 65504.0f);
+                bits = __half_as_ushort(__float2half_rn(fminf(fmaxf(hv, -65504.0f), 65504.0f)));
+              } else {
+                bits = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
+              }
+              reinterpret_cast<uint16_t *>(a.h)[(size_t)(row0 + n) * I + col] = bits;
+            }
           }
         }
         // h is read by tensor copies (async proxy) of other CTAs' down tiles:
@@ -874,7 +1157,7 @@ __global__ void __launch_bounds__(32) grid_wait_check_kernel(uint32_t *status) {
 
 // Tensor maps of one launch, cached by everything they depend on.
 struct DecodeKey {
-  int dev, T, H, E, I, k, shared;
+  int dev, T, H, E, I, k, shared, fp8;
   const void *w13, *w2, *w13s, *w2s, *x, *h;
   bool operator==(const DecodeKey &o) const { return memcmp(this, &o, sizeof o) == 0; }
 };
@@ -894,17 +1177,20 @@ bool decode_maps(const DecodeKey &key, DecodeMaps *out) {
     }
   DecodeMaps m;
   const int64_t R = (int64_t)key.T * key.k + (key.shared ? key.T : 0);
-  if (!weight_map(&m.gu, key.w13, key.H, key.I, 2, key.E, kBM)) return false;
-  if (!weight_map(&m.dn, key.w2, key.I, key.H, 1, key.E, 2 * kBM)) return false;
+  auto wmap = key.fp8 ? weight_map_u8 : weight_map;
+  if (!wmap(&m.gu, key.w13, key.H, key.I, 2, key.E, kBM)) return false;
+  if (!wmap(&m.dn, key.w2, key.I, key.H, 1, key.E, 2 * kBM)) return false;
   if (key.shared) {
-    if (!weight_map(&m.gu_sh, key.w13s, key.H, key.I, 2, 1, kBM)) return false;
-    if (!weight_map(&m.dn_sh, key.w2s, key.I, key.H, 1, 1, 2 * kBM)) return false;
+    if (!wmap(&m.gu_sh, key.w13s, key.H, key.I, 2, 1, kBM)) return false;
+    if (!wmap(&m.dn_sh, key.w2s, key.I, key.H, 1, 1, 2 * kBM)) return false;
   } else {
     m.gu_sh = m.gu;
     m.dn_sh = m.dn;
   }
-  if (!act_map(&m.x, key.x, key.H, key.T, kDecodeMaxT)) return false;
-  if (!act_map(&m.h, key.h, key.I, R, kDecodeMaxT)) return false;
+  // FP8 weights: operand stages of one K block
+  const int kbl = key.fp8 ? 1 : kStageKB;
+  if (!act_map(&m.x, key.x, key.H, key.T, kDecodeMaxT, kbl)) return false;
+  if (!act_map(&m.h, key.h, key.I, R, kDecodeMaxT, kbl)) return false;
   keys[next] = key;
   maps[next] = m;
   used[next] = true;
@@ -936,9 +1222,19 @@ bool decode_layer_supported(const moe_layer_desc_t &d) {
          num_sms() <= kDecodeMaxCtas;
 }
 
-cudaError_t launch_decode_layer(const moe_layer_desc_t &d, const moe_layer_weights_t &w,
-                                const __nv_bfloat16 *x, __nv_bfloat16 *y, void *workspace,
-                                const Layout &L, cudaStream_t s) {
+namespace {
+
+// The weights of one launch, either format.
+struct DecodeWeights {
+  const float *w_router, *sel_bias;
+  const void *w13, *w2, *w13s, *w2s;
+  const int8_t *s13, *s2, *s13s, *s2s;  // FP8 only
+};
+
+template <bool kFp8>
+cudaError_t launch_decode(const moe_layer_desc_t &d, const DecodeWeights &w,
+                          const __nv_bfloat16 *x, __nv_bfloat16 *y, void *workspace,
+                          const Layout &L, cudaStream_t s) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -951,11 +1247,14 @@ cudaError_t launch_decode_layer(const moe_layer_desc_t &d, const moe_layer_weigh
   key.I = d.I;
   key.k = d.k;
   key.shared = d.has_shared_expert ? 1 : 0;
+  key.fp8 = kFp8 ? 1 : 0;
   key.w13 = w.w13;
   key.w2 = w.w2;
-  key.w13s = key.shared ? w.w13_shared : nullptr;
-  key.w2s = key.shared ? w.w2_shared : nullptr;
-  key.x = x;
+  key.w13s = key.shared ? w.w13s : nullptr;
+  key.w2s = key.shared ? w.w2s : nullptr;
+  // FP8 weights: the gate/up tiles read x in fp16, kept in the x_perm buffer
+  // (which the persistent layer does not otherwise use)
+  key.x = kFp8 ? static_cast<const void *>(ws + L.x_perm) : static_cast<const void *>(x);
   key.h = ws + L.h;
   DecodeMaps maps;
   if (!decode_maps(key, &maps)) return cudaErrorInvalidValue;
@@ -984,16 +1283,40 @@ cudaError_t launch_decode_layer(const moe_layer_desc_t &d, const moe_layer_weigh
   a.y = y;
   a.part = reinterpret_cast<float *>(ws + L.split_part);
   a.status = reinterpret_cast<uint32_t *>(ws + L.status);
+  a.x16 = reinterpret_cast<__half *>(ws + L.x_perm);
+  a.s13 = w.s13;
+  a.s2 = w.s2;
+  a.s13_sh = w.s13s;
+  a.s2_sh = w.s2s;
   static bool configured[64] = {};
   if (!configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_layer_kernel,
+    cudaError_t e = cudaFuncSetAttribute(decode_layer_kernel<kFp8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kDSmemBytes);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  return launch_cooperative(decode_layer_kernel, dim3(num_sms()), dim3(kDThreads), kDSmemBytes, s,
-                            maps, a);
+  return launch_cooperative(decode_layer_kernel<kFp8>, dim3(num_sms()),
+                            dim3(kFp8 ? kDThreads8 : kDThreads), kDSmemBytes, s, maps, a);
+}
+
+}  // namespace
+
+cudaError_t launch_decode_layer(const moe_layer_desc_t &d, const moe_layer_weights_t &w,
+                                const __nv_bfloat16 *x, __nv_bfloat16 *y, void *workspace,
+                                const Layout &L, cudaStream_t s) {
+  const DecodeWeights dw = {w.w_router, w.sel_bias, w.w13, w.w2, w.w13_shared, w.w2_shared,
+                            nullptr,    nullptr,    nullptr, nullptr};
+  return launch_decode<false>(d, dw, x, y, workspace, L, s);
+}
+
+cudaError_t launch_decode_layer_fp8(const moe_layer_desc_t &d, const moe_layer_weights_fp8_t &w,
+                                    const __nv_bfloat16 *x, __nv_bfloat16 *y, void *workspace,
+                                    const Layout &L, cudaStream_t s) {
+  const DecodeWeights dw = {w.w_router,   w.sel_bias, w.w13,     w.w2,
+                            w.w13_shared, w.w2_shared, w.w13_scale, w.w2_scale,
+                            w.w13_shared_scale, w.w2_shared_scale};
+  return launch_decode<true>(d, dw, x, y, workspace, L, s);
 }
 
 cudaError_t launch_grid_wait_check(uint32_t *status_block, cudaStream_t s) {

@@ -92,6 +92,17 @@ bool encode_bf16_map(CUtensorMap *m, const void *base, int rank, const cuuint64_
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Byte tensor map (E4M3 codes), no swizzle: rows of a box land densely.
+static bool encode_u8_map(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims,
+                          const cuuint64_t *strides, const cuuint32_t *box) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void *>(base), dims,
+            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 
 namespace {
 
@@ -702,12 +713,25 @@ bool weight_map(CUtensorMap *m, const void *w, int K, int rows, int P, int E, in
   return encode_bf16_map(m, w, 5, dims, strides, box);
 }
 
-// Token rows [R][K] viewed as dims {64, R, K/64}; a box [kStageKB][h][64].
-bool act_map(CUtensorMap *m, const void *a, int K, int64_t R, int box_rows) {
+// Token rows [R][K] viewed as dims {64, R, K/64}; a box [kblocks][h][64]
+// (kblocks = kStageKB unless given).
+bool act_map(CUtensorMap *m, const void *a, int K, int64_t R, int box_rows, int kblocks) {
   const cuuint64_t dims[3] = {(cuuint64_t)kBK, (cuuint64_t)R, (cuuint64_t)(K / kBK)};
   const cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)kBK * 2};
-  const cuuint32_t box[3] = {(cuuint32_t)kBK, (cuuint32_t)box_rows, (cuuint32_t)kStageKB};
+  const cuuint32_t box[3] = {(cuuint32_t)kBK, (cuuint32_t)box_rows, (cuuint32_t)kblocks};
   return encode_bf16_map(m, a, 3, dims, strides, box);
+}
+
+// E4M3 weights [E][P][rows][K] (one byte per weight) as {64, rows, P, K/64,
+// E}: a box [kStageKB][P][box_rows][64 bytes], unswizzled.
+bool weight_map_u8(CUtensorMap *m, const void *w, int K, int rows, int P, int E, int box_rows) {
+  const cuuint64_t dims[5] = {(cuuint64_t)kBK, (cuuint64_t)rows, (cuuint64_t)P,
+                              (cuuint64_t)(K / kBK), (cuuint64_t)E};
+  const cuuint64_t rs = (cuuint64_t)K;
+  const cuuint64_t strides[4] = {rs, rs * rows, (cuuint64_t)kBK, rs * rows * P};
+  const cuuint32_t box[5] = {(cuuint32_t)kBK, (cuuint32_t)box_rows, (cuuint32_t)P,
+                             (cuuint32_t)kStageKB, 1};
+  return encode_u8_map(m, w, 5, dims, strides, box);
 }
 
 namespace {

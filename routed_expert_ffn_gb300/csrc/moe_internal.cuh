@@ -250,7 +250,16 @@ cudaError_t launch_grid_wait_check(uint32_t *status_block, cudaStream_t s);
 // as {64, rows, P, K/64, E} with boxes of box_rows rows and kStageKB K
 // blocks; token rows [R][K] as {64, R, K/64} with boxes of box_rows rows.
 bool weight_map(CUtensorMap *m, const void *w, int K, int rows, int P, int E, int box_rows);
-bool act_map(CUtensorMap *m, const void *a, int K, int64_t R, int box_rows);
+bool act_map(CUtensorMap *m, const void *a, int K, int64_t R, int box_rows,
+             int kblocks = kStageKB);
+// The same weight view over E4M3 codes (one byte each), unswizzled boxes.
+bool weight_map_u8(CUtensorMap *m, const void *w, int K, int rows, int P, int E, int box_rows);
+// FP8 expert weights (quantize.cu, decode_layer.cu).
+cudaError_t launch_quantize_fp8(const __nv_bfloat16 *w, int n, int rows, int K, uint8_t *q,
+                                int8_t *scale, cudaStream_t s);
+cudaError_t launch_decode_layer_fp8(const moe_layer_desc_t &d, const moe_layer_weights_fp8_t &w,
+                                    const __nv_bfloat16 *x, __nv_bfloat16 *y, void *workspace,
+                                    const Layout &L, cudaStream_t s);
 // One thread waits on an mbarrier nothing arrives on (waitcheck.cu).
 cudaError_t launch_bounded_wait_check(uint32_t *status, cudaStream_t s);
 // EP <-> TP expert-weight reshard permute (reshard.cu); a null source skips

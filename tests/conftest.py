@@ -52,3 +52,12 @@ def pytest_terminal_summary(terminalreporter):
     terminalreporter.write_line(
         f"routing total over {len(ROUTING_REPORT)} checks: tokens={tot['tokens']} "
         f"near_ties={tot['near_ties']} flips={tot['flips']} order_swaps={tot['order_swaps']}")
+
+    try:
+        from test_gpu_fp8 import FP8_QUALITY
+    except Exception:
+        FP8_QUALITY = []
+    if FP8_QUALITY:
+        terminalreporter.write_sep("-", "FP8 weights: relative L2 of the layer output vs bf16 weights")
+        for label, r in FP8_QUALITY:
+            terminalreporter.write_line(f"{label}: {r:.3e}")

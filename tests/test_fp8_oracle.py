@@ -58,10 +58,22 @@ def test_e4m3_saturates():
     assert oracle.e4m3_encode([-500.0])[0] == 0xFE
 
 
-@pytest.mark.parametrize("amax", [1.0, 448.0, 448.0001, 0.0779, 3e-7, 2.0 ** -20 * 448])
+@pytest.mark.parametrize("amax", [1.0, 448.0, 448.0001, 0.0779, 0.01, 2.0 ** -14 * 448])
 def test_block_exponent_is_the_smallest(amax):
     s = oracle.fp8_block_exponent(amax)
     assert amax / 2.0 ** s <= 448.0 < amax / 2.0 ** (s - 1)
+
+
+def test_block_exponent_clamps_to_the_fp16_exact_range():
+    assert oracle.fp8_block_exponent(3e-7) == -15          # would be -31
+    assert oracle.fp8_block_exponent(2.0 ** -16 * 448) == -15
+    assert oracle.fp8_block_exponent(1e6) == 7             # would be 12 (codes saturate)
+    # every code times 2^s for s in [-15, 7] is exact in fp16
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], dtype=np.uint8)
+    v = oracle.e4m3_decode(codes)
+    for s in (-15, -12, 0, 7):
+        x = np.ldexp(v, s)
+        assert np.array_equal(x.astype(np.float16).astype(np.float64), x)
 
 
 def test_quantize_blocks_and_dequantise_exactly():
@@ -79,7 +91,7 @@ def test_quantize_blocks_and_dequantise_exactly():
                 blk = np.s_[i, r * 128:(r + 1) * 128, c * 128:(c + 1) * 128]
                 s = int(sc[i, r, c])
                 amax = np.max(np.abs(wd[blk]))
-                assert amax / 2.0 ** s <= 448
+                assert amax / 2.0 ** s <= 448 or s == 7
                 # rounding error: half a step of E4M3 at the value's binade
                 # (2^-4 relative for normals), 2^-10 * 2^s absolute below
                 err = np.abs(dd[blk] - wd[blk])
@@ -88,3 +100,15 @@ def test_quantize_blocks_and_dequantise_exactly():
     # the quantised layer's weights are within FP8 precision of the originals
     rel = np.linalg.norm(dd - wd) / np.linalg.norm(wd)
     assert rel < 0.03
+
+
+def test_c_quantizer_equals_the_numpy_definition():
+    w = synth.normal((4, 300, 448), 5, 3, 0.05, torch.bfloat16)
+    w[0, :7, :] *= 3000                        # saturating-range block neighbours
+    w[1, 128:256, 128:256] = 0
+    w[2, 40, 17] = -0.0
+    w[3] = (w[3].float() * 2.0 ** -30).to(torch.bfloat16)   # tiny values (negative exponents)
+    qa, sa = oracle.quantize_fp8(w)
+    qc, sc = oracle.quantize_fp8_c(w)
+    assert np.array_equal(sa, sc)
+    assert np.array_equal(qa, qc)

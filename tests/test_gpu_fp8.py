@@ -1,0 +1,121 @@
+"""FP8 expert weights (needs a GB300): the quantiser (moe_quantize_fp8) bit
+for bit against the oracle's, and the FP8 layer (moe_layer_forward_fp8: the
+persistent decode layer streaming E4M3 codes) against the oracle's fp64 layer
+over its own dequantised weights, on every layer configuration at decode
+sizes.  The oracle quantises the weights itself; the GPU's codes and block
+exponents must equal its bytes, so both sides run the same FP8 layer."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import routed_expert_ffn_gb300 as moe
+import synth
+from gpu_check import (LayerRun, assert_output_close, bf16_np, check_routing, host_copy,
+                       rel_l2)
+from test_gpu_layer import layer_inputs
+
+pytestmark = pytest.mark.gpu
+
+# relative L2 of the FP8 layer's output against the bf16 layer's, per case
+FP8_QUALITY = []
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from routed_expert_ffn_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+
+
+@pytest.mark.parametrize("n,rows,K,seed", [(3, 200, 448, 1), (1, 128, 128, 2), (2, 1536, 4096, 3),
+                                           (5, 64, 64, 4), (2, 192, 7168, 5)])
+def test_quantizer_matches_oracle(n, rows, K, seed):
+    w = synth.normal((n, rows, K), seed, 1, 0.03, torch.bfloat16)
+    if n >= 3:
+        w[0, :5] *= 4000                    # saturation-range neighbours
+        w[1, :128, :128] = 0                # an all-zero block
+        w[2] = (w[2].float() * 2.0 ** -30).to(torch.bfloat16)
+    wd = w.cuda()
+    q = torch.empty((n, rows, K), dtype=torch.uint8, device="cuda")
+    sc = torch.empty((n, -(-rows // 128), -(-K // 128)), dtype=torch.int8, device="cuda")
+    moe.moe_quantize_fp8(wd, n, rows, K, q, sc)
+    torch.cuda.synchronize()
+    rq, rs = oracle.quantize_fp8_c(w)
+    assert np.array_equal(sc.cpu().numpy(), rs)
+    assert np.array_equal(q.cpu().numpy(), rq)
+
+
+def _oracle_expert(w13_e, w2_e):
+    """The oracle's own quantisation of one expert: dequantised bf16 W13 and
+    W2, and the codes / exponents (to compare with the GPU's)."""
+    I2, H = w13_e.shape
+    q13, s13 = oracle.quantize_fp8_c(w13_e.reshape(2, I2 // 2, H))
+    q2, s2 = oracle.quantize_fp8_c(w2_e.reshape(1, H, I2 // 2))
+    d13 = oracle.dequantize_fp8(q13, s13).reshape(I2, H)
+    d2 = oracle.dequantize_fp8(q2, s2).reshape(H, I2 // 2)
+    return d13, d2, (q13, s13, q2, s2)
+
+
+def check_fp8_layer(inputs):
+    cfg, T = inputs.cfg, inputs.T
+    E, k, I, H = cfg.E, cfg.k, cfg.I, cfg.H
+    q = moe.quantize_layer_fp8(inputs.w13, inputs.w2, inputs.w13_shared, inputs.w2_shared)
+    run = LayerRun(inputs)
+    wq = moe.layer_weights_fp8(inputs.w_router, q, inputs.sel_bias)
+    moe.moe_layer_forward_fp8(run.d, wq, inputs.x, run.y, run.ws)
+    torch.cuda.synchronize()
+    st, raw = moe.moe_get_device_status(run.ws)
+    assert st == moe.MOE_OK, (st, raw)
+    meta = run.metadata()
+    host = host_copy(inputs, experts=[])
+    s = oracle.router_logits(host["x"], host["w_router"])
+    ids, w, gap = oracle.topk_gating(s, k, cfg.gating, host["sel_bias"])
+    bias = None if host["sel_bias"] is None else host["sel_bias"].numpy()
+    check_routing(meta["ids"], meta["w"], {"logits": s, "ids": ids, "w": w, "gap": gap},
+                  cfg.gating, bias, label=f"{cfg.name} T={T} fp8")
+    rc, ro, rp, ri = oracle.dispatch(meta["ids"], E)
+    assert np.array_equal(meta["counts"], rc) and np.array_equal(meta["perm_src"], rp)
+    toks = [t for t in range(T) if not (gap[t] < 1e-5)]
+    need = sorted({int(e) for t in toks for e in ids[t]})
+    host = host_copy(inputs, experts=need)
+    d13, d2 = {}, {}
+    for e in need:
+        d13[e], d2[e], (q13, s13, q2, s2) = _oracle_expert(host["w13"][e], host["w2"][e])
+        # the GPU's bytes for this expert are the oracle's
+        assert np.array_equal(q["w13"][e].cpu().numpy().reshape(q13.shape), q13)
+        assert np.array_equal(q["w13_scale"][e].cpu().numpy().reshape(s13.shape), s13)
+        assert np.array_equal(q["w2"][e].cpu().numpy().reshape(q2.shape), q2)
+        assert np.array_equal(q["w2_scale"][e].cpu().numpy().reshape(s2.shape), s2)
+    d13s = d2s = None
+    if cfg.shared:
+        d13s, d2s, _ = _oracle_expert(host["w13_shared"], host["w2_shared"])
+    y_ref = oracle.layer_tokens(host["x"], ids, w, d13, d2, toks, d13s, d2s)
+    got = bf16_np(run.y[toks])
+    assert_output_close(got, y_ref, "y (fp8)")
+    # the quantisation's own effect: the bf16 layer's output
+    y_bf16 = oracle.layer_tokens(host["x"], ids, w, host["w13"], host["w2"], toks,
+                                 host["w13_shared"], host["w2_shared"])
+    FP8_QUALITY.append((f"{cfg.name} T={T}", rel_l2(y_ref, y_bf16)))
+    return rel_l2(y_ref, y_bf16)
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 1), ("tiny", 16), ("mixtral", 1), ("mixtral", 4),
+                                    ("qwen3", 1), ("qwen3", 8), ("qwen3_tp8", 1),
+                                    ("qwen3_tp8", 16), ("dsv3", 2)])
+def test_fp8_layer_matches_oracle(name, T):
+    q_err = check_fp8_layer(layer_inputs(name, T))
+    # E4M3 with 128 x 128 block scales: a few percent of relative error against
+    # the bf16 weights' layer (reported; the parity above is exact-format)
+    assert q_err < 0.06
+
+
+def test_fp8_rejects_prefill_batches():
+    inp = layer_inputs("qwen3", 17)
+    q = moe.quantize_layer_fp8(inp.w13, inp.w2)
+    run = LayerRun(inp)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_layer_forward_fp8(run.d, moe.layer_weights_fp8(inp.w_router, q), inp.x, run.y,
+                                  run.ws)
+    assert ei.value.status == moe.MOE_ERR_UNSUPPORTED_SHAPE
