@@ -291,7 +291,7 @@ moe_status_t moe_grouped_swiglu_ffn(const moe_layer_desc_t *d, const void *x,
   float *split_part = at<float>(workspace, L.split_part);
   uint32_t *split_cnt = at<uint32_t>(workspace, L.status) + kSplitCounterWord;
   cudaError_t e = launch_gather_plan(bf(x), perm_src, nullptr, offsets, d->T, d->k, d->E, d->H,
-                                     d->I, d->has_shared_expert, x_perm, plan, status, s);
+                                     d->I, d->has_shared_expert, x_perm, h, plan, status, s);
   if (e == cudaSuccess)
     e = launch_expert_gateup(*d, w13, w13_shared, x_perm, plan, 0, split_part, split_cnt, h,
                              status, s);
@@ -374,7 +374,7 @@ moe_status_t moe_layer_forward_ex(const moe_layer_desc_t *d, const moe_layer_wei
     e = launch_gather_plan(bf(x), perm_src,
                            (int64_t)d->T * d->H * 2 > kGatherByTokenBytes ? inv_pos : nullptr,
                            offsets, d->T, d->k, d->E, d->H, d->I, d->has_shared_expert, x_perm,
-                           nullptr, status, s);  // the dispatch wrote the plan
+                           h, nullptr, status, s);  // the dispatch wrote the plan
   if (e == cudaSuccess) e = mark(3);
   if (e == cudaSuccess)
     e = launch_expert_gateup(*d, w->w13, w->w13_shared, x_perm, plan, 1, split_part, split_cnt, h,
@@ -453,7 +453,7 @@ moe_status_t moe_layer_forward_capacity(const moe_layer_desc_t *d, const moe_lay
     e = launch_gather_plan(bf(x), perm_src,
                            (int64_t)d->T * d->H * 2 > kGatherByTokenBytes ? inv_pos : nullptr,
                            offsets, d->T, d->k, d->E, d->H, d->I, d->has_shared_expert, x_perm,
-                           plan, status, s);
+                           h, plan, status, s);
   if (e == cudaSuccess)
     e = launch_expert_gateup(*d, w->w13, w->w13_shared, x_perm, plan, 0, split_part, split_cnt, h,
                              status, s);

@@ -125,8 +125,9 @@ __global__ void __launch_bounds__(256)
     gather_plan_kernel(const __nv_bfloat16 *__restrict__ x, const int32_t *__restrict__ perm_src,
                        const int32_t *__restrict__ inv_pos, const int32_t *__restrict__ offsets,
                        int T, int k, int E, int H, int I, int shared,
-                       __nv_bfloat16 *__restrict__ x_perm, int32_t *__restrict__ plan,
-                       int with_plan, int num_sms, uint32_t *__restrict__ status) {
+                       __nv_bfloat16 *__restrict__ x_perm, __nv_bfloat16 *__restrict__ h,
+                       int32_t *__restrict__ plan, int with_plan, int num_sms,
+                       uint32_t *__restrict__ status) {
   pdl_wait();
   pdl_launch_dependents();
   const int64_t Na = (int64_t)T * k;
@@ -134,6 +135,19 @@ __global__ void __launch_bounds__(256)
   if (with_plan && blockIdx.x == gridDim.x - 1) {
     write_tile_plan(offsets, T, k, E, H, I, shared, plan, num_sms, status);
     return;
+  }
+  {
+    // Rows past the last segment exist only when the segments end before
+    // T*k (a capacity limit, or caller-given offsets): the down GEMM's tiles
+    // read up to 256 h rows past their start, so the first 256 such rows of
+    // h are zeroed here (gate/up writes only segment rows).
+    const int64_t end = (int64_t)offsets[E] + (shared ? T : 0);
+    const int64_t tail = min(R, end + 256);
+    const int64_t nvh = (tail > end ? tail - end : 0) * (I / 8);
+    const int64_t nb = gridDim.x - with_plan;  // the gather blocks (not the plan block)
+    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvh;
+         v += nb * blockDim.x)
+      reinterpret_cast<uint4 *>(h + end * I)[v] = make_uint4(0, 0, 0, 0);
   }
   // ---- gather ----
   // the shared expert's rows start at offsets[E] (= Na without a capacity
@@ -341,15 +355,15 @@ cudaError_t launch_dispatch(const int32_t *ids, const float *topk_w, int T, int 
 
 cudaError_t launch_gather_plan(const __nv_bfloat16 *x, const int32_t *perm_src,
                                const int32_t *inv_pos, const int32_t *offsets, int T, int k, int E,
-                               int H, int I, int shared, __nv_bfloat16 *x_perm, int32_t *plan,
-                               uint32_t *status, cudaStream_t s) {
+                               int H, int I, int shared, __nv_bfloat16 *x_perm, __nv_bfloat16 *h,
+                               int32_t *plan, uint32_t *status, cudaStream_t s) {
   // eight warps per block: one per token (with inv_pos) or per x_perm row;
   // one more block writes the tile plan when `plan` is given
   const int64_t units = inv_pos != nullptr ? (int64_t)T : (int64_t)T * k + (shared ? T : 0);
   const int with_plan = plan != nullptr ? 1 : 0;
   const int blocks = (int)((units + 7) / 8) + with_plan;
   return launch_pdl(gather_plan_kernel, dim3(blocks), dim3(256), 0, s, x, perm_src, inv_pos,
-                    offsets, T, k, E, H, I, shared, x_perm, plan, with_plan, num_sms(), status);
+                    offsets, T, k, E, H, I, shared, x_perm, h, plan, with_plan, num_sms(), status);
 }
 
 }  // namespace moe

@@ -207,10 +207,12 @@ cudaError_t launch_dispatch(const int32_t *ids, const float *topk_w, int T, int 
 #define MOE_GATHER_TOKEN_KB 8192
 #endif
 constexpr int64_t kGatherByTokenBytes = (int64_t)MOE_GATHER_TOKEN_KB << 10;
+// h: the first 256 rows past the last segment (if the segments end before
+// T*k) are zeroed.
 cudaError_t launch_gather_plan(const __nv_bfloat16 *x, const int32_t *perm_src,
                                const int32_t *inv_pos, const int32_t *offsets, int T, int k, int E,
-                               int H, int I, int shared, __nv_bfloat16 *x_perm, int32_t *plan,
-                               uint32_t *status, cudaStream_t s);
+                               int H, int I, int shared, __nv_bfloat16 *x_perm, __nv_bfloat16 *h,
+                               int32_t *plan, uint32_t *status, cudaStream_t s);
 // split_part: kMaxSplitTiles x 2 x kBM x kSplitMaxRows fp32; split_cnt: the
 // GEMM's kMaxSplitTiles arrival counters (in the workspace status block).
 // plan_early: the plan was written before the kernel preceding the GEMM
