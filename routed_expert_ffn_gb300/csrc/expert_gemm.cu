@@ -130,7 +130,7 @@ struct TokenMaps {
 template <bool kGateUp>
 struct Cfg {
   static constexpr uint32_t STAGE_UNIT = kStageKB * kChunkBytes;  // 128 rows of a stage
-  static constexpr uint32_t SOUT_BYTES = 16 * kBM * 2;            // one 16-token slice
+  static constexpr uint32_t SOUT_BYTES = 16 * kBM * 2;            // one 16-token slice (8 x kBM words)
   // gate/up, wide layout: up-row values handed to the gate rows' threads
   static constexpr uint32_t BAR_BYTES = (2 * kMaxStages + 5) * 8 + 16;
   static constexpr size_t smem_bytes(int nseg) {
@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   uint8_t *ring = smem;  // [stages][weights | token rows]
-  uint16_t *sOut = reinterpret_cast<uint16_t *>(ring + kRingBytes);  // [2][16][kBM]
+  uint16_t *sOut = reinterpret_cast<uint16_t *>(ring + kRingBytes);  // [2][8][kBM] words
   // wide gate/up: the up values handed to the gate rows' threads, [2][16][64],
   // in the ring's last 12 KB (two 96 KB stages leave them free)
   float *sUp = reinterpret_cast<float *>(ring + 2 * 3 * kStageKB * kChunkBytes);
@@ -504,34 +504,61 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tile adds the S partials in split order and runs the same epilogue.
     const int r = warp * 32 + lane;  // TMEM lane = weight row of the tile
     uint32_t tl = 0, slice = 0;
-    bool range_bad = false;
+    // down: the largest magnitude written (NaN-propagating), checked once
+    float vmax = 0.f;
+    // A 16-token slice goes through smem as 32-bit words [8 token pairs][kBM
+    // columns]: word (p, r) holds column r of tokens n0 + 2p (low half) and
+    // n0 + 2p + 1 (high half), so each thread converts two values per
+    // instruction and stores one word per token pair.  Then every thread
+    // takes one (token pair, 8-column chunk), splits the halves apart with
+    // byte permutes and stores 16 bytes to each token's row.
     auto emit16 = [&](const Tile &t, int n0, int col0, const float(&g)[16],
                       const float(&u)[16]) {
-      uint16_t *so = sOut + (slice & 1u) * (16 * kBM);
+      uint32_t *so = reinterpret_cast<uint32_t *>(sOut) + (slice & 1u) * (8 * kBM);
+      float wv[16];
+      if (!kGateUp) {
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        uint16_t bits;
+        for (int q = 0; q < 16; q += 4) {
+          const float4 a = *reinterpret_cast<const float4 *>(sW + n0 + q);
+          wv[q] = a.x;
+          wv[q + 1] = a.y;
+          wv[q + 2] = a.z;
+          wv[q + 3] = a.w;
+        }
+      }
+#pragma unroll
+      for (int p = 0; p < 8; ++p) {
+        uint32_t word;
         if (kGateUp) {
-          bits = __bfloat16_as_ushort(__float2bfloat16_rn(g[q] / (1.0f + __expf(-g[q])) * u[q]));
+          const float g0 = g[2 * p], g1 = g[2 * p + 1];
+          word = pack_bf16x2(__fdividef(g0, 1.0f + __expf(-g0)) * u[2 * p],
+                             __fdividef(g1, 1.0f + __expf(-g1)) * u[2 * p + 1]);
         } else {
-          const float val = g[q] * sW[n0 + q];
+          const float v0 = g[2 * p] * wv[2 * p], v1 = g[2 * p + 1] * wv[2 * p + 1];
           // every column counts: the token rows a tile reads past its own
           // are another segment's, zero-filled past the tensor, or zeroed by
           // the gather past the last segment (measured: checking only the
           // stored columns made the TP-8 slice's down GEMM 3-70% slower)
-          range_bad |= !(fabsf(val) <= 65504.0f);
-          bits = __half_as_ushort(__float2half_rn(fminf(fmaxf(val, -65504.0f), 65504.0f)));
+          vmax = fmax_nan(vmax, fabsf(v0));
+          vmax = fmax_nan(vmax, fabsf(v1));
+          // magnitudes past the fp16 range saturate to +-65504
+          word = pack_f16x2_satfinite(v0, v1);
         }
-        so[q * kBM + r] = bits;
+        so[p * kBM + r] = word;
       }
       epi_sync();
-      // 16 token rows x 128 columns x 2 bytes = 256 chunks of 16 bytes
-      for (int c = r; c < 16 * (kBM / 8); c += 128) {
-        const int q = c / (kBM / 8), ch = c % (kBM / 8);
-        const int n = n0 + q, col = col0 + ch * 8;
-        if (n < t.nrows && col < out_cols)
-          *reinterpret_cast<uint4 *>(out + ((int64_t)t.row0 + n) * out_cols + col) =
-              *reinterpret_cast<const uint4 *>(so + q * kBM + ch * 8);
+      const int p = r >> 4, ch = r & 15;  // 8 token pairs x 16 chunks of 8 columns
+      const uint4 lo = *reinterpret_cast<const uint4 *>(so + p * kBM + ch * 8);
+      const uint4 hi = *reinterpret_cast<const uint4 *>(so + p * kBM + ch * 8 + 4);
+      const uint4 a = make_uint4(__byte_perm(lo.x, lo.y, 0x5410), __byte_perm(lo.z, lo.w, 0x5410),
+                                 __byte_perm(hi.x, hi.y, 0x5410), __byte_perm(hi.z, hi.w, 0x5410));
+      const uint4 b = make_uint4(__byte_perm(lo.x, lo.y, 0x7632), __byte_perm(lo.z, lo.w, 0x7632),
+                                 __byte_perm(hi.x, hi.y, 0x7632), __byte_perm(hi.z, hi.w, 0x7632));
+      const int n = n0 + 2 * p, col = col0 + ch * 8;
+      if (col < out_cols) {
+        uint16_t *o = out + ((int64_t)t.row0 + n) * out_cols + col;
+        if (n < t.nrows) *reinterpret_cast<uint4 *>(o) = a;
+        if (n + 1 < t.nrows) *reinterpret_cast<uint4 *>(o + out_cols) = b;
       }
       ++slice;
     };
@@ -550,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
           const float g = v[q], u = su[q * W + r];
-          so[q * W + r] = __bfloat16_as_ushort(__float2bfloat16_rn(g / (1.0f + __expf(-g)) * u));
+          so[q * W + r] = __bfloat16_as_ushort(__float2bfloat16_rn(__fdividef(g, 1.0f + __expf(-g)) * u));
         }
       }
       epi_sync();
@@ -687,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (range_bad) atomicOr(status, kStatusRange);
+    if (!kGateUp && !(vmax <= 65504.0f)) atomicOr(status, kStatusRange);
   }
 
   __syncthreads();
