@@ -62,9 +62,11 @@ def parse():
     p.add_argument("--capacity-factor", type=float, default=0.0,
                    help="time moe_layer_forward_capacity with C = ceil(cf * T * k / E) "
                         "(0: the dropless layer)")
-    p.add_argument("--path", default="auto", choices=["auto", "chain", "persistent"],
+    p.add_argument("--path", default="auto", choices=["auto", "chain", "persistent", "chain1sm"],
                    help="execution path of the layer forward: automatic choice (default), "
-                        "the kernel chain, or the persistent single-kernel layer (T <= 16)")
+                        "the kernel chain, the persistent single-kernel layer (T <= 16), or "
+                        "the kernel chain with one-SM GEMM tiles only (no CTA-pair tiles for "
+                        "prefill batches)")
     p.add_argument("--l2-flush", action="store_true",
                    help="write a 256 MB buffer before every timed step (each step then "
                         "timed alone); for layers whose working set fits in L2")
@@ -348,7 +350,7 @@ def new_events(stream, n):
     return evs
 
 
-PATHS = {"auto": None, "chain": 1, "persistent": 2}
+PATHS = {"auto": None, "chain": 1, "persistent": 2, "chain1sm": 3}
 
 # the persistent single-kernel layer's shapes (moe_layer_forward_ex)
 DECODE_MAX_T = 16
@@ -358,6 +360,14 @@ def uses_persistent(cfg, T, path):
     """Whether a forward of this shape runs as the persistent decode layer."""
     fits = T <= DECODE_MAX_T and cfg.H >= 256
     return path == "persistent" or (path == "auto" and fits)
+
+
+def uses_pair_tiles(cfg, T, path):
+    """Whether the chain's expert GEMMs run on CTA pairs (prefill batches:
+    T*k >= 256*E, H a multiple of 256, I of 128)."""
+    if path in ("persistent", "chain1sm") or uses_persistent(cfg, T, path):
+        return False
+    return T * cfg.k >= 256 * cfg.E and cfg.H % 256 == 0 and cfg.I % 128 == 0
 
 
 def time_layer(moe, d, wts, x, y, ws, lay, cfg, T, steps, warmup, pg, stream, l2_flush=False,
@@ -521,6 +531,8 @@ def layer_line(cfg, T, args, world, tm, pk, sampler):
                      "algorithmic_bytes": kern_bytes, "launch_us": kern_us,
                      "peak_source": pk["source"]},
         "path": "persistent" if persistent else "chain",
+        "gemm_tiles": ("cta_pair" if uses_pair_tiles(cfg, T, getattr(args, "path", "auto"))
+                       else "one_sm"),
         "layer_roofline": {"bound": "hbm" if layer_t_hbm >= layer_t_tc else "tensor",
                            "roof_us": layer_roof * 1e6, "step_us": step_s * 1e6,
                            "frac": layer_roof / step_s, "bytes": alg["layer_bytes"],

@@ -319,7 +319,9 @@ enum {
   MOE_PATH_KERNEL_CHAIN = 1,/* route, dispatch, gather, two GEMMs, combine: one
                                launch per stage, linked by programmatic
                                dependent launch */
-  MOE_PATH_PERSISTENT = 2   /* one cooperative launch for the whole layer */
+  MOE_PATH_PERSISTENT = 2,  /* one cooperative launch for the whole layer */
+  MOE_PATH_CHAIN_ONE_SM = 3 /* the kernel chain with one-SM GEMM tiles only: no
+                               CTA-pair tiles for prefill batches */
 };
 
 /*
@@ -341,6 +343,14 @@ enum {
  * latches a timeout (MOE_ERR_TIMEOUT from moe_get_device_status); call
  * moe_workspace_init before the next use of that workspace.
  * MOE_PATH_AUTO takes the persistent path for those shapes.
+ *
+ * In the kernel chain, prefill batches (T*k >= 256*E, H and I multiples of
+ * 128, H a multiple of 256) run both expert GEMMs on CTA pairs: a cluster of
+ * two CTAs on two SMs computes tiles of 256 weight rows by up to 256 token
+ * rows with tcgen05.mma.cta_group::2, each CTA holding half of both operands.
+ * MOE_PATH_CHAIN_ONE_SM runs the chain with one-SM tiles at every size; the
+ * two give results within rounding of each other (the K order of the fp32
+ * accumulation is the same; tile shapes differ).
  *   path: MOE_PATH_*; anything else returns MOE_ERR_INVALID_ARG.
  *   stage_events (as moe_layer_forward): with the persistent path the first
  *   event is recorded before the launch and all others after it.

@@ -33,6 +33,7 @@ MOE_GATE_SIGMOID_BIAS_RENORM = 3
 MOE_PATH_AUTO = 0
 MOE_PATH_KERNEL_CHAIN = 1
 MOE_PATH_PERSISTENT = 2
+MOE_PATH_CHAIN_ONE_SM = 3
 
 MOE_STAGE_EVENTS = 7
 STAGE_NAMES = ("route", "dispatch", "gather", "gateup", "down", "combine")

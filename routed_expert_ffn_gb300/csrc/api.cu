@@ -294,10 +294,10 @@ moe_status_t moe_grouped_swiglu_ffn(const moe_layer_desc_t *d, const void *x,
                                      d->I, d->has_shared_expert, x_perm, h, plan, status, s);
   if (e == cudaSuccess)
     e = launch_expert_gateup(*d, w13, w13_shared, x_perm, plan, 0, split_part, split_cnt, h,
-                             status, s);
+                             status, true, s);
   if (e == cudaSuccess)
     e = launch_expert_down(*d, w2, w2_shared, h, plan, w_perm, split_part,
-                           split_cnt + kMaxSplitTiles, static_cast<__half *>(out_perm), status, s);
+                           split_cnt + kMaxSplitTiles, static_cast<__half *>(out_perm), status, true, s);
   return cuda_status(e);
 }
 
@@ -327,7 +327,10 @@ moe_status_t moe_layer_forward_ex(const moe_layer_desc_t *d, const moe_layer_wei
   if (d->gating == MOE_GATE_SIGMOID_BIAS_RENORM && !ok_ptr(w->sel_bias)) return MOE_ERR_INVALID_ARG;
   if (d->has_shared_expert && (!ok_ptr(w->w13_shared) || !ok_ptr(w->w2_shared)))
     return MOE_ERR_INVALID_ARG;
-  if (path < MOE_PATH_AUTO || path > MOE_PATH_PERSISTENT) return MOE_ERR_INVALID_ARG;
+  if (path < MOE_PATH_AUTO || path > MOE_PATH_CHAIN_ONE_SM) return MOE_ERR_INVALID_ARG;
+  // the expert GEMMs may take CTA-pair tiles (prefill batches) unless the
+  // one-SM chain is asked for
+  const bool pair_ok = path != MOE_PATH_CHAIN_ONE_SM;
   const bool persistent_ok = decode_layer_supported(*d);
   if (path == MOE_PATH_PERSISTENT && !persistent_ok) return MOE_ERR_UNSUPPORTED_SHAPE;
   if ((st = check_device()) != MOE_OK) return st;
@@ -378,11 +381,11 @@ moe_status_t moe_layer_forward_ex(const moe_layer_desc_t *d, const moe_layer_wei
   if (e == cudaSuccess) e = mark(3);
   if (e == cudaSuccess)
     e = launch_expert_gateup(*d, w->w13, w->w13_shared, x_perm, plan, 1, split_part, split_cnt, h,
-                             status, s);
+                             status, pair_ok, s);
   if (e == cudaSuccess) e = mark(4);
   if (e == cudaSuccess)
     e = launch_expert_down(*d, w->w2, w->w2_shared, h, plan, w_perm, split_part,
-                           split_cnt + kMaxSplitTiles, out_perm, status, s);
+                           split_cnt + kMaxSplitTiles, out_perm, status, pair_ok, s);
   if (e == cudaSuccess) e = mark(5);
   if (e == cudaSuccess)
     e = launch_combine(out_perm, inv_pos, nullptr, d->T, d->k, d->H, d->has_shared_expert, bfw(y), s);
@@ -456,10 +459,10 @@ moe_status_t moe_layer_forward_capacity(const moe_layer_desc_t *d, const moe_lay
                            h, plan, status, s);
   if (e == cudaSuccess)
     e = launch_expert_gateup(*d, w->w13, w->w13_shared, x_perm, plan, 0, split_part, split_cnt, h,
-                             status, s);
+                             status, true, s);
   if (e == cudaSuccess)
     e = launch_expert_down(*d, w->w2, w->w2_shared, h, plan, w_perm, split_part,
-                           split_cnt + kMaxSplitTiles, out_perm, status, s);
+                           split_cnt + kMaxSplitTiles, out_perm, status, true, s);
   if (e == cudaSuccess)
     e = launch_combine(out_perm, inv_pos, nullptr, d->T, d->k, d->H, d->has_shared_expert, bfw(y),
                        s, offsets + d->E);

@@ -121,12 +121,6 @@ static_assert(kMaxStages == 5 && kRingBytes == 3 * (2 * kStageKB * kChunkBytes +
 static_assert(kRingBytes >= 2 * 3 * kStageKB * kChunkBytes + 16 * 64 * 4 * 2,
               "wide gate/up: 2 stages of 96 KB and the up-value exchange buffer");
 
-// Token-row tensor maps with box heights 16, 32, ..., 256 rows (x kStageKB K
-// blocks).
-struct TokenMaps {
-  CUtensorMap m[16];
-};
-
 template <bool kGateUp>
 struct Cfg {
   static constexpr uint32_t STAGE_UNIT = kStageKB * kChunkBytes;  // 128 rows of a stage
@@ -843,7 +837,7 @@ cudaError_t launch_gemm(const moe_layer_desc_t &d, const void *w, const void *w_
                         const __nv_bfloat16 *act, const int32_t *plan, int plan_early,
                         const float *w_perm,
                         void *out, float *split_part, uint32_t *split_cnt, uint32_t *status,
-                        cudaStream_t s) {
+                        bool pair_ok, cudaStream_t s) {
   using C = Cfg<kGateUp>;
   const int shared = d.has_shared_expert ? 1 : 0;
   const int nseg = d.E + shared;
@@ -869,6 +863,12 @@ cudaError_t launch_gemm(const moe_layer_desc_t &d, const void *w, const void *w_
   GemmMaps g;
   if (!gemm_maps<kGateUp>(key, &g)) return cudaErrorInvalidValue;
 
+  // prefill batches: tiles of 256 weight rows on CTA pairs (the pair kernel
+  // reads only the plan's segment rows)
+  if (pair_ok && gemm_pair_supported(d, kGateUp))
+    return launch_expert_gemm_pair(kGateUp, kGateUp ? g.maw : g.ma, kGateUp ? g.mawsh : g.msh,
+                                   g.mb, plan, nseg, d.E, K, rows, Na, w_perm, out, status, s);
+
   const size_t smem = C::smem_bytes(nseg);
   auto kern = expert_gemm_kernel<kGateUp>;
   static size_t configured[64] = {};  // per device
@@ -891,19 +891,19 @@ cudaError_t launch_gemm(const moe_layer_desc_t &d, const void *w, const void *w_
 cudaError_t launch_expert_gateup(const moe_layer_desc_t &d, const void *w13, const void *w13_shared,
                                  const __nv_bfloat16 *x_perm, const int32_t *plan, int plan_early,
                                  float *split_part, uint32_t *split_cnt, __nv_bfloat16 *h,
-                                 uint32_t *status, cudaStream_t s) {
+                                 uint32_t *status, bool pair_ok, cudaStream_t s) {
   return launch_gemm<true>(d, w13, w13_shared, x_perm, plan, plan_early, nullptr, h, split_part,
-                           split_cnt, status, s);
+                           split_cnt, status, pair_ok, s);
 }
 
 cudaError_t launch_expert_down(const moe_layer_desc_t &d, const void *w2, const void *w2_shared,
                                const __nv_bfloat16 *h, const int32_t *plan, const float *w_perm,
                                float *split_part, uint32_t *split_cnt, __half *out_perm,
-                               uint32_t *status, cudaStream_t s) {
+                               uint32_t *status, bool pair_ok, cudaStream_t s) {
   // the plan comes from the dispatch or the gather kernel: at least two
   // launches before the down GEMM
   return launch_gemm<false>(d, w2, w2_shared, h, plan, 1, w_perm, out_perm, split_part, split_cnt,
-                            status, s);
+                            status, pair_ok, s);
 }
 
 }  // namespace moe

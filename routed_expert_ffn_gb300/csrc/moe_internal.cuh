@@ -217,14 +217,30 @@ cudaError_t launch_gather_plan(const __nv_bfloat16 *x, const int32_t *perm_src,
 // GEMM's kMaxSplitTiles arrival counters (in the workspace status block).
 // plan_early: the plan was written before the kernel preceding the GEMM
 // (by the dispatch), so the GEMM may read it before waiting on that kernel.
+// pair_ok: prefill-sized batches may run on CTA pairs (gemm_pair_supported)
 cudaError_t launch_expert_gateup(const moe_layer_desc_t &d, const void *w13, const void *w13_shared,
                                  const __nv_bfloat16 *x_perm, const int32_t *plan, int plan_early,
                                  float *split_part, uint32_t *split_cnt, __nv_bfloat16 *h,
-                                 uint32_t *status, cudaStream_t s);
+                                 uint32_t *status, bool pair_ok, cudaStream_t s);
 cudaError_t launch_expert_down(const moe_layer_desc_t &d, const void *w2, const void *w2_shared,
                                const __nv_bfloat16 *h, const int32_t *plan, const float *w_perm,
                                float *split_part, uint32_t *split_cnt, __half *out_perm,
-                               uint32_t *status, cudaStream_t s);
+                               uint32_t *status, bool pair_ok, cudaStream_t s);
+
+// Token-row tensor maps with box heights 16, 32, ..., 256 rows (x kStageKB K
+// blocks).
+struct TokenMaps {
+  CUtensorMap m[16];
+};
+// The expert GEMMs on CTA pairs (tcgen05.mma.cta_group::2): shapes it takes
+// (K a whole number of stages, output columns a whole number of pair tiles,
+// T*k >= 256*E), and its launch.  a / a_sh: this CTA's weight rows (gate/up:
+// 64 gate + 64 up rows; down: 128 W2 rows), kStageKB K blocks per box.
+bool gemm_pair_supported(const moe_layer_desc_t &d, bool gate_up);
+cudaError_t launch_expert_gemm_pair(bool gate_up, const CUtensorMap &a, const CUtensorMap &a_sh,
+                                    const TokenMaps &b, const int32_t *plan, int nseg, int E,
+                                    int K, int out_cols, int64_t Na, const float *w_perm,
+                                    void *out, uint32_t *status, cudaStream_t s);
 // shared_base: null (the shared expert's rows at T*k) or a device pointer to
 // their first row (offsets[E] under a capacity limit).
 cudaError_t launch_combine(const __half *out_perm, const int32_t *inv_pos,

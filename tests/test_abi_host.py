@@ -167,13 +167,14 @@ def test_forward_path_validation_before_launch(lib):
                                                    FAKE, moe.moe_workspace_size(d), None, None,
                                                    path)
     # an unknown path
-    assert fwd(qwen3(T=4), 3) == moe.MOE_ERR_INVALID_ARG
+    assert fwd(qwen3(T=4), 4) == moe.MOE_ERR_INVALID_ARG
     assert fwd(qwen3(T=4), -1) == moe.MOE_ERR_INVALID_ARG
     # the persistent layer takes at most 16 tokens and H >= 256
     assert fwd(qwen3(T=17), moe.MOE_PATH_PERSISTENT) == moe.MOE_ERR_UNSUPPORTED_SHAPE
     assert fwd(qwen3(T=4, H=128), moe.MOE_PATH_PERSISTENT) == moe.MOE_ERR_UNSUPPORTED_SHAPE
     # valid otherwise: the device check, which fails without a GPU
-    for path in (moe.MOE_PATH_AUTO, moe.MOE_PATH_KERNEL_CHAIN, moe.MOE_PATH_PERSISTENT):
+    for path in (moe.MOE_PATH_AUTO, moe.MOE_PATH_KERNEL_CHAIN, moe.MOE_PATH_PERSISTENT,
+                 moe.MOE_PATH_CHAIN_ONE_SM):
         assert fwd(qwen3(T=4), path) in (moe.MOE_ERR_CUDA, moe.MOE_ERR_UNSUPPORTED_DEVICE)
     assert lib.moe_check_bounded_grid_wait(None, 1 << 20, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_check_bounded_grid_wait(0x10000, 16, None) == moe.MOE_ERR_INVALID_ARG
