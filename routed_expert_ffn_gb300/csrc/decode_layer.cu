@@ -61,7 +61,7 @@ namespace {
 
 constexpr int kDThreads = 192;  // warps 0-3 epilogue, 4 TMA producer, 5 MMA
 // FP8 weights: four more warps (6-9) convert the staged E4M3 weight tiles
-// to the bf16 operand tiles the MMA reads
+// to the fp16 operand tiles the MMA reads
 constexpr int kDThreads8 = 320;
 constexpr int kDMaxWarps = kDThreads8 / 32;
 constexpr uint32_t kDChunk = kBM * kBK * 2;                       // 128 rows x 64 bf16
@@ -76,7 +76,7 @@ constexpr int kDSlotFloats = 2 * kBM * kDecodeMaxT;  // one split piece: 2 x 128
 static_assert(kStageKB == 2, "a unit of work is two K blocks");
 // FP8 ring: staging stages of one unit's E4M3 weights (two K blocks x 256
 // rows x 64 bytes) filled by tensor copies, and operand stages of one K
-// block (256 bf16 weight rows written by the converters + 16 token rows by
+// block (256 fp16 weight rows written by the converters + 16 token rows by
 // a tensor copy) read by the MMA
 constexpr uint32_t kF8Stage = 2 * 2 * kBM * kBK;           // 32 KB
 constexpr int kF8Stages = 4;

@@ -129,10 +129,12 @@ static __device__ void write_tile_plan(const int32_t *__restrict__ offsets, int 
   const bool wide_gu = st_narrow > 0 && 8 * st_wide <= 9 * st_narrow;
   const bool thin_all = max_m <= kThinRows;
   const bool medium_all = max_m <= kMediumRows;
-  // down, where it would otherwise be narrow: "pair" tiles of 256 W2 rows by
-  // <= 128 token rows (H >= 256)
-  // (measured in place of wide as well: Mixtral T=4096 down 744 -> 827 us)
-  const bool pair_dn = kDownPair && !thin_all && !medium_all && !wide_dn && H >= 2 * kBM;
+  // down, where it would otherwise be narrow or medium: "pair" tiles of 256
+  // W2 rows by <= 128 token rows (H >= 256)
+  // (measured in place of wide as well: Mixtral T=4096 down 744 -> 827 us;
+  // in place of medium: Qwen3 TP-8 slice T=128 down 61 -> 47 us, T=256
+  // 63 -> 49 us, Mixtral T=64 160 -> 155 us, Qwen3 T=128 unchanged)
+  const bool pair_dn = kDownPair && !thin_all && !wide_dn && H >= 2 * kBM;
   // thin (decode) pairing only for a short down K (I <= 4096); measured:
   // Qwen3 TP-8 slice (I = 192) down 3.6-10.6 us faster at T = 2..16, Qwen3
   // (I = 1536) 1.5 us at T = 1, Mixtral (I = 14336) 3.5 us slower at T = 1
@@ -176,10 +178,10 @@ static __device__ void write_tile_plan(const int32_t *__restrict__ offsets, int 
     plan[3 * (nseg + 1) + 2] = thin ? 2 : (wide_gu ? 1 : 0);
     // down only: 3 = medium (every tile <= 64 token rows: stages of 64 rows,
     // four in flight; measured 2% faster than narrow there, and far slower
-    // once hot experts reload their weights per 64-row unit); 4 = pair;
-    // 5 = thin pair
+    // once hot experts reload their weights per 64-row unit), taken only
+    // where pair tiles are not (H < 256); 4 = pair; 5 = thin pair
     plan[3 * (nseg + 1) + 3] =
-        thin ? (thin_pair_dn ? 5 : 2) : (medium_all ? 3 : (pair_dn ? 4 : (wide_dn ? 1 : 0)));
+        thin ? (thin_pair_dn ? 5 : 2) : (pair_dn ? 4 : (medium_all ? 3 : (wide_dn ? 1 : 0)));
   }
 }
 

@@ -467,11 +467,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
 bool gemm_pair_supported(const moe_layer_desc_t &d, bool gate_up) {
   const int K = gate_up ? d.H : d.I;
   const int cols = gate_up ? d.I : d.H;
-  // whole stages of K, whole pair tiles of output columns, and batches with
-  // at least 256 rows per routed expert on average (prefill)
+  // Rows per routed expert (on average) from which pair tiles pay, measured
+  // against the one-SM tiles: gate/up from 256 (at 64, Qwen3 T=1024 gate/up
+  // 521 -> 537 us); down from 64 when its K (= I) is at least 2048
+  // (DeepSeek-V3 T=2048 down 1210 -> 1132 us, Mixtral T=512 237 -> 172 us),
+  // else from 256 (Qwen3, I = 1536: no gain at 64).
+  const int min_rows = gate_up ? kPRows : (d.I >= 2048 ? 64 : kPRows);
+  // whole stages of K and whole pair tiles of output columns
   return num_sms() >= 2 && K % (kStageKB * kBK) == 0 &&
          cols % (gate_up ? 2 * kPWide : 2 * kBM) == 0 &&
-         (int64_t)d.T * d.k >= (int64_t)kPRows * d.E;
+         (int64_t)d.T * d.k >= (int64_t)min_rows * d.E;
 }
 
 cudaError_t launch_expert_gemm_pair(bool gate_up, const CUtensorMap &a, const CUtensorMap &a_sh,

@@ -234,7 +234,8 @@ struct TokenMaps {
 };
 // The expert GEMMs on CTA pairs (tcgen05.mma.cta_group::2): shapes it takes
 // (K a whole number of stages, output columns a whole number of pair tiles,
-// T*k >= 256*E), and its launch.  a / a_sh: this CTA's weight rows (gate/up:
+// enough rows per expert: gate/up T*k >= 256*E, down 64*E when I >= 2048),
+// and its launch.  a / a_sh: this CTA's weight rows (gate/up:
 // 64 gate + 64 up rows; down: 128 W2 rows), kStageKB K blocks per box.
 bool gemm_pair_supported(const moe_layer_desc_t &d, bool gate_up);
 cudaError_t launch_expert_gemm_pair(bool gate_up, const CUtensorMap &a, const CUtensorMap &a_sh,

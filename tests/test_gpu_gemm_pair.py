@@ -27,9 +27,12 @@ def built():
     torch.cuda.empty_cache()
 
 
-# (name, T, H, E, k, I, gating, shared, skew): every case has T*k >= 256*E
+# (name, T, H, E, k, I, gating, shared, skew): T*k >= 256*E (both GEMMs on
+# pairs) except pair_down, whose down GEMM alone takes pairs (I >= 2048 with
+# 64 <= T*k/E < 256)
 CASES = [
     ("pair_min", 512, 256, 4, 2, 128, synth.GATE_TOPK_SOFTMAX, False, None),
+    ("pair_down", 256, 256, 4, 2, 2048, synth.GATE_TOPK_SOFTMAX, True, ("normal", 0.5)),
     ("pair_skew", 700, 512, 4, 2, 256, synth.GATE_SIGMOID_BIAS_RENORM, True, ("normal", 1.0)),
     ("pair_wide", 300, 768, 2, 2, 384, synth.GATE_SOFTMAX_TOPK_RENORM, True, None),
     ("pair_mid", 2048, 1024, 8, 2, 512, synth.GATE_SOFTMAX_TOPK, False, ("normal", 0.5)),

@@ -186,8 +186,8 @@ def test_tile_plan(name, T):
     gu = [cdiv(m, 256) * cdiv(cfg.I, 64) if m > wide_above else cdiv(m, 128) * cdiv(cfg.I, 128)
           for m in ms]
     # down: "pair" tiles (256 W2 rows by <= 128 token rows) where the launch
-    # would otherwise be narrow
-    pair = max(ms) > 64 and not wide_dn and cfg.H >= 256
+    # would otherwise be narrow or medium
+    pair = max(ms) > 16 and not wide_dn and cfg.H >= 256
     # the same tiles in the thin layout when the down K is short
     thin_pair = max(ms) <= 16 and cfg.H >= 256 and cfg.I <= 4096
     dn = [cdiv(m, 128) * cdiv(cfg.H, 256) if pair or thin_pair
@@ -203,7 +203,7 @@ def test_tile_plan(name, T):
     medium = max(ms) <= 64
     want += [2 if thin else int(wide_gu),
              (5 if thin_pair else 2) if thin else
-             (3 if medium else (1 if wide_dn else (4 if pair else 0)))]
+             (4 if pair else (3 if medium else (1 if wide_dn else 0)))]
     assert plan == want
     if name == "mixtral":
         assert wide_gu and wide_dn   # uniform prefill: both GEMMs run wide
@@ -212,4 +212,4 @@ def test_tile_plan(name, T):
     if (name, T) in (("qwen3", 1), ("qwen3_tp8", 8)):
         assert thin
     if (name, T) == ("qwen3", 256):
-        assert medium and not thin
+        assert medium and not thin and pair   # the pair layout takes the medium batches
