@@ -362,12 +362,17 @@ def uses_persistent(cfg, T, path):
     return path == "persistent" or (path == "auto" and fits)
 
 
-def uses_pair_tiles(cfg, T, path):
-    """Whether the chain's expert GEMMs run on CTA pairs (prefill batches:
-    T*k >= 256*E, H a multiple of 256, I of 128)."""
+def pair_tiles(cfg, T, path):
+    """Tiles of the chain's expert GEMMs: "cta_pair" (tcgen05.mma.cta_group::2)
+    or "one_sm", by the library's rule -- gate/up on pairs from 256 rows per
+    routed expert on average, down from 64 when I >= 2048 (else 256); H a
+    multiple of 256, H and I of 128."""
     if path in ("persistent", "chain1sm") or uses_persistent(cfg, T, path):
-        return False
-    return T * cfg.k >= 256 * cfg.E and cfg.H % 256 == 0 and cfg.I % 128 == 0
+        return {"gateup": "one_sm", "down": "one_sm"}
+    shape_ok = cfg.H % 256 == 0 and cfg.I % 128 == 0
+    gu = shape_ok and T * cfg.k >= 256 * cfg.E
+    dn = shape_ok and T * cfg.k >= (64 if cfg.I >= 2048 else 256) * cfg.E
+    return {"gateup": "cta_pair" if gu else "one_sm", "down": "cta_pair" if dn else "one_sm"}
 
 
 def time_layer(moe, d, wts, x, y, ws, lay, cfg, T, steps, warmup, pg, stream, l2_flush=False,
@@ -531,8 +536,7 @@ def layer_line(cfg, T, args, world, tm, pk, sampler):
                      "algorithmic_bytes": kern_bytes, "launch_us": kern_us,
                      "peak_source": pk["source"]},
         "path": "persistent" if persistent else "chain",
-        "gemm_tiles": ("cta_pair" if uses_pair_tiles(cfg, T, getattr(args, "path", "auto"))
-                       else "one_sm"),
+        "gemm_tiles": pair_tiles(cfg, T, getattr(args, "path", "auto")),
         "layer_roofline": {"bound": "hbm" if layer_t_hbm >= layer_t_tc else "tensor",
                            "roof_us": layer_roof * 1e6, "step_us": step_s * 1e6,
                            "frac": layer_roof / step_s, "bytes": alg["layer_bytes"],

@@ -344,10 +344,12 @@ enum {
  * moe_workspace_init before the next use of that workspace.
  * MOE_PATH_AUTO takes the persistent path for those shapes.
  *
- * In the kernel chain, prefill batches (T*k >= 256*E, H and I multiples of
- * 128, H a multiple of 256) run both expert GEMMs on CTA pairs: a cluster of
- * two CTAs on two SMs computes tiles of 256 weight rows by up to 256 token
- * rows with tcgen05.mma.cta_group::2, each CTA holding half of both operands.
+ * In the kernel chain, prefill-sized batches run the expert GEMMs on CTA
+ * pairs: a cluster of two CTAs on two SMs computes tiles of 256 weight rows by
+ * up to 256 token rows with tcgen05.mma.cta_group::2, each CTA holding half
+ * of both operands.  Gate/up takes pairs from T*k >= 256*E, down from
+ * T*k >= 64*E when I >= 2048 (else 256*E); H must be a multiple of 256 and I
+ * of 128.
  * MOE_PATH_CHAIN_ONE_SM runs the chain with one-SM tiles at every size; the
  * two give results within rounding of each other (the K order of the fp32
  * accumulation is the same; tile shapes differ).
