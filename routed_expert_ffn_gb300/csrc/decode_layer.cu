@@ -75,19 +75,25 @@ constexpr int kDMaxAssign = kDecodeMaxT * kMaxK;
 constexpr int kDSlotFloats = 2 * kBM * kDecodeMaxT;  // one split piece: 2 x 128 x 16 fp32
 static_assert(kStageKB == 2, "a unit of work is two K blocks");
 // FP8 ring: staging stages of one unit's E4M3 weights (two K blocks x 256
-// rows x 64 bytes) filled by tensor copies, and operand stages of one K
-// block (256 fp16 weight rows written by the converters + 16 token rows by
-// a tensor copy) read by the MMA
+// rows x 64 bytes, 64-byte swizzled) filled by tensor copies, and operand
+// stages of one K block.  An operand stage's weights (two 128-row halves x
+// 64 fp16) are written by the converters into TMEM, where the MMA reads its
+// A operand; only its 16 token rows (a tensor copy) are in shared memory.
 constexpr uint32_t kF8Stage = 2 * 2 * kBM * kBK;           // 32 KB
-constexpr int kF8Stages = 4;
-constexpr uint32_t kOpA = 2 * kBM * kBK * 2;               // 32 KB: two 128-row halves
-constexpr uint32_t kOpB = kDecodeMaxT * kBK * 2;           // 2 KB
-constexpr uint32_t kOpStage = kOpA + kOpB;
-constexpr int kOpStages = 2;
+constexpr int kF8Stages = 6;
+constexpr uint32_t kOpStage = kDecodeMaxT * kBK * 2;       // 2 KB of token rows
+constexpr int kOpStages = 4;
+// TMEM of the FP8 layer: the accumulators in columns [0, 64), then per
+// operand stage two halves of 32 columns (128 lanes = weight rows, a column
+// = two fp16 of K)
+constexpr uint32_t kF8ACol = 64;
+constexpr uint32_t kF8AStageCols = 2 * kBK / 2;
+constexpr uint32_t kDTmemColsF8 = 512;
+static_assert(kF8ACol + kOpStages * kF8AStageCols <= kDTmemColsF8, "FP8 operands fit TMEM");
 static_assert(kF8Stages * kF8Stage + kOpStages * kOpStage <= kDStages * kDStage,
               "the FP8 ring fits the stage ring");
-static_assert((kF8Stages * kF8Stage) % 1024 == 0 && kOpStage % 1024 == 0 && kOpA % 1024 == 0,
-              "operand tiles 1024-byte aligned (128-byte swizzle)");
+static_assert((kF8Stages * kF8Stage) % 1024 == 0 && kOpStage % 1024 == 0,
+              "staging and token tiles 1024-byte aligned");
 
 struct DecodeMaps {
   CUtensorMap gu, gu_sh;  // W13 [E][2][I][H]: box 128 rows x 2 halves x 2 K blocks
@@ -275,6 +281,45 @@ __device__ __forceinline__ void mma_kblock(uint32_t d, uint64_t a, uint64_t b, u
   umma_bf16(d, a + 6, b + 6, idesc, 1u);
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T, one CTA: A's rows in the TMEM lanes, two
+// 16-bit elements of K per column.
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// One 64-deep K block with A in TMEM: four K16 steps of 8 columns.
+__device__ __forceinline__ void mma_kblock_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
+                                              uint32_t acc) {
+  umma_ts(d, a, b, idesc, acc);
+  umma_ts(d, a + 8, b + 2, idesc, 1u);
+  umma_ts(d, a + 16, b + 4, idesc, 1u);
+  umma_ts(d, a + 24, b + 6, idesc, 1u);
+}
+
+// 32 lanes x 32 consecutive 32-bit columns from registers; thread i writes
+// lane (base + i).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0],"
+      " {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16,"
+      " %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+      "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Top-k and gate weights of every token into shared memory, one warp per
 // token (NV logits per lane, E <= 32 * NV).
 template <int NV>
@@ -353,7 +398,7 @@ __global__ void __launch_bounds__(kFp8 ? kDThreads8 : kDThreads, 1)
     fence_mbar_init();
   }
   if (warp == 5) {
-    tmem_alloc(&S.tmem_slot, kDTmemCols);
+    tmem_alloc(&S.tmem_slot, kFp8 ? kDTmemColsF8 : kDTmemCols);
     tmem_relinquish();
   }
   if (warp == 4 && lane == 0) {
@@ -629,8 +674,8 @@ __global__ void __launch_bounds__(kFp8 ? kDThreads8 : kDThreads, 1)
               pok = false;
               break;
             }
-            mbar_arrive_expect_tx(&S.op_full[st], kOpB);
-            tma_load_3d(op + st * kOpStage + kOpA, pc.dn ? &maps.h : &maps.x, &S.op_full[st], 0,
+            mbar_arrive_expect_tx(&S.op_full[st], kOpStage);
+            tma_load_3d(op + st * kOpStage, pc.dn ? &maps.h : &maps.x, &S.op_full[st], 0,
                         pc.dn ? row0 : 0, 2 * v + hk);
             ++issued;
             if (++st == (uint32_t)kOpStages) {
@@ -672,12 +717,13 @@ __global__ void __launch_bounds__(kFp8 ? kDThreads8 : kDThreads, 1)
               break;
             }
             tc_fence_after();
-            const uint64_t adesc = desc0 + st * (kOpStage >> 4);
-            const uint64_t bdesc = adesc + (kOpA >> 4);
+            const uint64_t bdesc = desc0 + st * (kOpStage >> 4);
+            const uint32_t a0 = tmem_base + kF8ACol + st * kF8AStageCols;
             const uint32_t acc = (v != pc.p0 || hk != 0) ? 1u : 0u;
-            // gate/up: gate rows, then up rows; down: W2 rows [0,128), [128,256)
-            mma_kblock(d0, adesc, bdesc, id, acc);
-            mma_kblock(d0 + 16, adesc + ((kBM * kBK * 2) >> 4), bdesc, id, acc);
+            // A from TMEM -- gate/up: gate rows, then up rows; down: W2 rows
+            // [0,128), [128,256)
+            mma_kblock_ts(d0, a0, bdesc, id, acc);
+            mma_kblock_ts(d0 + 16, a0 + kF8AStageCols / 2, bdesc, id, acc);
             umma_commit(&S.op_empty[st]);
             if (++st == (uint32_t)kOpStages) {
               st = 0;
@@ -695,14 +741,18 @@ __global__ void __launch_bounds__(kFp8 ? kDThreads8 : kDThreads, 1)
   } else if (kFp8 && warp >= 6) {
     // ------------------------------------------- converters (FP8 weights) --
     // Each K block of a staged unit: the two 128-row halves (128 rows x 64
-    // E4M3 codes each) become 128 rows x 64 fp16 in the 128-byte swizzled
-    // K-major layout the MMA reads, each code times its block's scale.  The
+    // E4M3 codes each) become 128 rows x 64 fp16, each code times its
+    // block's scale, stored into the operand stage's TMEM columns, where the
+    // MMA reads its A operand.  Warp w writes the TMEM lanes of its quarter
+    // (w % 4), one weight row per thread: the row's 64 codes are four 16-byte
+    // chunks, read through the 64-byte swizzle (so the warp's 32 rows touch
+    // every bank once per phase), and become 32 columns of fp16 pairs.  The
     // MMA runs on fp16 operands: E4M3 codes convert to fp16 in one
     // instruction, and the token rows (x, h) are fp16 in this mode.
-    // Thread ct takes 16-byte chunks ct, ct+128, ... of a half: a warp reads
-    // 512 consecutive bytes and writes eight whole swizzled rows.
-    const int ct = threadIdx.x - 6 * 32;
-    uint8_t *op = ring + kF8Stages * kF8Stage;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // weight row of a 128-row half
+    const int sw = (r >> 1) & 3;        // 64-byte swizzle of the staged rows
+    const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16) + kF8ACol;
     uint32_t s1 = 0, p1 = 0, s2 = 0, p2 = 0;
     bool cok = true;
     const int nrb13 = (I + kBM - 1) / kBM, nkb13 = (H + kBM - 1) / kBM;
@@ -734,31 +784,25 @@ __global__ void __launch_bounds__(kFp8 ? kDThreads8 : kDThreads, 1)
             cok = false;
             break;
           }
-          uint8_t *dst = op + s2 * kOpStage;
+          tc_fence_after();  // the MMAs that read this stage's columns are complete
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
-            const uint8_t *rs = src + (hk * 2 + half) * (kBM * kBK);
-            uint8_t *rd = dst + half * (kBM * kBK * 2);
+            const uint8_t *rs = src + (hk * 2 + half) * (kBM * kBK) + r * kBK;
+            uint32_t w[32];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int ci = ct + 128 * i;  // chunk: row ci / 4, codes (ci % 4) * 16 ..
-              const int row = ci >> 2, c = ci & 3;
-              const uint4 raw = *reinterpret_cast<const uint4 *>(rs + ci * 16);
+            for (int c = 0; c < 4; ++c) {
+              const uint4 raw = *reinterpret_cast<const uint4 *>(rs + ((c ^ sw) << 4));
               const uint32_t wd[4] = {raw.x, raw.y, raw.z, raw.w};
-              uint32_t b[8];
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
-                b[2 * q] = e4m3x2_to_f16x2(wd[q], scl[half]);
-                b[2 * q + 1] = e4m3x2_to_f16x2(wd[q] >> 16, scl[half]);
+                w[8 * c + 2 * q] = e4m3x2_to_f16x2(wd[q], scl[half]);
+                w[8 * c + 2 * q + 1] = e4m3x2_to_f16x2(wd[q] >> 16, scl[half]);
               }
-              const int sw = row & 7;
-              *reinterpret_cast<uint4 *>(rd + row * 128 + (((2 * c) ^ sw) << 4)) =
-                  make_uint4(b[0], b[1], b[2], b[3]);
-              *reinterpret_cast<uint4 *>(rd + row * 128 + (((2 * c + 1) ^ sw) << 4)) =
-                  make_uint4(b[4], b[5], b[6], b[7]);
             }
+            tmem_st32(lane_base + s2 * kF8AStageCols + half * (kF8AStageCols / 2), w);
           }
-          fence_proxy_async_shared();  // generic stores, read by the MMA (async proxy)
+          tmem_st_wait();
+          tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&S.op_full[s2]);
           if (++s2 == (uint32_t)kOpStages) {
@@ -1143,7 +1187,7 @@ __global__ void __launch_bounds__(kFp8 ? kDThreads8 : kDThreads, 1)
   __syncthreads();
   if (warp == 5) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kDTmemCols);
+    tmem_dealloc(tmem_base, kFp8 ? kDTmemColsF8 : kDTmemCols);
   }
 }
 

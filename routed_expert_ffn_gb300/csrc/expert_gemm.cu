@@ -92,14 +92,17 @@ bool encode_bf16_map(CUtensorMap *m, const void *base, int rank, const cuuint64_
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Byte tensor map (E4M3 codes), no swizzle: rows of a box land densely.
+// Byte tensor map (E4M3 codes) with 64-byte swizzle: in the 64-byte rows of
+// a box, the 16-byte chunk c of row r lands at chunk c ^ ((r >> 1) & 3)
+// (address bits 4-5 XOR bits 7-8), so a warp reading chunk c of 32
+// consecutive rows, one row per thread, touches every bank once per phase.
 static bool encode_u8_map(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims,
                           const cuuint64_t *strides, const cuuint32_t *box) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void *>(base), dims,
-            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -746,7 +749,7 @@ bool act_map(CUtensorMap *m, const void *a, int K, int64_t R, int box_rows, int 
 }
 
 // E4M3 weights [E][P][rows][K] (one byte per weight) as {64, rows, P, K/64,
-// E}: a box [kStageKB][P][box_rows][64 bytes], unswizzled.
+// E}: a box [kStageKB][P][box_rows][64 bytes], 64-byte swizzled.
 bool weight_map_u8(CUtensorMap *m, const void *w, int K, int rows, int P, int E, int box_rows) {
   const cuuint64_t dims[5] = {(cuuint64_t)kBK, (cuuint64_t)rows, (cuuint64_t)P,
                               (cuuint64_t)(K / kBK), (cuuint64_t)E};
