@@ -58,7 +58,7 @@ def parse():
                    help="--sweep: keep batch sizes up to this many tokens (default: all)")
     p.add_argument("--weights", default="bf16", choices=["bf16", "fp8"],
                    help="expert weight format: bf16, or E4M3 codes with a power-of-two scale "
-                        "per 128x128 block (moe_layer_forward_fp8, T <= 16)")
+                        "per 128x128 block (moe_layer_forward_fp8)")
     p.add_argument("--capacity-factor", type=float, default=0.0,
                    help="time moe_layer_forward_capacity with C = ceil(cf * T * k / E) "
                         "(0: the dropless layer)")
@@ -500,11 +500,17 @@ def layer_line(cfg, T, args, world, tm, pk, sampler):
     stage_us = tm["stage_us"]
     # the persistent decode layer is one kernel (its stage events all fall at
     # its end): its roofline is the whole layer's
-    persistent = (uses_persistent(cfg, T, args.path) and not tm["capacity"]) or fp8
-    whole = persistent or tm["capacity"] > 0
+    # FP8 weights: the persistent layer up to 16 tokens, else the kernel chain
+    # with FP8 GEMMs (no stage events either way: the whole layer is timed)
+    fp8_chain = fp8 and not (T <= DECODE_MAX_T and cfg.H >= 256)
+    persistent = ((uses_persistent(cfg, T, args.path) and not tm["capacity"]) or
+                  (fp8 and not fp8_chain))
+    whole = persistent or tm["capacity"] > 0 or fp8_chain
     if whole:
-        kern = ("persistent decode layer (router, dispatch, tcgen05 GEMMs, combine)"
-                if persistent else "capacity-limited layer forward (kernel chain)")
+        kern = ("persistent decode layer (router, dispatch, tcgen05 GEMMs, combine)" if persistent
+                else "FP8-weight layer forward (kernel chain: route, dispatch, fp16 gather, FP8 "
+                     "GEMMs with the weight operand in TMEM, combine)" if fp8_chain
+                else "capacity-limited layer forward (kernel chain)")
         kern_bytes, kern_us = alg["layer_bytes"], stage_us["route"]
     else:
         kern = "expert gate/up GEMM + SwiGLU (tcgen05)"
@@ -536,7 +542,8 @@ def layer_line(cfg, T, args, world, tm, pk, sampler):
                      "algorithmic_bytes": kern_bytes, "launch_us": kern_us,
                      "peak_source": pk["source"]},
         "path": "persistent" if persistent else "chain",
-        "gemm_tiles": pair_tiles(cfg, T, getattr(args, "path", "auto")),
+        "gemm_tiles": ({"gateup": "fp8, weight operand in TMEM", "down": "fp8, weight operand in TMEM"}
+                       if fp8 else pair_tiles(cfg, T, getattr(args, "path", "auto"))),
         "layer_roofline": {"bound": "hbm" if layer_t_hbm >= layer_t_tc else "tensor",
                            "roof_us": layer_roof * 1e6, "step_us": step_s * 1e6,
                            "frac": layer_roof / step_s, "bytes": alg["layer_bytes"],

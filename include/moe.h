@@ -385,11 +385,15 @@ moe_status_t moe_quantize_fp8(const void *w, int32_t n, int32_t rows, int32_t K,
 
 /*
  * moe_layer_forward_fp8 -- the layer forward (Moebius reading notes eq. (1))
- * with FP8 expert weights (moe_layer_weights_fp8_t), for decode batches: the
- * persistent single-kernel layer of moe_layer_forward_ex, its weight copies
- * streaming E4M3 codes that converter warps turn into bf16 operand tiles
- * (times the block scale) for the tensor cores.  Shapes: T <= 16 and
- * H >= 256 (MOE_ERR_UNSUPPORTED_SHAPE otherwise); other arguments as
+ * with FP8 expert weights (moe_layer_weights_fp8_t).  The weight copies
+ * stream E4M3 codes; converter warps turn them into fp16 values (times the
+ * block scale, exact in fp16) and store them into TMEM, where the tensor
+ * cores read the weight operand; the token rows are fp16 (x converted on the
+ * way into x_perm, h written in fp16).  Decode batches (T <= 16, H >= 256)
+ * run the persistent single-kernel layer of moe_layer_forward_ex; larger
+ * batches the kernel chain (route, dispatch, fp16 gather, FP8 gate/up and
+ * down GEMMs, combine).  An h or gate-weighted value beyond fp16's range is
+ * saturated and latches MOE_ERR_DEVICE_CHECK.  Other arguments as
  * moe_layer_forward.
  */
 moe_status_t moe_layer_forward_fp8(const moe_layer_desc_t *d, const moe_layer_weights_fp8_t *w,

@@ -341,7 +341,8 @@ def layer_weights_fp8(w_router, q: Dict, sel_bias=None) -> LayerWeightsFp8:
 
 
 def moe_layer_forward_fp8(d: LayerDesc, w: LayerWeightsFp8, x, y, ws, stream=None):
-    """Layer forward with FP8 expert weights (decode batches, T <= 16)."""
+    """Layer forward with FP8 expert weights: the persistent decode layer up to
+    16 tokens, else the kernel chain with FP8 GEMMs on fp16 token rows."""
     _check("moe_layer_forward_fp8", library().moe_layer_forward_fp8(
         ctypes.byref(d), ctypes.byref(w), _ptr(x), _ptr(y), _ptr(ws), _nbytes(ws),
         _stream(stream)))

@@ -494,10 +494,43 @@ moe_status_t moe_layer_forward_fp8(const moe_layer_desc_t *d, const moe_layer_we
   if (d->has_shared_expert && (!ok_ptr(w->w13_shared) || !ok_ptr(w->w2_shared) ||
                                w->w13_shared_scale == nullptr || w->w2_shared_scale == nullptr))
     return MOE_ERR_INVALID_ARG;
-  if (!decode_layer_supported(*d)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if ((st = check_device()) != MOE_OK) return st;
-  return cuda_status(
-      launch_decode_layer_fp8(*d, *w, bf(x), bfw(y), workspace, L, (cudaStream_t)stream));
+  cudaStream_t s = (cudaStream_t)stream;
+  if (decode_layer_supported(*d))
+    return cuda_status(launch_decode_layer_fp8(*d, *w, bf(x), bfw(y), workspace, L, s));
+  // larger batches: the kernel chain with FP8 GEMMs on fp16 token rows
+  uint32_t *status = at<uint32_t>(workspace, L.status);
+  int32_t *ids = at<int32_t>(workspace, L.topk_ids);
+  float *tw = at<float>(workspace, L.topk_w);
+  int32_t *offsets = at<int32_t>(workspace, L.offsets);
+  int32_t *perm_src = at<int32_t>(workspace, L.perm_src);
+  int32_t *inv_pos = at<int32_t>(workspace, L.inv_pos);
+  float *w_perm = at<float>(workspace, L.w_perm);
+  int32_t *plan = at<int32_t>(workspace, L.plan);
+  __nv_bfloat16 *x_perm = at<__nv_bfloat16>(workspace, L.x_perm);  // fp16 rows in this mode
+  __nv_bfloat16 *h = at<__nv_bfloat16>(workspace, L.h);            // fp16 rows in this mode
+  __half *out_perm = at<__half>(workspace, L.out_perm);
+  cudaError_t e = route(*d, L, bf(x), w->w_router, w->sel_bias, at<float>(workspace, L.logits), ids,
+                        tw, at<float>(workspace, L.gap), workspace, s);
+  if (e == cudaSuccess)
+    e = launch_dispatch(ids, tw, d->T, d->k, d->E, at<int32_t>(workspace, L.blk_counts),
+                        at<int32_t>(workspace, L.blk_base), at<int32_t>(workspace, L.counts),
+                        offsets, perm_src, inv_pos, w_perm, status, plan, d->H, d->I,
+                        d->has_shared_expert, s);
+  if (e == cudaSuccess)
+    e = launch_gather_plan(bf(x), perm_src,
+                           (int64_t)d->T * d->H * 2 > kGatherByTokenBytes ? inv_pos : nullptr,
+                           offsets, d->T, d->k, d->E, d->H, d->I, d->has_shared_expert, x_perm, h,
+                           nullptr, status, s, /*to_fp16=*/true);
+  if (e == cudaSuccess)
+    e = launch_expert_gemm_fp8(true, *d, w->w13, w->w13_scale, w->w13_shared, w->w13_shared_scale,
+                               x_perm, plan, nullptr, h, status, s);
+  if (e == cudaSuccess)
+    e = launch_expert_gemm_fp8(false, *d, w->w2, w->w2_scale, w->w2_shared, w->w2_shared_scale, h,
+                               plan, w_perm, out_perm, status, s);
+  if (e == cudaSuccess)
+    e = launch_combine(out_perm, inv_pos, nullptr, d->T, d->k, d->H, d->has_shared_expert, bfw(y), s);
+  return cuda_status(e);
 }
 
 moe_status_t moe_check_bounded_grid_wait(void *workspace, size_t ws_bytes, moe_stream_t stream) {

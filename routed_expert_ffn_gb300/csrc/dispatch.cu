@@ -114,8 +114,23 @@ __global__ void __launch_bounds__(kDispatchThreads)
   (void)lane;
 }
 
+// Eight bf16 values to eight fp16 values (round to nearest even; exact for
+// |x| in fp16's normal range, which covers the layers' activations).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 h2 = __floats2half2_rn(__uint_as_float(w[i] << 16),
+                                         __uint_as_float(w[i] & 0xffff0000u));
+    o[i] = *reinterpret_cast<const uint32_t *>(&h2);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // Rows [0, Na): x_perm[p] = x[perm_src[p] / k]; rows [Na, Na+T) (shared
-// expert): x_perm[Na+t] = x[t].  16-byte vectors.  With inv_pos (the layer
+// expert): x_perm[Na+t] = x[t].  16-byte vectors (to_fp16: converted to
+// fp16, the token operand of the FP8-weight GEMMs).  With inv_pos (the layer
 // forward) one warp per token reads its row of x once and writes it to the
 // token's k positions (and its shared-expert row), so x is read once even
 // when it does not fit in L2; without (the standalone FFN call) one warp per
@@ -127,7 +142,7 @@ __global__ void __launch_bounds__(256)
                        int T, int k, int E, int H, int I, int shared,
                        __nv_bfloat16 *__restrict__ x_perm, __nv_bfloat16 *__restrict__ h,
                        int32_t *__restrict__ plan, int with_plan, int num_sms,
-                       uint32_t *__restrict__ status) {
+                       uint32_t *__restrict__ status, int to_fp16) {
   pdl_wait();
   pdl_launch_dependents();
   const int64_t Na = (int64_t)T * k;
@@ -173,6 +188,10 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
       for (int i = 0; i < kBatch; ++i)
         if (v0 + 32 * i < nv) r[i] = src[v0 + 32 * i];
+      if (to_fp16) {
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) r[i] = bf16x8_to_f16x8(r[i]);
+      }
       for (int j = 0; j <= k; ++j) {
         int64_t row;
         if (j < k) {
@@ -213,7 +232,7 @@ __global__ void __launch_bounds__(256)
       if (v0 + 32 * i < nv) r[i] = s[v0 + 32 * i];
 #pragma unroll
     for (int i = 0; i < kBatch; ++i)
-      if (v0 + 32 * i < nv) dst[v0 + 32 * i] = r[i];
+      if (v0 + 32 * i < nv) dst[v0 + 32 * i] = to_fp16 ? bf16x8_to_f16x8(r[i]) : r[i];
   }
 }
 
@@ -356,14 +375,15 @@ cudaError_t launch_dispatch(const int32_t *ids, const float *topk_w, int T, int 
 cudaError_t launch_gather_plan(const __nv_bfloat16 *x, const int32_t *perm_src,
                                const int32_t *inv_pos, const int32_t *offsets, int T, int k, int E,
                                int H, int I, int shared, __nv_bfloat16 *x_perm, __nv_bfloat16 *h,
-                               int32_t *plan, uint32_t *status, cudaStream_t s) {
+                               int32_t *plan, uint32_t *status, cudaStream_t s, bool to_fp16) {
   // eight warps per block: one per token (with inv_pos) or per x_perm row;
   // one more block writes the tile plan when `plan` is given
   const int64_t units = inv_pos != nullptr ? (int64_t)T : (int64_t)T * k + (shared ? T : 0);
   const int with_plan = plan != nullptr ? 1 : 0;
   const int blocks = (int)((units + 7) / 8) + with_plan;
   return launch_pdl(gather_plan_kernel, dim3(blocks), dim3(256), 0, s, x, perm_src, inv_pos,
-                    offsets, T, k, E, H, I, shared, x_perm, h, plan, with_plan, num_sms(), status);
+                    offsets, T, k, E, H, I, shared, x_perm, h, plan, with_plan, num_sms(), status,
+                    to_fp16 ? 1 : 0);
 }
 
 }  // namespace moe

@@ -209,10 +209,12 @@ cudaError_t launch_dispatch(const int32_t *ids, const float *topk_w, int T, int 
 constexpr int64_t kGatherByTokenBytes = (int64_t)MOE_GATHER_TOKEN_KB << 10;
 // h: the first 256 rows past the last segment (if the segments end before
 // T*k) are zeroed.
+// to_fp16: x_perm rows in fp16 (the token operand of the FP8-weight GEMMs)
 cudaError_t launch_gather_plan(const __nv_bfloat16 *x, const int32_t *perm_src,
                                const int32_t *inv_pos, const int32_t *offsets, int T, int k, int E,
                                int H, int I, int shared, __nv_bfloat16 *x_perm, __nv_bfloat16 *h,
-                               int32_t *plan, uint32_t *status, cudaStream_t s);
+                               int32_t *plan, uint32_t *status, cudaStream_t s,
+                               bool to_fp16 = false);
 // split_part: kMaxSplitTiles x 2 x kBM x kSplitMaxRows fp32; split_cnt: the
 // GEMM's kMaxSplitTiles arrival counters (in the workspace status block).
 // plan_early: the plan was written before the kernel preceding the GEMM
@@ -232,6 +234,14 @@ cudaError_t launch_expert_down(const moe_layer_desc_t &d, const void *w2, const 
 struct TokenMaps {
   CUtensorMap m[16];
 };
+// The expert GEMMs with FP8 (E4M3) weights and per-128x128-block exponents
+// (w_scale, as moe_layer_weights_fp8_t lays them out) for the kernel chain:
+// act = fp16 token rows [R][K] (x_perm or h), out = fp16 h or out_perm.
+cudaError_t launch_expert_gemm_fp8(bool gate_up, const moe_layer_desc_t &d, const void *w,
+                                   const int8_t *w_scale, const void *w_sh,
+                                   const int8_t *w_sh_scale, const void *act,
+                                   const int32_t *plan, const float *w_perm, void *out,
+                                   uint32_t *status, cudaStream_t s);
 // The expert GEMMs on CTA pairs (tcgen05.mma.cta_group::2): shapes it takes
 // (K a whole number of stages, output columns a whole number of pair tiles,
 // enough rows per expert: gate/up T*k >= 256*E, down 64*E when I >= 2048),

@@ -1,9 +1,10 @@
 """FP8 expert weights (needs a GB300): the quantiser (moe_quantize_fp8) bit
 for bit against the oracle's, and the FP8 layer (moe_layer_forward_fp8: the
-persistent decode layer streaming E4M3 codes) against the oracle's fp64 layer
-over its own dequantised weights, on every layer configuration at decode
-sizes.  The oracle quantises the weights itself; the GPU's codes and block
-exponents must equal its bytes, so both sides run the same FP8 layer."""
+persistent decode layer up to 16 tokens, the kernel chain with FP8 GEMMs
+above) against the oracle's fp64 layer over its own dequantised weights, on
+every layer configuration at decode and larger batch sizes.  The oracle
+quantises the weights itself; the GPU's codes and block exponents must equal
+its bytes, so both sides run the same FP8 layer."""
 
 import numpy as np
 import pytest
@@ -13,7 +14,7 @@ import oracle
 import routed_expert_ffn_gb300 as moe
 import synth
 from gpu_check import (LayerRun, assert_output_close, bf16_np, check_routing, host_copy,
-                       rel_l2)
+                       rel_l2, sample_tokens)
 from test_gpu_layer import layer_inputs
 
 pytestmark = pytest.mark.gpu
@@ -58,7 +59,7 @@ def _oracle_expert(w13_e, w2_e):
     return d13, d2, (q13, s13, q2, s2)
 
 
-def check_fp8_layer(inputs):
+def check_fp8_layer(inputs, n_sample=None):
     cfg, T = inputs.cfg, inputs.T
     E, k, I, H = cfg.E, cfg.k, cfg.I, cfg.H
     q = moe.quantize_layer_fp8(inputs.w13, inputs.w2, inputs.w13_shared, inputs.w2_shared)
@@ -77,7 +78,14 @@ def check_fp8_layer(inputs):
                   cfg.gating, bias, label=f"{cfg.name} T={T} fp8")
     rc, ro, rp, ri = oracle.dispatch(meta["ids"], E)
     assert np.array_equal(meta["counts"], rc) and np.array_equal(meta["perm_src"], rp)
-    toks = [t for t in range(T) if not (gap[t] < 1e-5)]
+    if n_sample is None or T <= n_sample:
+        toks = list(range(T))
+    else:
+        # tile edges of the hottest experts and of the shared expert, the
+        # coldest touched expert, seeded random tokens
+        toks = sample_tokens(T, n_sample, meta["ids"], rc, perm_src=meta["perm_src"],
+                             offsets=meta["offsets"], shared=bool(cfg.shared))
+    toks = [t for t in toks if not (gap[t] < 1e-5)]
     need = sorted({int(e) for t in toks for e in ids[t]})
     host = host_copy(inputs, experts=need)
     d13, d2 = {}, {}
@@ -111,11 +119,13 @@ def test_fp8_layer_matches_oracle(name, T):
     assert q_err < 0.06
 
 
-def test_fp8_rejects_prefill_batches():
-    inp = layer_inputs("qwen3", 17)
-    q = moe.quantize_layer_fp8(inp.w13, inp.w2)
-    run = LayerRun(inp)
-    with pytest.raises(moe.MoeError) as ei:
-        moe.moe_layer_forward_fp8(run.d, moe.layer_weights_fp8(inp.w_router, q), inp.x, run.y,
-                                  run.ws)
-    assert ei.value.status == moe.MOE_ERR_UNSUPPORTED_SHAPE
+@pytest.mark.parametrize("name,T,n", [("tiny", 17, None), ("tiny", 64, None), ("mixtral", 33, None),
+                                      ("qwen3", 128, 128), ("qwen3_tp8", 256, 128), ("dsv3", 32, None),
+                                      ("qwen3", 1024, 96), ("mixtral", 512, 64)])
+def test_fp8_chain_matches_oracle(name, T, n):
+    """Batches above 16 tokens: the kernel chain with the FP8 GEMMs (fp16 token
+    rows, the weight operand in TMEM), against the oracle over the same
+    dequantised weights; every token up to n (sampled above, tile edges of the
+    hottest and shared experts included)."""
+    q_err = check_fp8_layer(layer_inputs(name, T), n_sample=n)
+    assert q_err < 0.06
