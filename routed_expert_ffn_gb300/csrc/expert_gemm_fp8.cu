@@ -23,7 +23,7 @@
 // codes through L2); CTA c walks tiles c, c + grid, ...  A K step is two K
 // blocks (one staged unit); a K range that ends inside a unit reads zeros.
 //
-// CTA = 10 warps:
+// CTA = 6 warps + the converters:
 //   warp 4 lane 0  TMA: each unit's codes (2 K blocks x 2 halves x 128 rows
 //                  x 64 bytes) into the four 32 KB staging stages;
 //   warp 4 lane 1  TMA: each K block's token rows into one of four operand
@@ -31,7 +31,8 @@
 //   warp 5         TMEM (512 columns: one accumulator buffer of 2 x 128
 //                  columns, four operand stages of 2 x 32); one thread
 //                  issues the MMAs;
-//   warps 6-9      converters, warp w writing the TMEM lanes of quarter w % 4;
+//   warps 6-       converters (kFConvSets sets of four), warp w writing the
+//                  TMEM lanes of quarter w % 4;
 //   warps 0-3      epilogue: SiLU(gate)*up into h, or the gate weighting into
 //                  out_perm, both fp16 (saturating at +-65504, which latches
 //                  the status word's range bit), then the tile's rows.
@@ -48,7 +49,12 @@ namespace moe {
 
 namespace {
 
-constexpr int kFThreads = 320;
+// converter sets: each set of four warps converts every kFConvSets-th K block
+// of a staged unit (measured with two sets: 0.5-1% slower at every shape;
+// building each code's fp16 bits with integer operations instead of the
+// conversion instruction: 26-50% slower)
+constexpr int kFConvSets = 1;
+constexpr int kFThreads = (6 + 4 * kFConvSets) * 32;
 constexpr int kFRows = 128;                           // token rows per tile
 constexpr uint32_t kFStage = 2 * 2 * kBM * kBK;       // 32 KB of codes per unit
 constexpr int kFStages = 4;
@@ -65,6 +71,8 @@ constexpr uint32_t kFAStageCols = 2 * kBK / 2;        // two halves x 32 columns
 constexpr uint32_t kFTmemCols = 512;
 static_assert(kFACol + kFOpStages * kFAStageCols <= kFTmemCols, "TMEM budget");
 static_assert(kStageKB == 2, "a unit is two K blocks");
+static_assert(kStageKB % kFConvSets == 0 && kFOpStages % kFConvSets == 0,
+              "each converter set owns every kFConvSets-th operand stage");
 
 constexpr size_t fp8_smem_bytes(int nseg) {
   return 1024 + (size_t)kFStages * kFStage + (size_t)kFOpStages * kFOpStage +
@@ -192,7 +200,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kFStages; ++i) {
       mbar_init(&st_full[i], 1);   // the producer's expected bytes
-      mbar_init(&st_empty[i], 4);  // the four converter warps
+      mbar_init(&st_empty[i], 4 * kFConvSets);  // every converter warp
     }
     for (int i = 0; i < kFOpStages; ++i) {
       mbar_init(&op_full[i], 5);   // token-row copy + four converter warps
@@ -358,10 +366,11 @@ __global__ void __launch_bounds__(kFThreads, 1)
     // codes are four 16-byte chunks read through the 64-byte swizzle (the
     // warp's 32 rows touch every bank once per phase).
     const int quarter = warp & 3;
+    const int cset = (warp - 6) >> 2;   // this warp's converter set
     const int r = quarter * 32 + lane;  // weight row of a half
     const int sw = (r >> 1) & 3;
     const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16) + kFACol;
-    uint32_t s1 = 0, p1 = 0, s2 = 0, p2 = 0;
+    uint32_t s1 = 0, p1 = 0, s2 = (uint32_t)cset, p2 = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
       const FTile t = fp8_tile(tile, seg_row, tp, nseg);
@@ -388,7 +397,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
           break;
         }
         const uint8_t *src = stg + s1 * kFStage;
-        for (int hk = 0; hk < kStageKB; ++hk) {
+        for (int hk = cset; hk < kStageKB; hk += kFConvSets) {
           if (!mbar_wait(&op_empty[s2], p2 ^ 1u, abort_flag, status, kCode)) {
             ok = false;
             break;
@@ -414,8 +423,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&op_full[s2]);
-          if (++s2 == (uint32_t)kFOpStages) {
-            s2 = 0;
+          s2 += kFConvSets;
+          if (s2 >= (uint32_t)kFOpStages) {
+            s2 -= kFOpStages;
             p2 ^= 1u;
           }
         }
