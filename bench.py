@@ -42,7 +42,10 @@ def parse():
                    help="override the number of experts (reduced cases for profiler captures)")
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-tokens", type=int, default=48)
+    p.add_argument("--cpu-tokens", type=int, default=0,
+                   help="tokens of the oracle's timed sample (0: sized from a short probe "
+                        "to about 15 s of CPU work for the cpu_baseline, about 90 s over all "
+                        "steps of --impl reference)")
     p.add_argument("--op", default="layer", choices=["layer", "reshard"],
                    help="layer: the MoE layer forward (default); reshard: the EP<->TP "
                         "expert-weight permute of one rank's experts")
@@ -320,9 +323,11 @@ def run_reference(args):
         inp = host_inputs(cfg, T, args.seed, experts_from_gpu=gen)
     else:
         inp = host_inputs(cfg, T, args.seed)
-    n = min(args.cpu_tokens, T)
-    for _ in range(max(0, min(args.warmup, 1))):
-        cpu_oracle_sample(inp, max(1, n // 8), seed=99)
+    # a short probe of the oracle's rate sizes the per-step sample (about 90 s
+    # over all steps) unless --cpu-tokens fixes it
+    k0, dt0, _ = cpu_oracle_sample(inp, min(16, T), seed=99)
+    n = args.cpu_tokens if args.cpu_tokens > 0 else int(max(16, 90.0 * k0 / dt0 / max(1, args.steps)))
+    n = min(n, T)
     total_tok, total_s, threads = 0, 0.0, 1
     for step in range(args.steps):
         k, dt, threads = cpu_oracle_sample(inp, n, seed=step)
@@ -666,7 +671,10 @@ def run_gpu(args):
     if not args.no_cpu_baseline:
         hin = (host_inputs(cfg, T, args.seed) if args.weights == "fp8"
                else host_inputs(cfg, T, args.seed, experts_from_gpu=inp))
-        n, dt, threads = cpu_oracle_sample(hin, args.cpu_tokens)
+        # the sample: about 15 s of oracle work (a short probe gives the rate)
+        k0, dt0, _ = cpu_oracle_sample(hin, min(16, T), seed=7)
+        want = args.cpu_tokens if args.cpu_tokens > 0 else int(max(48, 15.0 * k0 / dt0))
+        n, dt, threads = cpu_oracle_sample(hin, min(want, T))
         line["cpu_baseline"] = {"value": n / dt, "unit": "tokens/s", "cores": threads,
                                 "kind": "oracle", "cpu_model": cpu_model(),
                                 "sample": f"{n} seeded tokens of the T={T} batch (routing + "
