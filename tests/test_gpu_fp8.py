@@ -129,3 +129,52 @@ def test_fp8_chain_matches_oracle(name, T, n):
     hottest and shared experts included)."""
     q_err = check_fp8_layer(layer_inputs(name, T), n_sample=n)
     assert q_err < 0.06
+
+
+@pytest.mark.parametrize("T", [4, 48])
+def test_fp8_values_past_fp16_range_saturate_and_flag(T):
+    """h (fp16 in the FP8 layer) beyond +-65504: saturated, never inf, and the
+    status word reports a device check (range bit) -- the persistent layer
+    (T = 4) and the kernel chain (T = 48)."""
+    cfg = synth.LayerConfig("ovf", H=256, E=4, k=2, I=256, gating=synth.GATE_TOPK_SOFTMAX)
+    inp = synth.make_layer(cfg, T, 9, device="cuda")
+    x = (inp.x.float() * 4000.0).to(torch.bfloat16)
+    q = moe.quantize_layer_fp8(inp.w13, inp.w2)
+    run = LayerRun(inp)
+    moe.moe_layer_forward_fp8(run.d, moe.layer_weights_fp8(inp.w_router, q), x, run.y, run.ws)
+    torch.cuda.synchronize()
+    st, raw = moe.moe_get_device_status(run.ws)
+    assert st == moe.MOE_ERR_DEVICE_CHECK and raw & (1 << 5), (st, raw)
+    assert torch.isfinite(run.y.float()).all()
+
+
+@pytest.mark.parametrize("name,T", [("qwen3", 8), ("mixtral", 64)])
+def test_fp8_forward_replays_from_a_cuda_graph(name, T):
+    """The FP8 forward (the persistent layer's cooperative launch, or the
+    chain) captures into a CUDA graph; replays give the eager result bit for
+    bit."""
+    inp = layer_inputs(name, T)
+    q = moe.quantize_layer_fp8(inp.w13, inp.w2, inp.w13_shared, inp.w2_shared)
+    wq = moe.layer_weights_fp8(inp.w_router, q, inp.sel_bias)
+    run = LayerRun(inp)
+    moe.moe_layer_forward_fp8(run.d, wq, inp.x, run.y, run.ws)
+    torch.cuda.synchronize()
+    y_eager = run.y.clone()
+    y = torch.empty_like(y_eager)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        moe.moe_layer_forward_fp8(run.d, wq, inp.x, y, run.ws, stream=s)  # warm-up on s
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        moe.moe_layer_forward_fp8(run.d, wq, inp.x, y, run.ws, stream=s)
+    for _ in range(2):
+        y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y, y_eager)
+    st, raw = moe.moe_get_device_status(run.ws)
+    assert st == moe.MOE_OK, raw
+    del g
