@@ -120,11 +120,19 @@ struct DecodeArgs {
 };
 
 // The two regions of work (all gate/up tiles, then all down tiles), each cut
-// into Geff[r] equal contiguous unit ranges, one per CTA: every CTA streams
-// its share of the gate/up weights, then its share of the down weights.
+// into Geff[r] equal contiguous ranges of granules, one per CTA: every CTA
+// streams its share of the gate/up weights, then its share of the down
+// weights.  A granule is one unit (a K step), or a whole tile where tiles
+// have at most kDWholeTileUnits units: a tile split between CTAs costs a
+// partial store, a release and the finishing CTA's wait, about as much as
+// such a short tile itself (measured against unit granules: the TP-8 slice's
+// down tiles, K = 192, at T=1 37.7 -> 35.4 us and T=4 63.5 -> 61.4 us; the
+// tiny layer at T=16 32.1 -> 26.9 us; no change where tiles are longer).
+constexpr int kDWholeTileUnits = 4;
 struct Sched {
   int J[2], Uper[2], nt;  // tiles per segment, units per tile
   int U[2], Geff[2];      // units of the region (< 2^24), CTAs that share it
+  int gran[2];            // units per granule
   int start[2], end[2];   // this CTA's unit range in each region
 };
 
@@ -193,10 +201,11 @@ __device__ __forceinline__ bool next_piece(const Sched &sc, const int32_t *seg_l
   return false;
 }
 
-// The CTA whose range of region r holds unit x: the largest c with
-// floor(c * U / Geff) <= x.
+// The CTA whose range of region r holds unit x: with N = U / gran granules,
+// the largest c with floor(c * N / Geff) <= x / gran.
 __device__ __forceinline__ int cta_of(const Sched &sc, int r, int x) {
-  return (int)((((int64_t)x + 1) * sc.Geff[r] + sc.U[r] - 1) / sc.U[r] - 1);
+  const int64_t n = sc.U[r] / sc.gran[r], xg = x / sc.gran[r];
+  return (int)(((xg + 1) * sc.Geff[r] + n - 1) / n - 1);
 }
 
 // Grid barrier over the CTAs of the (cooperative) launch, used once per
@@ -598,10 +607,12 @@ __global__ void __launch_bounds__(kFp8 ? kDThreads8 : kDThreads, 1)
     w.nt = ok ? S.ntouched : 0;
     for (int r = 0; r < 2; ++r) {
       w.U[r] = w.nt * w.J[r] * w.Uper[r];
-      w.Geff[r] = min((int)G, w.U[r]);
+      w.gran[r] = w.Uper[r] <= kDWholeTileUnits ? w.Uper[r] : 1;
+      const int n = w.U[r] / w.gran[r];  // granules of the region
+      w.Geff[r] = min((int)G, n);
       if ((int)blockIdx.x < w.Geff[r]) {
-        w.start[r] = (int)((int64_t)blockIdx.x * w.U[r] / w.Geff[r]);
-        w.end[r] = (int)(((int64_t)blockIdx.x + 1) * w.U[r] / w.Geff[r]);
+        w.start[r] = (int)((int64_t)blockIdx.x * n / w.Geff[r]) * w.gran[r];
+        w.end[r] = (int)(((int64_t)blockIdx.x + 1) * n / w.Geff[r]) * w.gran[r];
       } else {
         w.start[r] = w.end[r] = w.U[r];
       }
