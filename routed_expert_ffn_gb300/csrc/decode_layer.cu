@@ -33,14 +33,16 @@
 //                  out_perm.  The K steps of all tiles (gate/up first, then
 //                  down) are cut into G equal contiguous ranges, one per CTA
 //                  ("stream-K"), so every SM streams the same weight bytes;
-//                  a tile shared by several CTAs is finished by the last of
-//                  them to arrive, which adds the fp32 partials in CTA order.
+//                  a tile shared by several CTAs is finished by the one
+//                  holding its first K steps (it reaches the tile last),
+//                  which adds the others' fp32 partials in CTA order.
 //                  A down tile of expert e waits (bounded) until every
 //                  gate/up tile of e has written its h rows; its weight
 //                  copies are issued before that wait.
 //      grid barrier
 //   D  combine     y[t] = sum_j out_perm[inv_pos[t, j]] (+ the shared
-//                  expert's row), fp32 in slot order, rounded once.
+//                  expert's row), fp32 in slot order, rounded once, spread
+//                  over every thread of the grid.
 //
 // Every wait (grid barrier, expert readiness, pipeline barriers) gives up
 // after kWaitLimitNs, latches kStatusTimeoutLayer in the status word and lets
@@ -148,8 +150,6 @@ struct DSmem {
   int32_t seg_list[kMaxE + 1];  // segments with rows, in order (shared expert last)
   float red[kDMaxWarps][kDecodeMaxT];
   int ntouched, last_flag, ok_flag;
-  int done_tok[kDecodeMaxT];  // tokens whose combine this CTA runs next
-  int ndone;
   uint64_t full[kDStages], empty[kDStages], tfull[2], tempty[2], fin;
   uint64_t st_full[kF8Stages], st_empty[kF8Stages], op_full[kOpStages], op_empty[kOpStages];
   uint64_t rbar;  // router staging copies
@@ -208,10 +208,10 @@ __device__ __forceinline__ int cta_of(const Sched &sc, int r, int x) {
   return (int)(((xg + 1) * sc.Geff[r] + n - 1) / n - 1);
 }
 
-// Grid barrier over the CTAs of the (cooperative) launch, used once per
-// launch: every CTA adds 1 to a counter with a release reduction (no reply
-// awaited) and polls it until it reaches `nblocks`; the last CTA to finish
-// the kernel clears it.  Bounded: gives up after kWaitLimitNs, or at once when
+// Grid barrier over the CTAs of the (cooperative) launch, each of the two
+// per launch on its own counter: every CTA adds 1 to it with a release
+// reduction (no reply awaited) and polls it until it reaches `nblocks`; the
+// last CTA to finish the kernel clears it.  Bounded: gives up after kWaitLimitNs, or at once when
 // another CTA has latched a timeout, and then latches kStatusTimeoutLayer.
 // Called by all threads.
 __device__ bool grid_sync(uint32_t *bar, uint32_t nblocks, uint32_t *status, int *s_ok) {
@@ -278,6 +278,45 @@ __device__ __forceinline__ bool epi_all_d(bool p) {
 __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// y[t, col..col+8) = sum_j out_perm[inv[t*k + j], col..col+8) (+ the
+// shared expert's row Na + t when nrow = k + 1), fp32 in slot order, rounded
+// once to bf16; eight rows' loads in flight.
+__device__ __forceinline__ void combine_vec(const DecodeArgs &a, const int32_t *inv, int k,
+                                            int nrow, int Na, int H, int t, int col) {
+  float acc[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+  for (int j0 = 0; j0 < nrow; j0 += 8) {
+    uint4 raw[8];
+#pragma unroll
+    for (int z = 0; z < 8; ++z) {
+      const int jj = j0 + z;
+      if (jj < nrow) {
+        const int pos = jj < k ? inv[t * k + jj] : Na + t;
+        raw[z] = __ldcg(reinterpret_cast<const uint4 *>(a.out_perm + (size_t)pos * H + col));
+      }
+    }
+#pragma unroll
+    for (int z = 0; z < 8; ++z) {
+      if (j0 + z < nrow) {
+        const uint32_t wd[4] = {raw[z].x, raw[z].y, raw[z].z, raw[z].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&wd[q]));
+          acc[2 * q] += f.x;
+          acc[2 * q + 1] += f.y;
+        }
+      }
+    }
+  }
+  uint4 o;
+  o.x = bf16x2_bits(acc[0], acc[1]);
+  o.y = bf16x2_bits(acc[2], acc[3]);
+  o.z = bf16x2_bits(acc[4], acc[5]);
+  o.w = bf16x2_bits(acc[6], acc[7]);
+  *reinterpret_cast<uint4 *>(a.y + (size_t)t * H + col) = o;
 }
 
 // Four MMAs over one 64-deep K block (16 bf16 = 32 bytes per K16 step inside
@@ -379,7 +418,6 @@ __global__ void __launch_bounds__(kFp8 ? kDThreads8 : kDThreads, 1)
   uint32_t *gbar = status + kDecodeBarrierWord;
   uint32_t *piece_cnt = status + kDecodePieceWord;
   uint32_t *seg_done = status + kDecodeSegWord;
-  uint32_t *tok_cnt = status + kDecodeTokWord;  // [T][H/256] row-block arrivals
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kDStages; ++i) {
@@ -403,7 +441,6 @@ __global__ void __launch_bounds__(kFp8 ? kDThreads8 : kDThreads, 1)
       }
     }
     S.abort_flag = 0;
-    S.ndone = 0;
     fence_mbar_init();
   }
   if (warp == 5) {
@@ -1116,81 +1153,37 @@ __global__ void __launch_bounds__(kFp8 ? kDThreads8 : kDThreads, 1)
             }
           }
         }
-        // One arrival per token of the segment on the counter of (token,
-        // this tile's 256 columns); the arrival that completes one (all k
-        // routed rows, and the shared row, of those columns written) makes
-        // this CTA combine those columns of that token.  Release: the
-        // barrier orders every thread's rows before the arriving threads'
-        // fences; acquire: the completing thread's fence after its arrival.
-        epi_sync_d();
-        if (r < m) {
-          const int t = s < E ? S.perm[row0 + r] / k : r;
-          const uint32_t target = (uint32_t)(k + a.shared);
-          __threadfence();
-          if (atomicInc(tok_cnt + t * sc.J[1] + pc.j, target - 1) == target - 1) {  // wraps to 0
-            __threadfence();
-            S.done_tok[atomicAdd(&S.ndone, 1)] = t;
-          }
-        }
-        epi_sync_d();
-        // D: combine, y[t, cols] = sum_j out_perm[inv_pos[t, j], cols] (+ the
-        // shared expert's row), fp32 in slot order, rounded once: 32 vectors
-        // of 8 columns per token, eight rows' loads in flight per vector
-        const int ndone = S.ndone;
-        const int nrow = k + a.shared;
-        for (int task = r; task < ndone * 32; task += 128) {
-          const int t = S.done_tok[task >> 5];
-          const int col = pc.j * 2 * kBM + (task & 31) * 8;
-          if (col >= H) continue;
-          float acc[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) acc[q] = 0.f;
-          for (int j0 = 0; j0 < nrow; j0 += 8) {
-            uint4 raw[8];
-#pragma unroll
-            for (int z = 0; z < 8; ++z) {
-              const int jj = j0 + z;
-              if (jj < nrow) {
-                const int pos = jj < k ? S.inv[t * k + jj] : Na + t;
-                raw[z] = __ldcg(reinterpret_cast<const uint4 *>(a.out_perm + (size_t)pos * H + col));
-              }
-            }
-#pragma unroll
-            for (int z = 0; z < 8; ++z) {
-              if (j0 + z < nrow) {
-                const uint32_t wd[4] = {raw[z].x, raw[z].y, raw[z].z, raw[z].w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                  const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&wd[q]));
-                  acc[2 * q] += f.x;
-                  acc[2 * q + 1] += f.y;
-                }
-              }
-            }
-          }
-          uint4 o;
-          o.x = bf16x2_bits(acc[0], acc[1]);
-          o.y = bf16x2_bits(acc[2], acc[3]);
-          o.z = bf16x2_bits(acc[4], acc[5]);
-          o.w = bf16x2_bits(acc[6], acc[7]);
-          *reinterpret_cast<uint4 *>(a.y + (size_t)t * H + col) = o;
-        }
-        epi_sync_d();
-        if (r == 0) S.ndone = 0;
       }
     }
     if (range_bad) atomicOr(status, kStatusRange);
   }
 
-  // The last CTA to finish clears the grid barrier and the readiness
-  // counters: every CTA has passed the barrier and its last readiness check
-  // by then.
+  // ------------------------------------------------------- D: combine --
+  // Once every CTA has written its down tiles' out_perm rows (a second grid
+  // barrier), one vector of 8 columns per thread of the grid.  (Combining
+  // each block of 256 columns in the CTA whose down tile completes it, with
+  // no second barrier, left the combines of a batch on the few CTAs that
+  // finish last.)
+  if (ok) {
+    ok = grid_sync(gbar + 1, G, status, &S.ok_flag);
+    const int nvec = H / 8, nrow = k + a.shared;
+    for (int task = (int)blockIdx.x * kNT + (int)threadIdx.x; ok && task < T * nvec;
+         task += (int)G * kNT) {
+      const int t = task / nvec;
+      combine_vec(a, S.inv, k, nrow, Na, H, t, (task - t * nvec) * 8);
+    }
+  }
+
+  // The last CTA to finish clears the grid barriers and the readiness
+  // counters: every CTA has passed both barriers and its last readiness
+  // check by then.
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
     if (atomicInc(gbar + 2, G - 1) == G - 1) {  // wraps to 0
       __threadfence();
       gbar[0] = 0u;
+      gbar[1] = 0u;
       for (int i = 0; i < sc.nt; ++i) seg_done[S.seg_list[i]] = 0u;
     }
   }

@@ -147,22 +147,19 @@ constexpr int kMaxSplitTiles = 1024;
 
 // Persistent decode layer (decode_layer.cu): batches of up to kDecodeMaxT
 // tokens run the whole layer in one cooperative launch of one CTA per SM.
-// Its counters follow the split-K counters in the status block: the grid
-// barrier's arrival count, a count of finished CTAs, one arrival counter per
-// (token, 256 output columns) (their combine runs when all of the token's
-// rows of those columns are written), one arrival counter per CTA and
-// work region (gate/up, down) for the pieces of a tile split between CTAs,
-// and one readiness counter per segment
-// (gate/up tiles finished).  Each returns to zero by the end of the launch
-// (the generation only ever grows).
+// Its counters follow the split-K counters in the status block: the
+// arrival counts of its two grid barriers (after the router; before the
+// combine), a count of finished CTAs, one arrival counter per CTA and work
+// region (gate/up, down) for the pieces of a tile split between CTAs, and
+// one readiness counter per segment (gate/up tiles finished).  Each returns
+// to zero by the end of the launch (the generation only ever grows).
 constexpr int kDecodeMaxT = 16;
 constexpr int kDecodeMaxCtas = 256;
-// words: +0 grid barrier arrivals, +2 finished CTAs
+// words: +0 first grid barrier's arrivals, +1 second's, +2 finished CTAs
 constexpr int kDecodeBarrierWord = kSplitCounterWord + 2 * kMaxSplitTiles;
 constexpr int kDecodePieceWord = kDecodeBarrierWord + 32;
 constexpr int kDecodeSegWord = kDecodePieceWord + 2 * kDecodeMaxCtas;
-constexpr int kDecodeTokWord = kDecodeSegWord + kMaxE + 16;  // [16][H/256 <= 64]
-constexpr size_t kStatusBlockBytes = (size_t)(kDecodeTokWord + kDecodeMaxT * 64) * 4;
+constexpr size_t kStatusBlockBytes = (size_t)(kDecodeSegWord + kMaxE + 16) * 4;
 
 // ------------------------------------------------------ argument checks --
 // Host-side validation shared by every entry point (api.cu, noalloc.cu):
