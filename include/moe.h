@@ -190,8 +190,9 @@ size_t moe_workspace_size(const moe_layer_desc_t *d);
 moe_status_t moe_workspace_layout(const moe_layer_desc_t *d, moe_workspace_layout_t *out);
 
 /* Clear the workspace's status block (async on stream): the status word and
- * the arrival counters the small-batch router and the split-K GEMM pieces
- * use (each returns to zero by itself when its kernel completes).  Call once
+ * the arrival counters the small-batch router, the split-K GEMM pieces and
+ * the persistent decode layer use (each returns to zero by itself when its
+ * kernel completes).  Call once
  * after allocating a workspace, and again after a call reported
  * MOE_ERR_TIMEOUT or MOE_ERR_CUDA. */
 moe_status_t moe_workspace_init(void *workspace, size_t ws_bytes, moe_stream_t stream);
